@@ -1,0 +1,497 @@
+"""Benchmark of the MLA tree-verify path on GB300.
+
+One step = one pass of the whole verify path on one batch of seeded
+synthetic input: the index/tree-mask builder, the split-KV partial kernel
+and the log-sum-exp combine, launched through the C ABI on one stream.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C]
+                    [--impl ours|reference] [--no-extras]
+
+The headline workload is the long-context verify (batch 1, 8 heads,
+prefix 184,728 keys, 64-node random tree, nsplit 64): the pages' longest
+measured context. Inputs are resident in HBM when the timed region starts;
+each timed step is preceded (outside its events) by a write of a buffer
+larger than L2, so every step reads the KV rows from HBM.
+
+--impl reference times the CPU fp64 oracle (the only reference that exists
+for this method) on the machine's host cores, on a bounded sample of the same
+workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import CONFIGS, make_config  # noqa: E402
+
+METRIC = "MLA tree-verify attention µs/call and KV GB/s vs HBM/tensor roofline (1×GB300)"
+UNIT = "us/call"
+ROW_BYTES = 576 * 2          # one latent row, bf16
+FLOPS_PER_PAIR = 2 * 576 + 2 * 512   # QK^T over 576 dims + PV over 512 dims
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ----------------------------------------------------------------- workload arithmetic
+def workload_figures(inp):
+    """Algorithmic bytes and flops of one verify call (each KV row read once;
+    flops count only visible (row, key) pairs)."""
+    L = inp.prefix_lens.astype(np.int64)
+    T, H, B = inp.T, inp.num_heads, inp.batch
+    keys = int(L.sum() + B * T)
+    kv_bytes = keys * ROW_BYTES
+    q_bytes = B * T * H * ROW_BYTES
+    out_bytes = B * T * H * (512 * 2 + 4)
+    idx_bytes = keys * 4
+    depth = np.zeros((B, T), dtype=np.int64)
+    for b in range(B):
+        for t in range(T):
+            p = int(inp.tree_parent[b, t])
+            depth[b, t] = depth[b, p] + 1 if p >= 0 else 0
+    vis = (L[:, None] + depth + 1).sum() * H  # visible keys summed over rows
+    flops = int(vis) * FLOPS_PER_PAIR
+    return dict(keys=keys, kv_bytes=kv_bytes, bytes=kv_bytes + q_bytes + out_bytes + idx_bytes,
+                flops=flops, visible_pairs=int(vis), rows=B * T * H)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def roofline_us(fig, peaks):
+    t_mem = fig["bytes"] / (peaks["hbm_gbs"] * 1e9) * 1e6
+    t_flop = fig["flops"] / (peaks["bf16_tflops"] * 1e12) * 1e6
+    return max(t_mem, t_flop), ("tensor" if t_flop > t_mem else "hbm"), t_mem, t_flop
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_speculative_decoding_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.startswith("partial"):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(config_idx):
+    """DRAM bytes per launch of the partial kernel from a committed ncu summary,
+    if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    e = t.get(str(config_idx))
+    if not e or e.get("kernel_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id=None):
+        self.samples = []
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in self.samples:
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, p[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- distributed helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value, world, backend_device=None):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=backend_device if backend_device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- CPU oracle timing
+def time_oracle(inp, target_s=10.0, max_rows=None):
+    """Oracle (as it stands) on a bounded row sample; returns (us per full call,
+    sample description, threads)."""
+    import oracle
+    ip, ix, _ = oracle.build_meta(inp)
+    threads = oracle.max_threads()
+    H, T = inp.num_heads, inp.T
+    L = inp.prefix_lens.astype(np.int64)
+    depth = np.zeros((inp.batch, T), dtype=np.int64)
+    for b in range(inp.batch):
+        for t in range(T):
+            p = int(inp.tree_parent[b, t])
+            depth[b, t] = depth[b, p] + 1 if p >= 0 else 0
+    vis_row = np.repeat((L[:, None] + depth + 1).reshape(-1), H)  # visible keys per row
+    total_vis = float(vis_row.sum())
+    rng = np.random.default_rng(1234)
+    order = rng.permutation(inp.num_rows)
+    # Calibrate on a few rows, then size the sample to ~target_s.
+    n0 = min(len(order), max(threads, 4))
+    t0 = time.perf_counter()
+    oracle.verify_attention(inp, ip, ix, rows=order[:n0])
+    dt0 = time.perf_counter() - t0
+    per_vis = dt0 / float(vis_row[order[:n0]].sum())
+    want = int(target_s / max(per_vis * float(vis_row.mean()), 1e-9))
+    n = max(n0, min(len(order), want if max_rows is None else min(want, max_rows)))
+    rows = order[:n]
+    t0 = time.perf_counter()
+    oracle.verify_attention(inp, ip, ix, rows=rows)
+    dt = time.perf_counter() - t0
+    us = dt * 1e6 * total_vis / float(vis_row[rows].sum())
+    return us, f"{n} of {inp.num_rows} query rows (random), scaled by visible keys", threads, dt
+
+
+# ----------------------------------------------------------------- GPU arm
+def run_ours(args):
+    import torch
+
+    import mla_speculative_decoding_gb300 as mv
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    mv.mla_verify_init(local)
+    peaks, peak_src = load_peaks()
+
+    idx = args.config
+    t0 = time.time()
+    inp = make_config(idx)
+    log(f"[bench] config {idx} generated in {time.time() - t0:.1f}s")
+    fig = workload_figures(inp)
+    d = mv.to_device(inp, device=dev)
+    stream = torch.cuda.current_stream()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    flush = torch.empty(max(4 * l2, 512 << 20), dtype=torch.uint8, device=dev)
+
+    def one_step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        d.build()
+        if ev is not None:
+            ev[1].record(stream)
+        d.partial(flags=args.flags)
+        if ev is not None:
+            ev[2].record(stream)
+        d.combine()
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        one_step()
+    torch.cuda.synchronize()
+    assert int(d.status.item()) == 0, "device status word set during warm-up"
+
+    gpu_id = None
+    try:
+        gpu_id = str(props.uuid)
+        if not gpu_id.startswith("GPU-"):
+            gpu_id = "GPU-" + gpu_id
+    except Exception:
+        gpu_id = None
+    clocks = ClockSampler(gpu_id)
+    time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.zero_()
+        one_step(evs[k])
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    step_us = [evs[k][0].elapsed_time(evs[k][3]) * 1e3 for k in range(args.steps)]
+    part_us = [evs[k][1].elapsed_time(evs[k][2]) * 1e3 for k in range(args.steps)]
+    build_us = [evs[k][0].elapsed_time(evs[k][1]) * 1e3 for k in range(args.steps)]
+    comb_us = [evs[k][2].elapsed_time(evs[k][3]) * 1e3 for k in range(args.steps)]
+    mean_step = statistics.mean(step_us)
+    mean_step_max = max_over_ranks(mean_step, world, dev if world > 1 else None)
+    value = mean_step_max / world  # whole-job: calls of all ranks over the slowest rank's time
+
+    # CUDA-graph replay of the same step (deployment mode on the pages).
+    graph_us = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            d.step()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            d.step()
+        ge = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for _ in range(3):
+            flush.zero_()
+            g.replay()
+        for k in range(args.steps):
+            flush.zero_()
+            ge[k][0].record(stream)
+            g.replay()
+            ge[k][1].record(stream)
+        torch.cuda.synchronize()
+        graph_us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in ge)
+    except Exception as e:  # reported, not hidden
+        log(f"[bench] graph replay failed: {e!r}")
+
+    # End to end through the public API with host buffers: per step, H2D of the
+    # step's inputs (queries, tree, prefix lengths, table rows, draft slots) from
+    # pinned memory, the verify path, D2H of out and lse. The KV pool and the
+    # req_to_token table are resident device state.
+    h_in = {k: getattr(d, k).cpu().pin_memory() for k in
+            ("q", "tree_parent", "prefix_lens", "req_pool_indices", "out_cache_loc")}
+    h_out = d.out.cpu().pin_memory()
+    h_lse = d.lse.cpu().pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+    e2e_us = []
+    for k in range(args.warmup + args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for name, ht in h_in.items():
+            getattr(d, name).copy_(ht, non_blocking=True)
+        d.step()
+        h_out.copy_(d.out, non_blocking=True)
+        h_lse.copy_(d.lse, non_blocking=True)
+        torch.cuda.synchronize()
+        if k >= args.warmup:
+            e2e_us.append((time.perf_counter() - t0) * 1e6)
+    e2e = max_over_ranks(statistics.mean(e2e_us), world, dev if world > 1 else None) / world
+    assert int(d.status.item()) == 0
+
+    roof_us, bound, t_mem, t_flop = roofline_us(fig, peaks)
+    part_mean = statistics.mean(part_us)
+    if bound == "tensor":
+        achieved = fig["flops"] / (part_mean * 1e-6) / 1e12
+        peak = peaks["bf16_tflops"]
+        runit = "TFLOP/s"
+    else:
+        achieved = fig["bytes"] / (part_mean * 1e-6) / 1e9
+        peak = peaks["hbm_gbs"]
+        runit = "GB/s"
+
+    result = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_step_max / 1e3, 6),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 q and latent KV; random trees; scattered slots)",
+        "config": {"workload": f"config{idx}:{CONFIGS[idx]['name']}", "batch": inp.batch,
+                   "heads": inp.num_heads, "prefix_lens": [int(x) for x in inp.prefix_lens][:8],
+                   "T": inp.T, "nsplit": inp.nsplit, "pool_slots": inp.pool_slots,
+                   "l2": "flushed before every timed step (buffer of 4x L2 written)",
+                   "parallelism": "replicas" if world > 1 else "single-gpu",
+                   "kernel": "simt" if args.flags else "default"},
+        "kv_gbps": round(fig["kv_bytes"] / (value * 1e-6) / 1e9, 1),
+        "roofline_frac": round(roof_us / value, 4),
+        "roofline_us": round(roof_us, 3),
+        "breakdown_us": {"build": round(statistics.mean(build_us), 3),
+                         "partial": round(part_mean, 3),
+                         "combine": round(statistics.mean(comb_us), 3)},
+        "graph_us": None if graph_us is None else round(graph_us, 3),
+        "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": runit,
+                     "frac": round(achieved / peak, 4), "traffic": ncu_traffic(idx),
+                     "kernel": "partial", "peak_source": f"{peak_src} (burst)",
+                     "algorithmic": {"bytes": fig["bytes"], "flops": fig["flops"]}},
+        "e2e": {"value": round(e2e, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 4),
+    }
+
+    if args.extras and rank == 0:
+        per = {}
+        for j in sorted(CONFIGS):
+            if j == idx:
+                continue
+            try:
+                per[j] = measure_config(j, mv, dev, flush, peaks, args)
+            except Exception as e:
+                per[j] = {"error": repr(e)}
+        per[idx] = {"us": round(value, 3), "roofline_us": round(roof_us, 3),
+                    "frac": round(roof_us / value, 4), "bound": bound}
+        result["per_config"] = {str(k): per[k] for k in sorted(per)}
+
+    if rank == 0 and world == 1 and args.cpu_baseline:
+        us, sample, threads, dt = time_oracle(inp, target_s=args.cpu_seconds)
+        result["cpu_baseline"] = {"value": round(us, 1), "unit": UNIT, "cores": threads,
+                                  "kind": "oracle", "sample": sample,
+                                  "sample_seconds": round(dt, 2)}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def measure_config(j, mv, dev, flush, peaks, args, steps=10):
+    import torch
+    inp = make_config(j)
+    fig = workload_figures(inp)
+    d = mv.to_device(inp, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        flush.zero_()
+        d.step()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for k in range(steps):
+        flush.zero_()
+        ev[k][0].record(stream)
+        d.step()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    us = statistics.mean(a.elapsed_time(b) * 1e3 for a, b in ev)
+    roof, bound, _, _ = roofline_us(fig, peaks)
+    ok = int(d.status.item()) == 0
+    del d
+    torch.cuda.empty_cache()
+    return {"us": round(us, 3), "roofline_us": round(roof, 3), "frac": round(roof / us, 4),
+            "bound": bound, "kv_gbps": round(fig["kv_bytes"] / (us * 1e-6) / 1e9, 1),
+            "status_ok": ok}
+
+
+# ----------------------------------------------------------------- reference arm
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return  # the CPU oracle runs once, on rank 0
+    idx = args.config
+    inp = make_config(idx)
+    per_step = []
+    sample = threads = None
+    # Each step: the oracle on a bounded random row sample (~cpu_step_s of CPU
+    # work), scaled to the whole call by visible keys.
+    for k in range(args.warmup + args.steps):
+        us, sample, threads, _ = time_oracle(inp, target_s=args.cpu_step_s)
+        if k >= args.warmup:
+            per_step.append(us)
+    value = statistics.mean(per_step)
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(value / 1e3, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"config{idx}:{CONFIGS[idx]['name']}", "batch": inp.batch,
+                   "heads": inp.num_heads, "T": inp.T, "nsplit": inp.nsplit},
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=4, choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--simt", action="store_true", help="force the CUDA-core partial kernel")
+    ap.add_argument("--no-extras", dest="extras", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-step-s", type=float, default=4.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    args.flags = 1 if args.simt else 0
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

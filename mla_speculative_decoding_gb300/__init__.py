@@ -1,0 +1,37 @@
+"""MLA tree-verify attention for speculative decoding on GB300 (sm_103a).
+
+The product is the C-ABI library libmlaverify.so (include/mla_verify.h):
+an index/tree-mask builder kernel, a split-KV partial attention kernel
+(tcgen05/TMEM tensor cores, with a CUDA-core path for other shapes) and a
+log-sum-exp combine kernel. This package is its thin Python binding.
+"""
+
+from .binding import (  # noqa: F401
+    D_QK,
+    D_V,
+    MLA_PARTIAL_SIMT,
+    MLA_STATUS_BAD_INDPTR,
+    MLA_STATUS_BAD_PARENT,
+    MLA_STATUS_BAD_PREFIX,
+    MLA_STATUS_BAD_SLOT,
+    MLA_STATUS_CAPACITY,
+    MLA_STATUS_EMPTY_ROW,
+    MlaError,
+    alloc_workspace,
+    library_path,
+    load,
+    mla_build_verify_meta,
+    mla_verify_attention,
+    mla_verify_attention_anc,
+    mla_verify_combine,
+    mla_verify_init,
+    mla_verify_partial,
+    mla_verify_reset_status,
+    mla_verify_status_offset,
+    mla_verify_version,
+    mla_verify_workspace_bytes,
+    partials,
+    status_string,
+    status_word,
+)
+from .device import DeviceInputs, to_device  # noqa: F401

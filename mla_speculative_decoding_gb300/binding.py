@@ -1,0 +1,245 @@
+"""Thin ctypes binding of libmlaverify.so (include/mla_verify.h).
+
+Argument marshalling only: every step of the verify path runs in the CUDA
+kernels of the library. The functions keep the C names; tensors are torch
+CUDA tensors (PyTorch provides device memory and streams), sizes are
+taken from their shapes, and a non-zero C status raises MlaError. If the
+library has not been built the import of a function fails loudly; there is
+no CPU fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+MLA_OK = 0
+MLA_ERR_INVALID_ARG = -1
+MLA_ERR_UNSUPPORTED = -2
+MLA_ERR_WORKSPACE_TOO_SMALL = -3
+MLA_ERR_CUDA = -4
+MLA_ERR_NOT_INITIALIZED = -5
+
+MLA_STATUS_BAD_SLOT = 0x1
+MLA_STATUS_BAD_PARENT = 0x2
+MLA_STATUS_BAD_INDPTR = 0x4
+MLA_STATUS_CAPACITY = 0x8
+MLA_STATUS_BAD_PREFIX = 0x10
+MLA_STATUS_EMPTY_ROW = 0x20
+
+MLA_PARTIAL_SIMT = 0x1
+D_QK = 576
+D_V = 512
+
+_c_int = ctypes.c_int
+_c_i64 = ctypes.c_int64
+_c_size = ctypes.c_size_t
+_c_f32 = ctypes.c_float
+_vp = ctypes.c_void_p
+
+_SIGS = {
+    "mla_verify_status_string": (ctypes.c_char_p, [_c_int]),
+    "mla_verify_version": (_c_int, []),
+    "mla_verify_init": (_c_int, [_c_int]),
+    "mla_verify_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "mla_verify_status_offset": (_c_size, []),
+    "mla_verify_reset_status": (_c_int, [_vp, _vp]),
+    "mla_build_verify_meta": (_c_int, [_vp, _c_i64, _c_i64, _vp, _vp, _vp, _vp, _c_int, _c_int,
+                                       _c_i64, _vp, _vp, _vp, _vp, _vp]),
+    "mla_verify_attention": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _vp, _vp,
+                                      _vp, _c_int, _c_int, _c_i64, _c_f32, _c_size, _vp]),
+    "mla_verify_attention_anc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _vp, _vp,
+                                          _vp, _c_int, _c_int, _c_i64, _c_f32, _c_size, _vp]),
+    "mla_verify_partial": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _vp,
+                                    _c_int, _c_int, _c_i64, _c_f32, _c_size, ctypes.c_uint, _vp]),
+    "mla_verify_combine": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _c_size,
+                                    _vp]),
+}
+
+_LIB = None
+
+
+class MlaError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__(f"{fn} failed: {status_string(code)} ({code})")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libmlaverify.so (building it in-tree first if it is missing or stale)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if build_if_missing and not _build.up_to_date():
+        _build.build_library()
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"libmlaverify.so not built ({path}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def _check(fn, code):
+    if code != MLA_OK:
+        raise MlaError(fn, code)
+
+
+def status_string(code: int) -> str:
+    return load().mla_verify_status_string(int(code)).decode()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _p(t):
+    """Device pointer of a torch tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _want(t, dtype, name):
+    if t is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+
+
+def mla_verify_version() -> int:
+    return int(load().mla_verify_version())
+
+
+def mla_verify_init(device: int = None) -> None:
+    if device is None:
+        device = torch.cuda.current_device()
+    _check("mla_verify_init", load().mla_verify_init(int(device)))
+
+
+def mla_verify_workspace_bytes(batch: int, T: int, num_heads: int, nsplit: int) -> int:
+    return int(load().mla_verify_workspace_bytes(batch, T, num_heads, nsplit))
+
+
+def mla_verify_status_offset() -> int:
+    return int(load().mla_verify_status_offset())
+
+
+def alloc_workspace(batch, T, num_heads, nsplit, device="cuda"):
+    n = mla_verify_workspace_bytes(batch, T, num_heads, nsplit)
+    if n == 0:
+        raise ValueError("shape outside the library's limits")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def status_word(workspace: torch.Tensor) -> torch.Tensor:
+    """int32 view of the device status word inside a workspace."""
+    off = mla_verify_status_offset()
+    return workspace[off:off + 4].view(torch.int32)
+
+
+def mla_verify_reset_status(status: torch.Tensor, stream=None) -> None:
+    _check("mla_verify_reset_status", load().mla_verify_reset_status(_p(status), _stream(stream)))
+
+
+def mla_build_verify_meta(req_to_token, req_pool_indices, prefix_lens, out_cache_loc, tree_parent,
+                          kv_indptr, kv_indices, anc_mask, status, stream=None) -> None:
+    """Device index/mask builder; capacity = kv_indices.numel()."""
+    for t, n in ((req_to_token, "req_to_token"), (req_pool_indices, "req_pool_indices"),
+                 (prefix_lens, "prefix_lens"), (out_cache_loc, "out_cache_loc"),
+                 (tree_parent, "tree_parent"), (kv_indptr, "kv_indptr"),
+                 (kv_indices, "kv_indices"), (status, "status")):
+        _want(t, torch.int32, n)
+    _want(anc_mask, torch.int64, "anc_mask")  # uint64 bits held in an int64 tensor
+    B, T = tree_parent.shape
+    rc = load().mla_build_verify_meta(
+        _p(req_to_token), req_to_token.shape[1], req_to_token.shape[0], _p(req_pool_indices),
+        _p(prefix_lens), _p(out_cache_loc), _p(tree_parent), B, T, kv_indices.numel(),
+        _p(kv_indptr), _p(kv_indices), _p(anc_mask), _p(status), _stream(stream))
+    _check("mla_build_verify_meta", rc)
+
+
+def _attn_shapes(q, kv_pool, T, out, lse):
+    _want(q, torch.bfloat16, "q")
+    _want(kv_pool, torch.bfloat16, "kv_pool")
+    if q.dim() != 3 or q.shape[2] != D_QK or q.shape[0] % T:
+        raise ValueError("q must be [batch*T, H, 576]")
+    if kv_pool.dim() != 2 or kv_pool.shape[1] != D_QK:
+        raise ValueError("kv_pool must be [pool_slots, 576]")
+    batch, H = q.shape[0] // T, q.shape[1]
+    if out is not None:
+        _want(out, torch.bfloat16, "out")
+        if tuple(out.shape) != (batch * T, H, D_V):
+            raise ValueError("out must be [batch*T, H, 512]")
+    if lse is not None:
+        _want(lse, torch.float32, "lse")
+        if tuple(lse.shape) != (batch * T, H):
+            raise ValueError("lse must be [batch*T, H]")
+    return batch, H
+
+
+def mla_verify_attention(q, kv_pool, kv_indices, kv_indptr, prefix_lens, tree_parent, T, nsplit,
+                         workspace, out, lse, softmax_scale, stream=None) -> None:
+    batch, H = _attn_shapes(q, kv_pool, T, out, lse)
+    rc = load().mla_verify_attention(
+        _p(q), _p(kv_pool), _p(kv_indices), _p(kv_indptr), _p(prefix_lens), _p(tree_parent), T,
+        nsplit, _p(workspace), _p(out), _p(lse), batch, H, kv_pool.shape[0], float(softmax_scale),
+        workspace.numel(), _stream(stream))
+    _check("mla_verify_attention", rc)
+
+
+def mla_verify_attention_anc(q, kv_pool, kv_indices, kv_indptr, prefix_lens, anc_mask, T, nsplit,
+                             workspace, out, lse, softmax_scale, stream=None) -> None:
+    batch, H = _attn_shapes(q, kv_pool, T, out, lse)
+    rc = load().mla_verify_attention_anc(
+        _p(q), _p(kv_pool), _p(kv_indices), _p(kv_indptr), _p(prefix_lens), _p(anc_mask), T,
+        nsplit, _p(workspace), _p(out), _p(lse), batch, H, kv_pool.shape[0], float(softmax_scale),
+        workspace.numel(), _stream(stream))
+    _check("mla_verify_attention_anc", rc)
+
+
+def mla_verify_partial(q, kv_pool, kv_indices, kv_indptr, prefix_lens, tree_parent, anc_mask, T,
+                       nsplit, workspace, softmax_scale, flags=0, stream=None) -> None:
+    batch, H = _attn_shapes(q, kv_pool, T, None, None)
+    rc = load().mla_verify_partial(
+        _p(q), _p(kv_pool), _p(kv_indices), _p(kv_indptr), _p(prefix_lens), _p(tree_parent),
+        _p(anc_mask), T, nsplit, _p(workspace), batch, H, kv_pool.shape[0], float(softmax_scale),
+        workspace.numel(), int(flags), _stream(stream))
+    _check("mla_verify_partial", rc)
+
+
+def mla_verify_combine(workspace, batch, T, num_heads, nsplit, out, lse, stream=None) -> None:
+    rc = load().mla_verify_combine(_p(workspace), batch, T, num_heads, nsplit, _p(out), _p(lse),
+                                   workspace.numel(), _stream(stream))
+    _check("mla_verify_combine", rc)
+
+
+def partials(workspace, batch, T, num_heads, nsplit):
+    """Views (lse_part [rows, nsplit], o_part [rows, nsplit, 512]) into a workspace."""
+    rows = batch * T * num_heads
+    n = rows * nsplit
+    lse_off = 256
+    o_off = lse_off + ((n * 4 + 255) // 256) * 256
+    lse_part = workspace[lse_off:lse_off + n * 4].view(torch.float32).view(rows, nsplit)
+    o_part = workspace[o_off:o_off + n * 512 * 4].view(torch.float32).view(rows, nsplit, 512)
+    return lse_part, o_part

@@ -1,0 +1,113 @@
+// Shared definitions of the MLA tree-verify attention library (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mla_verify.h"
+
+#define MLAV_API extern "C" __attribute__((visibility("default")))
+
+namespace mlav {
+
+constexpr int kDqk = 576;  // 512 latent + 64 RoPE dims
+constexpr int kDv = 512;   // V = first 512 dims of the latent row
+constexpr size_t kWsHeader = 256;  // status word + padding
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__host__ __device__ constexpr size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace layout: [header 256 B | lse_part fp32 [rows*nsplit] padded to
+// 256 B | o_part fp32 [rows*nsplit][512]].
+struct WsLayout {
+    size_t lse_off;
+    size_t o_off;
+    size_t total;
+};
+
+__host__ __device__ inline WsLayout ws_layout(int batch, int T, int H, int nsplit) {
+    const size_t parts = (size_t)batch * T * H * nsplit;
+    WsLayout w;
+    w.lse_off = kWsHeader;
+    w.o_off = w.lse_off + round_up(parts * sizeof(float), 256);
+    w.total = w.o_off + parts * kDv * sizeof(float);
+    return w;
+}
+
+// Key range of split s of a request with K keys: contiguous ranges of
+// ceil(K / nsplit) keys; trailing splits may be empty.
+__host__ __device__ inline void split_range(int K, int nsplit, int s, int& beg, int& end) {
+    const int chunk = (K + nsplit - 1) / nsplit;
+    beg = min(K, s * chunk);
+    end = min(K, beg + chunk);
+}
+
+__device__ __forceinline__ void status_or(int32_t* st, int bits) {
+    if (st != nullptr && bits != 0) atomicOr(st, bits);
+}
+
+// Ancestor-or-self masks of one request's tree, built in shared memory from
+// parent links (parents precede children). A node whose parent is invalid is
+// treated as a root and flagged. Called by one thread.
+__device__ inline int build_anc_serial(const int32_t* par, int T, uint64_t* anc) {
+    int bad = 0;
+    for (int t = 0; t < T; ++t) {
+        const int p = par[t];
+        const bool ok = (t == 0) ? (p == -1) : (p >= 0 && p < t);
+        if (!ok) bad = MLA_STATUS_BAD_PARENT;
+        anc[t] = ((t > 0 && ok) ? anc[p] : 0ull) | (1ull << t);
+    }
+    return bad;
+}
+
+struct PartialArgs;
+
+// Internal launchers (defined in the kernel translation units).
+struct PartialArgs {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* kv;
+    const int32_t* kv_indices;
+    const int32_t* kv_indptr;
+    const int32_t* prefix_lens;
+    const int32_t* tree_parent;  // exactly one of tree_parent / anc_mask
+    const uint64_t* anc_mask;
+    float* lse_part;
+    float* o_part;
+    int32_t* status;
+    int batch, T, H, nsplit;
+    int64_t pool_slots;
+    float scale_log2;  // softmax_scale * log2(e)
+};
+
+// Prefix length and key count of request b, made consistent: a negative
+// prefix counts as 0, and the key count is clamped to [0, L_b + T] (surplus
+// keys are ignored, missing ones are absent). Returns the status bits.
+__device__ inline int request_keys(const PartialArgs& a, int b, int& Lb, int& K) {
+    int bad = 0;
+    Lb = a.prefix_lens[b];
+    if (Lb < 0) {
+        Lb = 0;
+        bad |= MLA_STATUS_BAD_INDPTR;
+    }
+    K = a.kv_indptr[b + 1] - a.kv_indptr[b];
+    if (K != Lb + a.T) bad |= MLA_STATUS_BAD_INDPTR;
+    K = max(0, min(K, Lb + a.T));
+    return bad;
+}
+
+cudaError_t launch_partial_simt(const PartialArgs& a, cudaStream_t stream);
+cudaError_t setup_partial_simt();
+
+cudaError_t launch_combine(const float* lse_part, const float* o_part, int rows, int nsplit,
+                           __nv_bfloat16* out, float* lse, int32_t* status, cudaStream_t stream);
+
+cudaError_t launch_build_meta(const int32_t* req_to_token, int64_t stride, int64_t rows,
+                              const int32_t* req_pool_indices, const int32_t* prefix_lens,
+                              const int32_t* out_cache_loc, const int32_t* tree_parent,
+                              int batch, int T, int64_t capacity, int32_t* kv_indptr,
+                              int32_t* kv_indices, uint64_t* anc, int32_t* status,
+                              cudaStream_t stream);
+
+}  // namespace mlav

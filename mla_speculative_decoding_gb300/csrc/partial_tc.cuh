@@ -1,0 +1,13 @@
+// Tensor-core (tcgen05 / TMEM) split-KV partial attention: interface.
+#pragma once
+
+#include "common.cuh"
+
+namespace mlav {
+
+// True when the tensor-core kernel handles this shape.
+bool partial_tc_supported(const PartialArgs& a);
+cudaError_t launch_partial_tc(const PartialArgs& a, int sm_count, cudaStream_t stream);
+cudaError_t setup_partial_tc();
+
+}  // namespace mlav

@@ -1,0 +1,101 @@
+"""GPU verify attention vs the CPU fp64 oracle, element by element.
+
+Every test calls the C ABI (through the thin binding) on seeded inputs and
+compares with the oracle run on the same inputs. Both kernel paths are
+covered: the default (tensor-core where supported) and the CUDA-core one.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import mla_speculative_decoding_gb300 as mv
+from tests.gpu_util import config_cached, compare, host_out, oracle_ref, run_gpu, sample_rows, status
+from workloads import make_config, make_inputs
+
+pytestmark = pytest.mark.gpu
+PATHS = [0, mv.MLA_PARTIAL_SIMT]
+
+
+@pytest.mark.parametrize("flags", PATHS)
+@pytest.mark.parametrize("idx", [1, 2, 3])
+def test_configs_full(idx, flags):
+    inp = config_cached(idx)
+    d = run_gpu(inp, flags=flags)
+    assert status(d) == 0
+    out, lse = host_out(d)
+    ref_out, ref_lse = oracle_ref(inp)
+    compare(out, lse, ref_out, ref_lse, f"config {idx} flags {flags}")
+
+
+@pytest.mark.parametrize("flags", PATHS)
+@pytest.mark.parametrize("idx", [4, 5])
+def test_configs_sampled_rows(idx, flags):
+    """Full-size long/batched workloads in the benchmark's launch configuration;
+    the oracle computes a sample of rows one by one."""
+    inp = config_cached(idx)
+    d = run_gpu(inp, flags=flags)
+    assert status(d) == 0
+    out, lse = host_out(d)
+    rows = sample_rows(inp, per_request=12 if inp.batch == 1 else 6, seed=idx)
+    ref_out, ref_lse = oracle_ref(inp, rows=rows)
+    compare(out[rows], lse[rows], ref_out, ref_lse, f"config {idx} flags {flags}")
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+
+
+def test_config3_contiguous_placement():
+    inp = config_cached(3, placement="contiguous")
+    d = run_gpu(inp)
+    out, lse = host_out(d)
+    ref_out, ref_lse = oracle_ref(inp)
+    compare(out, lse, ref_out, ref_lse, "config 3 contiguous")
+
+
+CASES = [
+    # (batch, heads, prefix, T, tree, nsplit)
+    (1, 8, [1000], 16, "random", 7),        # ragged tail, odd split count
+    (2, 16, [333, 2049], 8, "random", 5),   # ragged batch, 128 rows per request
+    (1, 128, [700], 1, "chain", 3),         # maximum heads, single token
+    (1, 2, [0], 64, "chain", 4),            # no prefix, maximum tree (causal)
+    (3, 8, [0, 129, 5], 16, "star", 64),    # more splits than keys in some requests
+    (1, 8, [300], 16, "random", 128),       # maximum split count
+    (4, 32, [64, 0, 1, 4000], 4, "random", 16),
+]
+
+
+@pytest.mark.parametrize("flags", PATHS)
+@pytest.mark.parametrize("case", CASES, ids=[f"c{i}" for i in range(len(CASES))])
+def test_edge_cases(case, flags):
+    B, H, L, T, tree, ns = case
+    inp = make_inputs(batch=B, num_heads=H, prefix=L, T=T, tree=tree, pool_slots=16384,
+                      nsplit=ns, seed=sum(L) + T)
+    d = run_gpu(inp, flags=flags)
+    assert status(d) == 0
+    out, lse = host_out(d)
+    ref_out, ref_lse = oracle_ref(inp)
+    compare(out, lse, ref_out, ref_lse, f"case {case} flags {flags}")
+
+
+@pytest.mark.parametrize("flags", PATHS)
+def test_single_key_returns_v_bit_exact(flags):
+    """L = 0, T = 1: every head's output is the token's own V row, bit for bit."""
+    inp = make_inputs(batch=4, num_heads=8, prefix=[0] * 4, T=1, tree="chain", pool_slots=256,
+                      nsplit=4, seed=3)
+    d = run_gpu(inp, flags=flags)
+    got = d.out.cpu().view(torch.int16).numpy().view(np.uint16)
+    for b in range(4):
+        v = inp.kv_pool[inp.out_cache_loc[b], :512]
+        for h in range(8):
+            assert np.array_equal(got[b, h], v)
+    _, ref_lse = oracle_ref(inp)
+    _, lse = host_out(d)
+    assert np.abs(lse - ref_lse).max() <= 1e-3
+
+
+def test_zero_query_closed_form_on_gpu():
+    inp = make_inputs(batch=2, num_heads=4, prefix=[500, 37], T=8, tree="random",
+                      pool_slots=4096, nsplit=8, seed=4, q_mode="zero")
+    d = run_gpu(inp)
+    out, lse = host_out(d)
+    ref_out, ref_lse = oracle_ref(inp)
+    compare(out, lse, ref_out, ref_lse, "q = 0")
