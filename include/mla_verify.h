@@ -216,6 +216,43 @@ int mla_verify_partial(const void *q, const void *kv_pool, const int32_t *kv_ind
 int mla_verify_combine(const void *workspace, int batch, int T, int num_heads, int nsplit,
                        void *out, float *lse, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * Allocation-free verify call. The pages have no counterpart to this entry
+ * point; it exists for callers that cannot allocate device memory where
+ * they run the verify step (for example a plugin enqueue callback inside an
+ * inference runtime that owns all device memory, or code running while the
+ * application's allocator is locked), and so cannot provide the workspace
+ * that mla_verify_attention needs.
+ *
+ * Same inputs, outputs and results as mla_verify_attention, but the
+ * per-split partials live in one fixed scratch area in device global memory
+ * that the library reserves on every GPU that loads it, for the life of the
+ * process: mla_verify_noalloc_scratch_bytes() bytes (32 MiB).
+ *   - Shapes whose mla_verify_workspace_bytes(batch, T, num_heads, nsplit)
+ *     exceeds that size are rejected with MLA_ERR_WORKSPACE_TOO_SMALL before
+ *     anything is launched.
+ *   - Nothing is allocated: no cudaMalloc/cudaFree, no allocating library
+ *     call. The call enqueues a 4-byte memset (clearing the area's status
+ *     word), the two kernels, and, if `status` is not NULL, a 4-byte
+ *     device-to-device copy of this call's status bits into *status
+ *     (overwriting it; NULL discards them).
+ *   - The first call on each device looks up the area's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     outside stream capture (inside capture it returns
+ *     MLA_ERR_NOT_INITIALIZED).
+ *   - All calls share the one area and it keeps the previous call's
+ *     contents: calls whose GPU work overlaps on the same device (other
+ *     streams, other host threads) race on it and must be serialised by the
+ *     caller.
+ */
+size_t mla_verify_noalloc_scratch_bytes(void);
+
+int mla_verify_attention_noalloc(const void *q, const void *kv_pool, const int32_t *kv_indices,
+                                 const int32_t *kv_indptr, const int32_t *prefix_lens,
+                                 const int32_t *tree_parent, int T, int nsplit, void *out,
+                                 float *lse, int batch, int num_heads, int64_t pool_slots,
+                                 float softmax_scale, int32_t *status, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

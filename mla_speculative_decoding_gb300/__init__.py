@@ -23,8 +23,10 @@ from .binding import (  # noqa: F401
     mla_build_verify_meta,
     mla_verify_attention,
     mla_verify_attention_anc,
+    mla_verify_attention_noalloc,
     mla_verify_combine,
     mla_verify_init,
+    mla_verify_noalloc_scratch_bytes,
     mla_verify_partial,
     mla_verify_reset_status,
     mla_verify_status_offset,

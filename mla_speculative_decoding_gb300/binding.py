@@ -58,6 +58,9 @@ _SIGS = {
                                     _c_int, _c_int, _c_i64, _c_f32, _c_size, ctypes.c_uint, _vp]),
     "mla_verify_combine": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _c_size,
                                     _vp]),
+    "mla_verify_noalloc_scratch_bytes": (_c_size, []),
+    "mla_verify_attention_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _vp,
+                                              _vp, _c_int, _c_int, _c_i64, _c_f32, _vp, _vp]),
 }
 
 _LIB = None
@@ -243,3 +246,21 @@ def partials(workspace, batch, T, num_heads, nsplit):
     lse_part = workspace[lse_off:lse_off + n * 4].view(torch.float32).view(rows, nsplit)
     o_part = workspace[o_off:o_off + n * 512 * 4].view(torch.float32).view(rows, nsplit, 512)
     return lse_part, o_part
+
+
+def mla_verify_noalloc_scratch_bytes() -> int:
+    return int(load().mla_verify_noalloc_scratch_bytes())
+
+
+def mla_verify_attention_noalloc(q, kv_pool, kv_indices, kv_indptr, prefix_lens, tree_parent, T,
+                                 nsplit, out, lse, softmax_scale, status=None,
+                                 stream=None) -> None:
+    """Verify call without a workspace: the partials use the library's fixed
+    device scratch area (for callers that cannot allocate device memory)."""
+    batch, H = _attn_shapes(q, kv_pool, T, out, lse)
+    _want(status, torch.int32, "status")
+    rc = load().mla_verify_attention_noalloc(
+        _p(q), _p(kv_pool), _p(kv_indices), _p(kv_indptr), _p(prefix_lens), _p(tree_parent), T,
+        nsplit, _p(out), _p(lse), batch, H, kv_pool.shape[0], float(softmax_scale), _p(status),
+        _stream(stream))
+    _check("mla_verify_attention_noalloc", rc)
