@@ -18,6 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libmlaverify.so")
+SELFTEST_SRC = os.path.join(CSRC, "selftest", "umma_selftest.cu")
+SELFTEST_LIB = os.path.join(OUT_DIR, "libmlaselftest.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 
@@ -85,5 +87,23 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+def build_selftest(force: bool = False) -> str:
+    """Test-only library with the tcgen05 layout self-test (shares tc_ptx.cuh)."""
+    deps = [SELFTEST_SRC, os.path.join(CSRC, "tc_ptx.cuh"), os.path.abspath(__file__)]
+    if (not force and os.path.exists(SELFTEST_LIB)
+            and all(os.path.getmtime(d) <= os.path.getmtime(SELFTEST_LIB) for d in deps)):
+        return SELFTEST_LIB
+    os.makedirs(OUT_DIR, exist_ok=True)
+    tmp = SELFTEST_LIB + f".tmp{os.getpid()}"
+    cmd = [_nvcc()] + ARCH + ["-O2", "-std=c++17", "-I", CSRC, "-Xcompiler",
+                              "-fPIC,-fvisibility=hidden", "-shared", SELFTEST_SRC, "-o", tmp]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("selftest build failed:\n" + r.stdout + r.stderr)
+    os.replace(tmp, SELFTEST_LIB)
+    return SELFTEST_LIB
+
+
 if __name__ == "__main__":
     print(build_library(force="--force" in sys.argv, verbose=True))
+    print(build_selftest(force="--force" in sys.argv))

@@ -1,0 +1,60 @@
+"""tcgen05 building blocks (descriptors, swizzled layouts, TMEM operand,
+MMA, commit, TMEM loads) checked on one tile against a float64 matmul. The
+self-test library uses the same inline-PTX header as the tensor-core
+partial kernel."""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from mla_speculative_decoding_gb300 import build as B
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def probe():
+    lib = ctypes.CDLL(B.build_selftest())
+    f = lib.mlav_umma_probe
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p]
+    return f
+
+
+def _run(probe, mode, N, variant=0, seed=0):
+    g = torch.Generator().manual_seed(seed)
+    A = torch.randn(128, 64, generator=g).to(torch.bfloat16)
+    Bm = torch.randn(N, 64, generator=g).to(torch.bfloat16) if mode in (0, 1) else \
+        torch.randn(64, N, generator=g).to(torch.bfloat16)
+    dA, dB = A.cuda(), Bm.cuda()
+    D = torch.full((128, N), float("nan"), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = probe(dA.data_ptr(), dB.data_ptr(), D.data_ptr(), N, mode, variant, err.data_ptr())
+    assert rc == 0, f"probe launch failed: {rc}"
+    assert int(err.item()) == 0, "probe wait timed out"
+    a = A.double()
+    ref = a @ (Bm.double().T if mode in (0, 1) else Bm.double())
+    return D.cpu().double(), ref
+
+
+@pytest.mark.parametrize("N", [32, 64, 128, 256])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_kmajor_b(probe, mode, N):
+    got, ref = _run(probe, mode, N)
+    torch.testing.assert_close(got, ref, rtol=1e-4, atol=1e-3)
+
+
+@pytest.mark.parametrize("N", [64, 128, 256])
+@pytest.mark.parametrize("mode", [2, 3])
+def test_mnmajor_b(probe, mode, N):
+    """MN-major B (the V operand): one of the two stride assignments must be
+    right; the kernel uses variant 0 (atom-column stride in the leading
+    field)."""
+    got, ref = _run(probe, mode, N, variant=0)
+    ok0 = torch.allclose(got, ref, rtol=1e-4, atol=1e-3)
+    got1, _ = _run(probe, mode, N, variant=1)
+    ok1 = torch.allclose(got1, ref, rtol=1e-4, atol=1e-3)
+    print(f"mode {mode} N {N}: variant0 {ok0} variant1 {ok1}")
+    assert ok0, f"variant 0 wrong (variant 1 {'right' if ok1 else 'also wrong'})"
