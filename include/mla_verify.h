@@ -95,6 +95,8 @@ typedef enum {
                                       req_pool_indices[b] outside [0, rows): clamped */
 #define MLA_STATUS_EMPTY_ROW 0x20  /* a query row had no valid visible key: out row = 0,
                                       lse = -inf */
+#define MLA_STATUS_TIMEOUT 0x40    /* a bounded wait inside a kernel gave up (never expected);
+                                      that call's outputs are invalid */
 
 /* Human-readable name of an mla_status_t (static string, never NULL). */
 const char *mla_verify_status_string(int status);

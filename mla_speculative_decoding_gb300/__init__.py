@@ -16,6 +16,7 @@ from .binding import (  # noqa: F401
     MLA_STATUS_BAD_SLOT,
     MLA_STATUS_CAPACITY,
     MLA_STATUS_EMPTY_ROW,
+    MLA_STATUS_TIMEOUT,
     MlaError,
     alloc_workspace,
     library_path,

@@ -30,6 +30,7 @@ MLA_STATUS_BAD_INDPTR = 0x4
 MLA_STATUS_CAPACITY = 0x8
 MLA_STATUS_BAD_PREFIX = 0x10
 MLA_STATUS_EMPTY_ROW = 0x20
+MLA_STATUS_TIMEOUT = 0x40
 
 MLA_PARTIAL_SIMT = 0x1
 D_QK = 576

@@ -142,3 +142,76 @@ extern "C" __attribute__((visibility("default"))) int mlav_umma_probe(
     if (e != cudaSuccess) return (int)e;
     return (int)cudaDeviceSynchronize();
 }
+
+namespace {
+
+// Throughput probe: one thread issues `reps` rounds of MMAs (M = 128, K = 16,
+// N = n) cycling over `nacc` independent accumulators, with A from shared
+// memory or TMEM; reports the cycles from the first issue to the commit.
+__global__ void __launch_bounds__(128, 1)
+mma_rate_kernel(int N, int a_tmem, int reps, int nacc, int overwrite, long long* out, int* err) {
+    extern __shared__ __align__(1024) unsigned char raw[];
+    unsigned char* base = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+    ProbeSmem& sm = *reinterpret_cast<ProbeSmem*>(base);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    for (int i = tid; i < (int)(sizeof(sm.a) / 16); i += 128)
+        reinterpret_cast<uint4*>(sm.a)[i] = make_uint4(0x3f803f80u, 0, 0, 0);
+    for (int i = tid; i < (int)(sizeof(sm.b) / 16); i += 128)
+        reinterpret_cast<uint4*>(sm.b)[i] = make_uint4(0x3f803f80u, 0, 0, 0);
+    fence_proxy_async_smem();
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&sm.tmem), 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(smem_u32(&sm.bar), 1);
+        sm.abort_flag = 0;
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t taddr = sm.tmem;
+    if (tid == 0) {
+        const uint32_t idesc = make_idesc_bf16(kM, N, false, false);
+        const uint32_t a0 = smem_u32(sm.a), b0 = smem_u32(sm.b);
+        const long long t0 = clock64();
+        for (int r = 0; r < reps; ++r) {
+            const int ks = r & 3;
+            const uint64_t bd = make_sdesc(b0 + ks * 32, 16, 1024, kSwizzle128B);
+            const uint64_t ad = make_sdesc(a0 + ks * 32, 16, 1024, kSwizzle128B);
+            for (int c = 0; c < nacc; ++c) {
+                const uint32_t acc = overwrite ? 0u : 1u;
+                if (a_tmem)
+                    mma_ts(taddr + c * N, taddr + kAcol + ks * 8, bd, idesc, acc);
+                else
+                    mma_ss(taddr + c * N, ad, bd, idesc, acc);
+            }
+        }
+        mma_commit(smem_u32(&sm.bar));
+        const bool ok = mbar_wait(smem_u32(&sm.bar), 0, &sm.abort_flag);
+        const long long t1 = clock64();
+        out[0] = t1 - t0;
+        if (!ok) atomicExch(err, 1);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(taddr, 512);
+}
+
+}  // namespace
+
+extern "C" __attribute__((visibility("default"))) int mlav_mma_rate(int N, int a_tmem, int reps,
+                                                                    int nacc, int overwrite,
+                                                                    long long* out, int* err) {
+    if (N < 16 || N > 256 || (N % 16) != 0 || nacc < 1 || reps < 1) return -1;
+    if (N * nacc > (a_tmem ? 256 : 512)) return -1;
+    cudaError_t e = cudaFuncSetAttribute(mma_rate_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)sizeof(ProbeSmem) + 1024);
+    if (e != cudaSuccess) return (int)e;
+    mma_rate_kernel<<<1, 128, sizeof(ProbeSmem) + 1024>>>(N, a_tmem, reps, nacc, overwrite, out, err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return (int)e;
+    return (int)cudaDeviceSynchronize();
+}

@@ -99,3 +99,25 @@ def test_zero_query_closed_form_on_gpu():
     out, lse = host_out(d)
     ref_out, ref_lse = oracle_ref(inp)
     compare(out, lse, ref_out, ref_lse, "q = 0")
+
+
+@pytest.mark.parametrize("flags", PATHS)
+def test_growing_scores_force_rescaling(flags):
+    """Scores that grow along the key order (about 48 nats over the prefix)
+    make the running maximum overtake the lazy-rescale threshold (2^8, i.e.
+    5.5 nats) many times. Magnitudes stay where fp32 scores can meet the 1e-3
+    lse bound."""
+    from workloads import bf16_bits_to_f32, f32_to_bf16_bits
+    inp = make_inputs(batch=1, num_heads=4, prefix=[3000], T=8, tree="random", pool_slots=4096,
+                      nsplit=3, seed=41, placement="contiguous")
+    q = np.abs(bf16_bits_to_f32(inp.q))
+    inp.q = f32_to_bf16_bits(q)
+    n = 3000 + 8
+    kv = bf16_bits_to_f32(inp.kv_pool[:n]) + (0.0005 * np.arange(n, dtype=np.float32))[:, None]
+    inp.kv_pool = inp.kv_pool.copy()
+    inp.kv_pool[:n] = f32_to_bf16_bits(kv)
+    d = run_gpu(inp, flags=flags)
+    assert status(d) == 0
+    out, lse = host_out(d)
+    ref_out, ref_lse = oracle_ref(inp)
+    compare(out, lse, ref_out, ref_lse, "growing scores")
