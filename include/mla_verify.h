@@ -201,13 +201,17 @@ int mla_verify_attention_anc(const void *q, const void *kv_pool, const int32_t *
  *                                   (normalised within the split; 0 if none)
  * at workspace + 256 (lse_part, padded to 256 bytes) and right after it
  * (o_part). Exactly one of tree_parent / anc_mask must be non-NULL.
- * flags: 0 = default kernel; MLA_PARTIAL_SIMT forces the CUDA-core kernel.
+ * flags: 0 = default kernel (tensor cores, two SMs per 128-row block);
+ * MLA_PARTIAL_SIMT forces the CUDA-core kernel; MLA_PARTIAL_TC_QUARTER the
+ * single-SM tensor-core kernel that splits the V dims over four CTAs. All
+ * give results within the documented tolerance of each other.
  *
  * mla_verify_combine merges them ([VK] Part VII "reduce"):
  *   lse[n] = ln sum_s exp(lse_part[n,s]);  out[n] = sum_s exp(lse_part[n,s] - lse[n]) o_part[n,s]
  * rounded to bf16 (nearest even); splits with lse_part = -inf get weight 0.
  */
 #define MLA_PARTIAL_SIMT 0x1u
+#define MLA_PARTIAL_TC_QUARTER 0x2u
 int mla_verify_partial(const void *q, const void *kv_pool, const int32_t *kv_indices,
                        const int32_t *kv_indptr, const int32_t *prefix_lens,
                        const int32_t *tree_parent, const uint64_t *anc_mask, int T, int nsplit,

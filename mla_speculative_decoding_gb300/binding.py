@@ -33,6 +33,7 @@ MLA_STATUS_EMPTY_ROW = 0x20
 MLA_STATUS_TIMEOUT = 0x40
 
 MLA_PARTIAL_SIMT = 0x1
+MLA_PARTIAL_TC_QUARTER = 0x2
 D_QK = 576
 D_V = 512
 

@@ -42,7 +42,8 @@ int init_device(int device) {
         rc = MLA_ERR_CUDA;
     } else if (major != 10 || minor != 3) {
         rc = MLA_ERR_UNSUPPORTED;  // the library carries sm_103a code only
-    } else if (setup_partial_simt() != cudaSuccess || setup_partial_tc() != cudaSuccess) {
+    } else if (setup_partial_simt() != cudaSuccess || setup_partial_tc() != cudaSuccess ||
+               setup_partial_pair() != cudaSuccess) {
         rc = MLA_ERR_CUDA;
     }
     if (rc == MLA_OK) {
@@ -137,10 +138,12 @@ PartialArgs make_partial_args(const void* q, const void* kv_pool, const int32_t*
 
 int run_partial(const PartialArgs& a, unsigned flags, int sm_count, cudaStream_t stream) {
     cudaError_t e;
-    if (!(flags & MLA_PARTIAL_SIMT) && partial_tc_supported(a))
+    if (flags & MLA_PARTIAL_SIMT)
+        e = launch_partial_simt(a, stream);
+    else if ((flags & MLA_PARTIAL_TC_QUARTER) && partial_tc_supported(a))
         e = launch_partial_tc(a, sm_count, stream);
     else
-        e = launch_partial_simt(a, stream);
+        e = launch_partial_pair(a, stream);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -269,7 +272,7 @@ MLAV_API int mla_verify_partial(const void* q, const void* kv_pool, const int32_
                                 anc_mask, T, nsplit, workspace, batch, num_heads, pool_slots,
                                 softmax_scale, workspace_bytes);
     if (rc != MLA_OK) return rc;
-    if (flags & ~MLA_PARTIAL_SIMT) return MLA_ERR_INVALID_ARG;
+    if (flags & ~(MLA_PARTIAL_SIMT | MLA_PARTIAL_TC_QUARTER)) return MLA_ERR_INVALID_ARG;
     int sms = 0;
     rc = ensure_ready(stream, &sms);
     if (rc != MLA_OK) return rc;

@@ -1,0 +1,634 @@
+// Split-KV partial attention on tcgen05 tensor cores, two SMs per work item.
+//
+// The verify attention of "The Custom sm_120 Verify Kernel..." (Parts VI,
+// VII, IX): every tree-token x head row of a request attends over the
+// request's scattered latent KV rows (prefix unmasked, tree block masked),
+// in a KV-split "partial + reduce" design.
+//
+// Work item = (128-row block of the request's T*H rows, split s, request b),
+// run by a cluster of two CTAs on two SMs. TMEM holds 512 fp32 columns per
+// SM; an accumulator for all 512 V dims of 128 rows fills one SM's TMEM, so
+// the scores and the output live on different SMs:
+//
+//   S-CTA (rank 0): S = Q K^T for 256-key tiles (one N = 256 MMA per 16 dims,
+//     36 per tile). TMEM: Q's 512 latent dims [0, 256) as the A operand, S
+//     [256, 512). Q's 64 RoPE dims are an A operand in shared memory. K is
+//     streamed in 64-dim blocks of 256 keys (32 KB, 6-stage ring) by cp.async
+//     gathers of the scattered 1152-byte rows. Eight softmax warps (two per
+//     TMEM lane quarter, one per 128-key half) copy S out of TMEM at once
+//     (freeing it for the next tile's MMAs), mask it (tree mask only past the
+//     prefix), exchange the per-row tile maximum, keep a lazily updated
+//     reference maximum (rescaling only when the tile maximum exceeds it by
+//     2^8), and store P as bf16 straight into the O-CTA's shared memory
+//     (distributed shared memory), with the per-row rescale factor.
+//   O-CTA (rank 1): O += P V with TMEM O = [0, 512) (two N = 256 accumulator
+//     chains, one per half of the V dims). V rows are streamed in 32-key
+//     stages (32 KB, 4-stage ring). Four correction warps apply the rare
+//     rescales to O between tiles and, at the end, normalise O and write the
+//     partial (o, lse).
+//
+// Every wait is bounded; on a timeout a CTA drains its MMAs, frees TMEM,
+// reaches the final cluster barrier and flags MLA_STATUS_TIMEOUT.
+#include "partial_tc.cuh"
+#include "tc_ptx.cuh"
+
+namespace mlav {
+namespace {
+
+using namespace tc;
+
+constexpr int kM = 128;
+constexpr int kNT = 256;          // keys per tile
+constexpr int kThreads = 320;     // 10 warps
+constexpr int kKStages = 6;
+constexpr uint32_t kKBlock = kNT * 128;        // 256 keys x 64 dims (bf16)
+constexpr int kMetaRing = 4;
+constexpr int kVKeys = 32;
+constexpr int kVStages = 4;
+constexpr uint32_t kVBlock = kVKeys * 128;     // 32 keys x 64 dims
+constexpr uint32_t kVStage = 8 * kVBlock;      // 32 keys x 512 dims
+constexpr uint32_t kPBlock = kM * 128;         // 128 rows x 64 keys (bf16)
+constexpr uint32_t kQStageStride = 1040;       // padded staging row of 512 bf16
+constexpr uint32_t kColQ = 0, kColS = 256;     // S-CTA TMEM map
+constexpr float kRescaleLog2 = 8.0f;
+
+struct SmemS {
+    unsigned char q_rope[kM * 128];            // [128 rows x 64 dims], 128B-swizzled
+    unsigned char kring[kKStages][kKBlock];    // [256 keys x 64 dims] per stage
+    uint32_t valid[kMetaRing][kNT / 32];
+    float mx[2][2][kM];
+    uint64_t anc[MLA_MAX_TREE];
+    int32_t par[MLA_MAX_TREE];
+    uint64_t k_full[kKStages], k_empty[kKStages];
+    uint64_t meta_full[kMetaRing], meta_free[kMetaRing];
+    uint64_t s_full, s_free, q_ready, mx_bar[2];
+};
+struct SmemO {
+    unsigned char p[4 * kPBlock];              // [128 rows x 256 keys], 4 swizzled 64-key blocks
+    unsigned char vring[kVStages][kVStage];    // [32 keys x 512 dims] per stage
+    float alpha[kM];
+    float fin_m[kM];
+    float fin_l[2][kM];
+    uint64_t v_full[kVStages], v_empty[kVStages];
+    uint64_t o_gate, o_prog;
+};
+// The header sits at the same offset in both CTAs: the S-CTA arrives on the
+// O-CTA's p_full / fin and the O-CTA on the S-CTA's p_free.
+struct Header {
+    uint64_t p_full, p_free, fin, drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int no_abort;
+};
+struct __align__(1024) SmemPair {
+    union {
+        SmemS s;
+        SmemO o;
+    } u;
+    Header h;
+};
+
+constexpr size_t kSmemBytes = sizeof(SmemPair) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kM * kQStageStride <= kKStages * kKBlock, "Q staging must fit in the K ring");
+
+__device__ __forceinline__ uint32_t ba(const uint64_t& b) { return smem_u32(&b); }
+
+__device__ __forceinline__ bool warp_wait(const uint64_t& bar, uint32_t parity,
+                                          volatile int* abort) {
+    const bool ok = mbar_wait(ba(bar), parity, abort);
+    return __all_sync(0xffffffffu, ok);
+}
+__device__ __forceinline__ bool warp_wait_cluster(const uint64_t& bar, uint32_t parity,
+                                                  volatile int* abort) {
+    const bool ok = mbar_wait_cluster(ba(bar), parity, abort);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+partial_pair_kernel(const PartialArgs a) {
+    extern __shared__ __align__(1024) unsigned char raw[];
+    unsigned char* base = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+    SmemPair& sm = *reinterpret_cast<SmemPair*>(base);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int rb = blockIdx.x >> 1;
+    const int s = blockIdx.y, b = blockIdx.z;
+    const int T = a.T, H = a.H, rows_req = T * H;
+
+    int Lb, K;
+    int bad = request_keys(a, b, Lb, K);
+    int kb, ke;
+    split_range(K, a.nsplit, s, kb, ke);
+    const int ntiles = (ke - kb + kNT - 1) / kNT;
+    const int64_t kbase = a.kv_indptr[b];
+
+    if (ntiles <= 0) {  // empty split (fixed grid, early exit): lse = -inf, o = 0
+        if (rank == 1 && warp >= 2 && warp < 6) {
+            const int grow = rb * kM + 32 * (warp & 3) + lane;
+            if (grow < rows_req) {
+                const int64_t pid = ((int64_t)b * rows_req + grow) * a.nsplit + s;
+                float4* o = reinterpret_cast<float4*>(a.o_part + pid * kDv);
+                for (int c = 0; c < kDv / 4; ++c) o[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                a.lse_part[pid] = -INFINITY;
+            }
+        }
+        if (rank == 0 && tid == 0) status_or(a.status, bad);
+        return;
+    }
+    if (rank != 0) bad &= ~MLA_STATUS_BAD_INDPTR;  // reported once, by the S-CTA
+
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&sm.h.tmem_base), 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(ba(sm.h.p_full), 256);
+        mbar_init(ba(sm.h.p_free), 1);
+        mbar_init(ba(sm.h.fin), 256);
+        mbar_init(ba(sm.h.drain), 1);
+        if (rank == 0) {
+            SmemS& S = sm.u.s;
+            for (int i = 0; i < kKStages; ++i) {
+                mbar_init(ba(S.k_full[i]), 32);
+                mbar_init(ba(S.k_empty[i]), 1);
+            }
+            for (int i = 0; i < kMetaRing; ++i) {
+                mbar_init(ba(S.meta_full[i]), 1);
+                mbar_init(ba(S.meta_free[i]), 256);
+            }
+            mbar_init(ba(S.s_full), 1);
+            mbar_init(ba(S.s_free), 256);
+            mbar_init(ba(S.q_ready), 256);
+            mbar_init(ba(S.mx_bar[0]), 256);
+            mbar_init(ba(S.mx_bar[1]), 256);
+        } else {
+            SmemO& O = sm.u.o;
+            for (int i = 0; i < kVStages; ++i) {
+                mbar_init(ba(O.v_full[i]), 32);
+                mbar_init(ba(O.v_empty[i]), 1);
+            }
+            mbar_init(ba(O.o_gate), 128);
+            mbar_init(ba(O.o_prog), 1);
+        }
+        sm.h.abort_flag = 0;
+        sm.h.no_abort = 0;
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // both CTAs' barriers exist before any remote arrive
+    tc_fence_after();
+    const uint32_t tbase = sm.h.tmem_base;
+    volatile int* abort_p = &sm.h.abort_flag;
+    const uint32_t peer = rank ^ 1u;
+
+    if (rank == 0) {
+        SmemS& S = sm.u.s;
+        if (warp == 0) {
+            // ------------------------------------------------ S producer: K blocks
+            bool ok = warp_wait(S.q_ready, 0, abort_p);  // the ring doubles as Q staging
+            int32_t sl[8];
+            auto load_slots = [&](int i, int32_t (&out)[8]) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int j = kb + i * kNT + 32 * q + lane;
+                    int32_t v = -1;
+                    if (j < ke) {
+                        v = a.kv_indices[kbase + j];
+                        if (v < 0 || (int64_t)v >= a.pool_slots) {
+                            bad |= MLA_STATUS_BAD_SLOT;
+                            v = -1;
+                        }
+                    }
+                    out[q] = v;
+                }
+            };
+            load_slots(0, sl);
+            for (int i = 0; ok && i < ntiles; ++i) {
+                int32_t nxt[8];
+                if (i + 1 < ntiles) load_slots(i + 1, nxt);
+                const int mi = i % kMetaRing;
+                if (i >= kMetaRing && !warp_wait(S.meta_free[mi], ((i / kMetaRing) - 1) & 1, abort_p)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint32_t w = __ballot_sync(0xffffffffu, sl[q] >= 0);
+                    if (lane == q) S.valid[mi][q] = w;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ba(S.meta_full[mi]));
+                for (int kbk = 0; kbk < kDqk / 64; ++kbk) {
+                    const int g = i * (kDqk / 64) + kbk;
+                    const int st = g % kKStages;
+                    if (g >= kKStages && !warp_wait(S.k_empty[st], ((g / kKStages) - 1) & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst0 = smem_u32(S.kring[st]);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+#pragma unroll
+                        for (int it = 0; it < 8; ++it) {
+                            const int kl = it * 4 + (lane >> 3);  // key within the 32-key group q
+                            const int c = lane & 7;
+                            const int32_t slot = __shfl_sync(0xffffffffu, sl[q], kl);
+                            const __nv_bfloat16* src =
+                                a.kv + (slot >= 0 ? (int64_t)slot * kDqk : 0) + kbk * 64 + c * 8;
+                            cp_async_16_zfill(dst0 + sw128_offset(32 * q + kl, c), src, slot >= 0);
+                        }
+                    }
+                    cp_async_mbar_arrive_noinc(ba(S.k_full[st]));
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) sl[q] = nxt[q];
+            }
+            cp_async_wait_all();
+        } else if (warp == 1) {
+            // ------------------------------------------------ S MMA issuer
+            if (lane == 0) {
+                const uint32_t idesc = make_idesc_bf16(kM, kNT, false, false);
+                bool ok = mbar_wait(ba(S.q_ready), 0, abort_p);
+                fence_proxy_async_smem();
+                tc_fence_after();
+                const uint32_t dS = tbase + kColS;
+                const uint32_t qr = smem_u32(S.q_rope);
+                for (int i = 0; ok && i < ntiles; ++i) {
+                    if (i >= 1 && !mbar_wait(ba(S.s_free), (i - 1) & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int kbk = 0; kbk < kDqk / 64; ++kbk) {
+                        const int g = i * (kDqk / 64) + kbk;
+                        const int st = g % kKStages;
+                        if (!mbar_wait(ba(S.k_full[st]), (g / kKStages) & 1, abort_p)) {
+                            ok = false;
+                            break;
+                        }
+                        fence_proxy_async_smem();
+                        tc_fence_after();
+                        const uint32_t kt = smem_u32(S.kring[st]);
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint64_t bd = make_sdesc(kt + ks * 32, 16, 1024, kSwizzle128B);
+                            const uint32_t acc = (kbk | ks) ? 1u : 0u;
+                            if (kbk < 8)
+                                mma_ts(dS, tbase + kColQ + kbk * 32 + ks * 8, bd, idesc, acc);
+                            else
+                                mma_ss(dS, make_sdesc(qr + ks * 32, 16, 1024, kSwizzle128B), bd,
+                                       idesc, acc);
+                        }
+                        mma_commit(ba(S.k_empty[st]));
+                    }
+                    if (ok) mma_commit(ba(S.s_full));
+                }
+                mma_commit(ba(sm.h.drain));
+                mbar_wait(ba(sm.h.drain), 0, &sm.h.no_abort);
+            }
+            __syncwarp();
+        } else {
+            // ------------------------------------------------ softmax (8 warps)
+            const int quarter = warp & 3;
+            const int half = (warp - 2) >> 2;     // 128-key half of the tile
+            const int r = 32 * quarter + lane;     // row = TMEM lane
+            const int grow = rb * kM + r;
+            const bool row_ok = grow < rows_req;
+            const int t = row_ok ? grow / H : 0;
+            const uint32_t lb = (uint32_t)(32 * quarter) << 16;
+            const int stid = tid - 64;             // 0..255
+
+            // Q staging: latent dims into the K ring (padded rows), RoPE dims
+            // straight into their swizzled A-operand tile.
+            {
+                const uint32_t stage0 = smem_u32(S.kring[0]);
+                const __nv_bfloat16* q0 = a.q + ((int64_t)b * rows_req + rb * kM) * kDqk;
+                for (int f = stid; f < kM * (kDqk / 8); f += 256) {
+                    const int rr = f / (kDqk / 8), c = f % (kDqk / 8);
+                    const bool v = rb * kM + rr < rows_req;
+                    const __nv_bfloat16* src = v ? q0 + (int64_t)rr * kDqk + c * 8 : a.q;
+                    const uint32_t dst = c < 64 ? stage0 + rr * kQStageStride + c * 16
+                                                : smem_u32(S.q_rope) + sw128_offset(rr, c - 64);
+                    cp_async_16_zfill(dst, src, v);
+                }
+                if (stid < T) {
+                    if (a.anc_mask != nullptr)
+                        S.anc[stid] = a.anc_mask[(int64_t)b * T + stid];
+                    else
+                        S.par[stid] = a.tree_parent[(int64_t)b * T + stid];
+                }
+                cp_async_wait_all();
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                if (stid == 0 && a.anc_mask == nullptr) bad |= build_anc_serial(S.par, T, S.anc);
+                if (half == 0) {
+                    const unsigned char* row = S.kring[0] + r * kQStageStride;
+#pragma unroll 1
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t w[32];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(row + c * 128 + u * 16);
+                            w[4 * u] = v.x;
+                            w[4 * u + 1] = v.y;
+                            w[4 * u + 2] = v.z;
+                            w[4 * u + 3] = v.w;
+                        }
+                        tmem_st32(tbase + lb + kColQ + c * 32, w);
+                    }
+                    tmem_wait_st();
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                mbar_arrive(ba(S.q_ready));
+            }
+            const uint64_t anc_t = S.anc[t];
+            const uint32_t p_peer = mapa_shared(smem_u32(sm.u.o.p), peer);
+            const uint32_t alpha_peer = mapa_shared(smem_u32(&sm.u.o.alpha[r]), peer);
+            const uint32_t pfull_peer = mapa_shared(ba(sm.h.p_full), peer);
+            float m_ref = -INFINITY, l_part = 0.f;
+            bool ok = true;
+            for (int i = 0; i < ntiles; ++i) {
+                if (!warp_wait(S.s_full, i & 1, abort_p)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float sc[128];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t w[32];
+                    tmem_ld32(tbase + lb + kColS + half * 128 + c * 32, w);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) sc[c * 32 + u] = __uint_as_float(w[u]);
+                }
+                tc_fence_before();
+                mbar_arrive(ba(S.s_free));
+                const int mi = i % kMetaRing;
+                if (!warp_wait(S.meta_full[mi], (i / kMetaRing) & 1, abort_p)) {
+                    ok = false;
+                    break;
+                }
+                uint32_t vw[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) vw[q] = row_ok ? S.valid[mi][4 * half + q] : 0u;
+                mbar_arrive(ba(S.meta_free[mi]));
+                const int k0 = kb + i * kNT + 128 * half;
+                if (k0 + 128 > Lb) {  // this half reaches the tree keys
+#pragma unroll
+                    for (int c = 0; c < 128; ++c) {
+                        const int u = k0 + c - Lb;
+                        if (u >= 0 && !(u < T && ((anc_t >> u) & 1ull))) vw[c >> 5] &= ~(1u << (c & 31));
+                    }
+                }
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    sc[c] = ((vw[c >> 5] >> (c & 31)) & 1u) ? sc[c] * a.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, sc[c]);
+                }
+                S.mx[i & 1][half][r] = mx;
+                mbar_arrive(ba(S.mx_bar[i & 1]));
+                if (!warp_wait(S.mx_bar[i & 1], (i >> 1) & 1, abort_p)) {
+                    ok = false;
+                    break;
+                }
+                const float mt = fmaxf(mx, S.mx[i & 1][half ^ 1][r]);
+                float alpha = 1.f;
+                if (mt > -INFINITY) {
+                    if (m_ref == -INFINITY) {
+                        m_ref = mt;
+                    } else if (mt > m_ref + kRescaleLog2) {
+                        alpha = exp2f(m_ref - mt);
+                        m_ref = mt;
+                        l_part *= alpha;
+                    }
+                }
+                if (i >= 1 && !warp_wait_cluster(sm.h.p_free, (i - 1) & 1, abort_p)) {
+                    ok = false;
+                    break;
+                }
+                // P (bf16) -> the O-CTA's A-operand tile, 8 keys (16 bytes) at a time.
+                float psum = 0.f;
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+                    const uint32_t pb = p_peer + (2 * half + blk) * kPBlock;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int k = blk * 64 + c * 8 + 2 * u;
+                            const float p0 = sc[k] > -INFINITY ? exp2f(sc[k] - m_ref) : 0.f;
+                            const float p1 = sc[k + 1] > -INFINITY ? exp2f(sc[k + 1] - m_ref) : 0.f;
+                            psum += p0 + p1;
+                            w[u] = pack_bf16x2(p0, p1);
+                        }
+                        st_cluster_v4(pb + sw128_offset(r, c), w[0], w[1], w[2], w[3]);
+                    }
+                }
+                l_part += psum;
+                if (half == 0) st_cluster_f32(alpha_peer, alpha);
+                fence_proxy_async_all();
+                mbar_arrive_cluster(pfull_peer);
+            }
+            if (ok) {
+                if (half == 0) {
+                    st_cluster_f32(mapa_shared(smem_u32(&sm.u.o.fin_m[r]), peer), m_ref);
+                    st_cluster_f32(mapa_shared(smem_u32(&sm.u.o.fin_l[0][r]), peer), l_part);
+                } else {
+                    st_cluster_f32(mapa_shared(smem_u32(&sm.u.o.fin_l[1][r]), peer), l_part);
+                }
+                mbar_arrive_cluster(mapa_shared(ba(sm.h.fin), peer));
+            }
+        }
+    } else {
+        SmemO& O = sm.u.o;
+        if (warp == 0) {
+            // ------------------------------------------------ O producer: V rows
+            int32_t sl[8];
+            auto load_slots = [&](int i, int32_t (&out)[8]) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int j = kb + i * kNT + 32 * q + lane;
+                    int32_t v = -1;
+                    if (j < ke) {
+                        v = a.kv_indices[kbase + j];
+                        if (v < 0 || (int64_t)v >= a.pool_slots) v = -1;
+                    }
+                    out[q] = v;
+                }
+            };
+            load_slots(0, sl);
+            bool ok = true;
+            for (int i = 0; ok && i < ntiles; ++i) {
+                int32_t nxt[8];
+                if (i + 1 < ntiles) load_slots(i + 1, nxt);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int g = i * 8 + q;
+                    const int st = g % kVStages;
+                    if (g >= kVStages && !warp_wait(O.v_empty[st], ((g / kVStages) - 1) & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst0 = smem_u32(O.vring[st]);
+#pragma unroll 4
+                    for (int it = 0; it < 64; ++it) {
+                        const int kl = it >> 1;                 // key within the stage
+                        const int c = (it & 1) * 32 + lane;     // 16-byte chunk of the V row
+                        const int32_t slot = __shfl_sync(0xffffffffu, sl[q], kl);
+                        const __nv_bfloat16* src = a.kv + (slot >= 0 ? (int64_t)slot * kDqk : 0) + c * 8;
+                        cp_async_16_zfill(dst0 + (c >> 3) * kVBlock + sw128_offset(kl, c & 7), src,
+                                          slot >= 0);
+                    }
+                    cp_async_mbar_arrive_noinc(ba(O.v_full[st]));
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) sl[q] = nxt[q];
+            }
+            cp_async_wait_all();
+        } else if (warp == 1) {
+            // ------------------------------------------------ O MMA issuer
+            if (lane == 0) {
+                const uint32_t idesc = make_idesc_bf16(kM, 256, false, true);
+                const uint32_t pfree_peer = mapa_shared(ba(sm.h.p_free), peer);
+                const uint32_t p0 = smem_u32(O.p);
+                bool ok = true;
+                for (int i = 0; ok && i < ntiles; ++i) {
+                    if (!mbar_wait_cluster(ba(sm.h.p_full), i & 1, abort_p) ||
+                        !mbar_wait(ba(O.o_gate), i & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_after();
+                    for (int q = 0; q < 8; ++q) {
+                        const int g = i * 8 + q;
+                        const int st = g % kVStages;
+                        if (!mbar_wait(ba(O.v_full[st]), (g / kVStages) & 1, abort_p)) {
+                            ok = false;
+                            break;
+                        }
+                        fence_proxy_async_smem();
+                        tc_fence_after();
+                        const uint32_t vs = smem_u32(O.vring[st]);
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const int kg = q * 32 + kk * 16;  // key within the tile
+                            const uint64_t ad = make_sdesc(p0 + (kg >> 6) * kPBlock + ((kg & 63) >> 4) * 32,
+                                                           16, 1024, kSwizzle128B);
+#pragma unroll
+                            for (int hv = 0; hv < 2; ++hv) {
+                                const uint64_t bd = make_sdesc(vs + hv * 4 * kVBlock + kk * 2048,
+                                                               kVBlock, 1024, kSwizzle128B);
+                                mma_ss(tbase + hv * 256, ad, bd, idesc,
+                                       (i > 0 || q > 0 || kk > 0) ? 1u : 0u);
+                            }
+                        }
+                        mma_commit(ba(O.v_empty[st]));
+                    }
+                    if (!ok) break;
+                    mma_commit(ba(O.o_prog));
+                    // P is single-buffered: hand it back once this tile's P V is done.
+                    if (!mbar_wait(ba(O.o_prog), i & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_cluster(pfree_peer);
+                }
+                mma_commit(ba(sm.h.drain));
+                mbar_wait(ba(sm.h.drain), 0, &sm.h.no_abort);
+            }
+            __syncwarp();
+        } else if (warp < 6) {
+            // ------------------------------------------------ correction + epilogue
+            const int quarter = warp & 3;
+            const int r = 32 * quarter + lane;
+            const int grow = rb * kM + r;
+            const bool row_ok = grow < rows_req;
+            const uint32_t lb = (uint32_t)(32 * quarter) << 16;
+            bool ok = true;
+            for (int i = 0; i < ntiles; ++i) {
+                if (!warp_wait_cluster(sm.h.p_full, i & 1, abort_p)) {
+                    ok = false;
+                    break;
+                }
+                const float alpha = O.alpha[r];
+                if (__any_sync(0xffffffffu, alpha != 1.f) && i > 0) {
+                    if (!warp_wait(O.o_prog, (i - 1) & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c0 = 0; c0 < 512; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(tbase + lb + c0, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
+                        tmem_st32(tbase + lb + c0, o);
+                    }
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                mbar_arrive(ba(O.o_gate));
+            }
+            if (ok) ok = warp_wait_cluster(sm.h.fin, 0, abort_p);
+            if (ok) ok = warp_wait(O.o_prog, (ntiles - 1) & 1, abort_p);
+            tc_fence_after();
+            if (ok) {
+                const float l = O.fin_l[0][r] + O.fin_l[1][r];
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const int64_t pid = ((int64_t)b * rows_req + (row_ok ? grow : 0)) * a.nsplit + s;
+                float4* dst = reinterpret_cast<float4*>(a.o_part + pid * kDv);
+#pragma unroll 1
+                for (int c0 = 0; c0 < 512; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(tbase + lb + c0, o);
+                    tmem_wait_ld();
+                    if (row_ok) {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            dst[c0 / 4 + u] = make_float4(
+                                __uint_as_float(o[4 * u]) * inv, __uint_as_float(o[4 * u + 1]) * inv,
+                                __uint_as_float(o[4 * u + 2]) * inv, __uint_as_float(o[4 * u + 3]) * inv);
+                    }
+                }
+                if (row_ok)
+                    a.lse_part[pid] = l > 0.f ? (O.fin_m[r] + log2f(l)) * kLn2 : -INFINITY;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // no CTA leaves while its peer may still touch its shared memory
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 512);
+    }
+    if (sm.h.abort_flag) bad |= MLA_STATUS_TIMEOUT;
+    status_or(a.status, bad);
+}
+
+}  // namespace
+
+cudaError_t setup_partial_pair() {
+    return cudaFuncSetAttribute(partial_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kSmemBytes);
+}
+
+cudaError_t launch_partial_pair(const PartialArgs& a, cudaStream_t stream) {
+    const int rows_req = a.T * a.H;
+    const int nrb = (rows_req + kM - 1) / kM;
+    dim3 grid(2 * nrb, a.nsplit, a.batch);
+    partial_pair_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace mlav

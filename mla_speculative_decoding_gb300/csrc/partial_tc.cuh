@@ -10,4 +10,8 @@ bool partial_tc_supported(const PartialArgs& a);
 cudaError_t launch_partial_tc(const PartialArgs& a, int sm_count, cudaStream_t stream);
 cudaError_t setup_partial_tc();
 
+// Split-role pair kernel (two SMs per 128-row block): the default tensor-core path.
+cudaError_t launch_partial_pair(const PartialArgs& a, cudaStream_t stream);
+cudaError_t setup_partial_pair();
+
 }  // namespace mlav

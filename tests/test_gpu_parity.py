@@ -14,7 +14,7 @@ from tests.gpu_util import config_cached, compare, host_out, oracle_ref, run_gpu
 from workloads import make_config, make_inputs
 
 pytestmark = pytest.mark.gpu
-PATHS = [0, mv.MLA_PARTIAL_SIMT]
+PATHS = [0, mv.MLA_PARTIAL_SIMT, mv.MLA_PARTIAL_TC_QUARTER]
 
 
 @pytest.mark.parametrize("flags", PATHS)
