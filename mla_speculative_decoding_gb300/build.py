@@ -89,14 +89,16 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
 
 def build_selftest(force: bool = False) -> str:
     """Test-only library with the tcgen05 layout self-test (shares tc_ptx.cuh)."""
-    deps = [SELFTEST_SRC, os.path.join(CSRC, "tc_ptx.cuh"), os.path.abspath(__file__)]
+    deps = [SELFTEST_SRC, os.path.join(CSRC, "tc_ptx.cuh"), os.path.join(CSRC, "tmap.cu"),
+            os.path.join(CSRC, "tmap.cuh"), os.path.abspath(__file__)]
     if (not force and os.path.exists(SELFTEST_LIB)
             and all(os.path.getmtime(d) <= os.path.getmtime(SELFTEST_LIB) for d in deps)):
         return SELFTEST_LIB
     os.makedirs(OUT_DIR, exist_ok=True)
     tmp = SELFTEST_LIB + f".tmp{os.getpid()}"
     cmd = [_nvcc()] + ARCH + ["-O2", "-std=c++17", "-I", CSRC, "-Xcompiler",
-                              "-fPIC,-fvisibility=hidden", "-shared", SELFTEST_SRC, "-o", tmp]
+                              "-fPIC,-fvisibility=hidden", "-shared", SELFTEST_SRC,
+                              os.path.join(CSRC, "tmap.cu"), "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("selftest build failed:\n" + r.stdout + r.stderr)

@@ -9,7 +9,8 @@
 // reference did this on the host (tree-build 1.8 ms, mask-build 0.18 ms;
 // "The Capstone Report", section 2); here it is a capture-safe kernel.
 //
-// Grid: (batch, kBlocksPerReq). Each block recomputes its request's list
+// Grid: (batch, blocks per request sized from the host bound on the list
+// length). Each block recomputes its request's list
 // offset from prefix_lens (an integer block reduction over earlier
 // requests), so there is no inter-block communication and no atomics other
 // than the error word. Bit-exact and deterministic.
@@ -19,7 +20,7 @@ namespace mlav {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kBlocksPerReq = 32;
+constexpr int kMaxBlocksPerReq = 256;
 
 __device__ __forceinline__ int32_t clamp_prefix(const int32_t* prefix_lens,
                                                 const int32_t* req_pool_indices, int b,
@@ -107,7 +108,12 @@ cudaError_t launch_build_meta(const int32_t* req_to_token, int64_t stride, int64
                               int batch, int T, int64_t capacity, int32_t* kv_indptr,
                               int32_t* kv_indices, uint64_t* anc, int32_t* status,
                               cudaStream_t stream) {
-    dim3 grid(batch, kBlocksPerReq);
+    // Blocks per request from host-side bounds only (no device reads): enough
+    // that each thread copies about two entries of the longest possible list.
+    const int64_t per_req = stride + T;
+    const int64_t want = (per_req + 2 * kThreads - 1) / (2 * kThreads);
+    const int by = (int)(want < 1 ? 1 : (want > kMaxBlocksPerReq ? kMaxBlocksPerReq : want));
+    dim3 grid(batch, by);
     build_meta_kernel<<<grid, kThreads, 0, stream>>>(req_to_token, stride, rows,
                                                      req_pool_indices, prefix_lens, out_cache_loc,
                                                      tree_parent, batch, T, capacity, kv_indptr,

@@ -13,8 +13,10 @@
 //   S-CTA (rank 0): S = Q K^T for 256-key tiles (one N = 256 MMA per 16 dims,
 //     36 per tile). TMEM: Q's 512 latent dims [0, 256) as the A operand, S
 //     [256, 512). Q's 64 RoPE dims are an A operand in shared memory. K is
-//     streamed in 64-dim blocks of 256 keys (32 KB, 6-stage ring) by cp.async
-//     gathers of the scattered 1152-byte rows. Eight softmax warps (two per
+//     streamed in 64-dim blocks of 256 keys (32 KB, 6-stage ring), gathered
+//     from the scattered rows by three warps of 16-byte cp.async copies (eight
+//     lanes per 128-byte row segment; measured faster than TMA gather4 for
+//     this pattern). Eight softmax warps (two per
 //     TMEM lane quarter, one per 128-key half) copy S out of TMEM at once
 //     (freeing it for the next tile's MMAs), mask it (tree mask only past the
 //     prefix), exchange the per-row tile maximum, keep a lazily updated
@@ -22,8 +24,9 @@
 //     2^8), and store P as bf16 straight into the O-CTA's shared memory
 //     (distributed shared memory), with the per-row rescale factor.
 //   O-CTA (rank 1): O += P V with TMEM O = [0, 512) (two N = 256 accumulator
-//     chains, one per half of the V dims). V rows are streamed in 32-key
-//     stages (32 KB, 4-stage ring). Four correction warps apply the rare
+//     chains, one per half of the V dims). V rows are gathered by seven warps
+//     of cp.async copies in 32-key stages (32 KB, 4-stage ring). Four
+//     correction warps apply the rare
 //     rescales to O between tiles and, at the end, normalise O and write the
 //     partial (o, lse).
 //
@@ -39,7 +42,9 @@ using namespace tc;
 
 constexpr int kM = 128;
 constexpr int kNT = 256;          // keys per tile
-constexpr int kThreads = 320;     // 10 warps
+constexpr int kThreads = 384;     // 12 warps
+constexpr int kSProd = 3;         // S-side producer warps: 0, 10, 11
+constexpr int kOProd = 7;         // O-side producer warps: 0, 6..11
 constexpr int kKStages = 6;
 constexpr uint32_t kKBlock = kNT * 128;        // 256 keys x 64 dims (bf16)
 constexpr int kMetaRing = 4;
@@ -56,21 +61,25 @@ struct SmemS {
     unsigned char q_rope[kM * 128];            // [128 rows x 64 dims], 128B-swizzled
     unsigned char kring[kKStages][kKBlock];    // [256 keys x 64 dims] per stage
     uint32_t valid[kMetaRing][kNT / 32];
+    int32_t rows[2][kNT];                      // pool rows of the tiles being gathered
     float mx[2][2][kM];
     uint64_t anc[MLA_MAX_TREE];
     int32_t par[MLA_MAX_TREE];
     uint64_t k_full[kKStages], k_empty[kKStages];
     uint64_t meta_full[kMetaRing], meta_free[kMetaRing];
     uint64_t s_full, s_free, q_ready, mx_bar[2];
+    uint64_t rows_full[2], rows_free[2];
 };
 struct SmemO {
     unsigned char p[4 * kPBlock];              // [128 rows x 256 keys], 4 swizzled 64-key blocks
     unsigned char vring[kVStages][kVStage];    // [32 keys x 512 dims] per stage
+    int32_t rows[2][kNT];
     float alpha[kM];
     float fin_m[kM];
     float fin_l[2][kM];
     uint64_t v_full[kVStages], v_empty[kVStages];
     uint64_t o_gate, o_prog;
+    uint64_t rows_full[2], rows_free[2];
 };
 // The header sits at the same offset in both CTAs: the S-CTA arrives on the
 // O-CTA's p_full / fin and the O-CTA on the S-CTA's p_free.
@@ -150,7 +159,7 @@ partial_pair_kernel(const PartialArgs a) {
         if (rank == 0) {
             SmemS& S = sm.u.s;
             for (int i = 0; i < kKStages; ++i) {
-                mbar_init(ba(S.k_full[i]), 32);
+                mbar_init(ba(S.k_full[i]), 32 * kSProd);
                 mbar_init(ba(S.k_empty[i]), 1);
             }
             for (int i = 0; i < kMetaRing; ++i) {
@@ -162,14 +171,22 @@ partial_pair_kernel(const PartialArgs a) {
             mbar_init(ba(S.q_ready), 256);
             mbar_init(ba(S.mx_bar[0]), 256);
             mbar_init(ba(S.mx_bar[1]), 256);
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(ba(S.rows_full[i]), 1);
+                mbar_init(ba(S.rows_free[i]), kSProd);
+            }
         } else {
             SmemO& O = sm.u.o;
             for (int i = 0; i < kVStages; ++i) {
-                mbar_init(ba(O.v_full[i]), 32);
+                mbar_init(ba(O.v_full[i]), 32 * kOProd);
                 mbar_init(ba(O.v_empty[i]), 1);
             }
             mbar_init(ba(O.o_gate), 128);
             mbar_init(ba(O.o_prog), 1);
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(ba(O.rows_full[i]), 1);
+                mbar_init(ba(O.rows_free[i]), kOProd);
+            }
         }
         sm.h.abort_flag = 0;
         sm.h.no_abort = 0;
@@ -185,41 +202,50 @@ partial_pair_kernel(const PartialArgs a) {
 
     if (rank == 0) {
         SmemS& S = sm.u.s;
-        if (warp == 0) {
-            // ------------------------------------------------ S producer: K blocks
+        if (warp == 0 || warp >= 10) {
+            // ------------------------------------------------ S producers: K blocks
+            // Warp 0 stages each tile's pool rows (and the key-validity bits
+            // for the softmax); warps 0, 10, 11 split the 16-byte copies, eight
+            // lanes per 128-byte row segment.
+            const int pw = warp == 0 ? 0 : warp - 9;  // 0..2
             bool ok = warp_wait(S.q_ready, 0, abort_p);  // the ring doubles as Q staging
-            int32_t sl[8];
-            auto load_slots = [&](int i, int32_t (&out)[8]) {
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int j = kb + i * kNT + 32 * q + lane;
-                    int32_t v = -1;
-                    if (j < ke) {
-                        v = a.kv_indices[kbase + j];
-                        if (v < 0 || (int64_t)v >= a.pool_slots) {
-                            bad |= MLA_STATUS_BAD_SLOT;
-                            v = -1;
-                        }
-                    }
-                    out[q] = v;
-                }
-            };
-            load_slots(0, sl);
             for (int i = 0; ok && i < ntiles; ++i) {
-                int32_t nxt[8];
-                if (i + 1 < ntiles) load_slots(i + 1, nxt);
-                const int mi = i % kMetaRing;
-                if (i >= kMetaRing && !warp_wait(S.meta_free[mi], ((i / kMetaRing) - 1) & 1, abort_p)) {
+                const int rb2 = i & 1;
+                if (pw == 0) {
+                    if (i >= 2 && !warp_wait(S.rows_free[rb2], ((i >> 1) - 1) & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    const int mi = i % kMetaRing;
+                    if (i >= kMetaRing && !warp_wait(S.meta_free[mi], ((i / kMetaRing) - 1) & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int j = kb + i * kNT + 32 * q + lane;
+                        int32_t v = -1;
+                        if (j < ke) {
+                            v = a.kv_indices[kbase + j];
+                            if (v < 0 || (int64_t)v >= a.pool_slots) {
+                                bad |= MLA_STATUS_BAD_SLOT;
+                                v = -1;
+                            }
+                        }
+                        S.rows[rb2][32 * q + lane] = v;
+                        const uint32_t w = __ballot_sync(0xffffffffu, v >= 0);
+                        if (lane == q) S.valid[mi][q] = w;
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(ba(S.meta_full[mi]));
+                        mbar_arrive(ba(S.rows_full[rb2]));
+                    }
+                }
+                if (!warp_wait(S.rows_full[rb2], (i >> 1) & 1, abort_p)) {
                     ok = false;
                     break;
                 }
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const uint32_t w = __ballot_sync(0xffffffffu, sl[q] >= 0);
-                    if (lane == q) S.valid[mi][q] = w;
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(ba(S.meta_full[mi]));
                 for (int kbk = 0; kbk < kDqk / 64; ++kbk) {
                     const int g = i * (kDqk / 64) + kbk;
                     const int st = g % kKStages;
@@ -228,22 +254,18 @@ partial_pair_kernel(const PartialArgs a) {
                         break;
                     }
                     const uint32_t dst0 = smem_u32(S.kring[st]);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-#pragma unroll
-                        for (int it = 0; it < 8; ++it) {
-                            const int kl = it * 4 + (lane >> 3);  // key within the 32-key group q
-                            const int c = lane & 7;
-                            const int32_t slot = __shfl_sync(0xffffffffu, sl[q], kl);
-                            const __nv_bfloat16* src =
-                                a.kv + (slot >= 0 ? (int64_t)slot * kDqk : 0) + kbk * 64 + c * 8;
-                            cp_async_16_zfill(dst0 + sw128_offset(32 * q + kl, c), src, slot >= 0);
-                        }
+                    for (int it = pw; it < 64; it += kSProd) {
+                        const int key = it * 4 + (lane >> 3), c = lane & 7;
+                        const int32_t slot = S.rows[rb2][key];
+                        const __nv_bfloat16* src =
+                            a.kv + (slot >= 0 ? (int64_t)slot * kDqk : 0) + kbk * 64 + c * 8;
+                        cp_async_16_zfill_nc(dst0 + sw128_offset(key, c), src, slot >= 0);
                     }
                     cp_async_mbar_arrive_noinc(ba(S.k_full[st]));
                 }
-#pragma unroll
-                for (int q = 0; q < 8; ++q) sl[q] = nxt[q];
+                if (!ok) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ba(S.rows_free[rb2]));
             }
             cp_async_wait_all();
         } else if (warp == 1) {
@@ -402,7 +424,7 @@ partial_pair_kernel(const PartialArgs a) {
                     if (m_ref == -INFINITY) {
                         m_ref = mt;
                     } else if (mt > m_ref + kRescaleLog2) {
-                        alpha = exp2f(m_ref - mt);
+                        alpha = ex2_approx(m_ref - mt);
                         m_ref = mt;
                         l_part *= alpha;
                     }
@@ -422,8 +444,8 @@ partial_pair_kernel(const PartialArgs a) {
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
                             const int k = blk * 64 + c * 8 + 2 * u;
-                            const float p0 = sc[k] > -INFINITY ? exp2f(sc[k] - m_ref) : 0.f;
-                            const float p1 = sc[k + 1] > -INFINITY ? exp2f(sc[k + 1] - m_ref) : 0.f;
+                            const float p0 = sc[k] > -INFINITY ? ex2_approx(sc[k] - m_ref) : 0.f;
+                            const float p1 = sc[k + 1] > -INFINITY ? ex2_approx(sc[k + 1] - m_ref) : 0.f;
                             psum += p0 + p1;
                             w[u] = pack_bf16x2(p0, p1);
                         }
@@ -447,27 +469,36 @@ partial_pair_kernel(const PartialArgs a) {
         }
     } else {
         SmemO& O = sm.u.o;
-        if (warp == 0) {
-            // ------------------------------------------------ O producer: V rows
-            int32_t sl[8];
-            auto load_slots = [&](int i, int32_t (&out)[8]) {
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int j = kb + i * kNT + 32 * q + lane;
-                    int32_t v = -1;
-                    if (j < ke) {
-                        v = a.kv_indices[kbase + j];
-                        if (v < 0 || (int64_t)v >= a.pool_slots) v = -1;
-                    }
-                    out[q] = v;
-                }
-            };
-            load_slots(0, sl);
+        if (warp == 0 || warp >= 6) {
+            // ------------------------------------------------ O producers: V rows
+            // Warp 0 stages each tile's pool rows; warps 0, 6..11 split the
+            // 16-byte copies (32 lanes = one half of a 1024-byte V row).
+            const int pw = warp == 0 ? 0 : warp - 5;  // 0..6
             bool ok = true;
             for (int i = 0; ok && i < ntiles; ++i) {
-                int32_t nxt[8];
-                if (i + 1 < ntiles) load_slots(i + 1, nxt);
+                const int rb2 = i & 1;
+                if (pw == 0) {
+                    if (i >= 2 && !warp_wait(O.rows_free[rb2], ((i >> 1) - 1) & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
 #pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int j = kb + i * kNT + 32 * q + lane;
+                        int32_t v = -1;
+                        if (j < ke) {
+                            v = a.kv_indices[kbase + j];
+                            if (v < 0 || (int64_t)v >= a.pool_slots) v = -1;
+                        }
+                        O.rows[rb2][32 * q + lane] = v;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(ba(O.rows_full[rb2]));
+                }
+                if (!warp_wait(O.rows_full[rb2], (i >> 1) & 1, abort_p)) {
+                    ok = false;
+                    break;
+                }
                 for (int q = 0; q < 8; ++q) {
                     const int g = i * 8 + q;
                     const int st = g % kVStages;
@@ -476,19 +507,19 @@ partial_pair_kernel(const PartialArgs a) {
                         break;
                     }
                     const uint32_t dst0 = smem_u32(O.vring[st]);
-#pragma unroll 4
-                    for (int it = 0; it < 64; ++it) {
+                    for (int it = pw; it < 64; it += kOProd) {
                         const int kl = it >> 1;                 // key within the stage
                         const int c = (it & 1) * 32 + lane;     // 16-byte chunk of the V row
-                        const int32_t slot = __shfl_sync(0xffffffffu, sl[q], kl);
+                        const int32_t slot = O.rows[rb2][32 * q + kl];
                         const __nv_bfloat16* src = a.kv + (slot >= 0 ? (int64_t)slot * kDqk : 0) + c * 8;
-                        cp_async_16_zfill(dst0 + (c >> 3) * kVBlock + sw128_offset(kl, c & 7), src,
-                                          slot >= 0);
+                        cp_async_16_zfill_nc(dst0 + (c >> 3) * kVBlock + sw128_offset(kl, c & 7), src,
+                                             slot >= 0);
                     }
                     cp_async_mbar_arrive_noinc(ba(O.v_full[st]));
                 }
-#pragma unroll
-                for (int q = 0; q < 8; ++q) sl[q] = nxt[q];
+                if (!ok) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ba(O.rows_free[rb2]));
             }
             cp_async_wait_all();
         } else if (warp == 1) {
@@ -544,7 +575,7 @@ partial_pair_kernel(const PartialArgs a) {
                 mbar_wait(ba(sm.h.drain), 0, &sm.h.no_abort);
             }
             __syncwarp();
-        } else if (warp < 6) {
+        } else {
             // ------------------------------------------------ correction + epilogue
             const int quarter = warp & 3;
             const int r = 32 * quarter + lane;

@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include "../tc_ptx.cuh"
+#include "../tmap.cuh"
 
 using namespace mlav::tc;
 
@@ -211,6 +212,186 @@ extern "C" __attribute__((visibility("default"))) int mlav_mma_rate(int N, int a
                                          (int)sizeof(ProbeSmem) + 1024);
     if (e != cudaSuccess) return (int)e;
     mma_rate_kernel<<<1, 128, sizeof(ProbeSmem) + 1024>>>(N, a_tmem, reps, nacc, overwrite, out, err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return (int)e;
+    return (int)cudaDeviceSynchronize();
+}
+
+namespace {
+
+struct GatherRows {
+    int r[8];
+};
+
+// TMA gather check: two tile::gather4 loads of 4 rows x 64 columns each into
+// a 1024-byte-aligned tile; the raw shared-memory bytes are copied out.
+__global__ void __launch_bounds__(128, 1)
+gather_probe_kernel(const __grid_constant__ CUtensorMap map, GatherRows rows, int x,
+                    uint4* out, int* err) {
+    __shared__ __align__(1024) unsigned char buf[1024];
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        mbar_arrive_expect_tx(smem_u32(&bar), 1024);
+        tma_gather4(smem_u32(buf), &map, x, rows.r[0], rows.r[1], rows.r[2], rows.r[3], smem_u32(&bar));
+        tma_gather4(smem_u32(buf) + 512, &map, x, rows.r[4], rows.r[5], rows.r[6], rows.r[7],
+                    smem_u32(&bar));
+    }
+    const bool ok = mbar_wait(smem_u32(&bar), 0, &abort_flag);
+    if (!ok && tid == 0) atomicExch(err, 1);
+    if (ok && tid < 64) out[tid] = reinterpret_cast<const uint4*>(buf)[tid];
+}
+
+}  // namespace
+
+extern "C" __attribute__((visibility("default"))) int mlav_gather_probe(const void* kv,
+                                                                        long long slots,
+                                                                        const int* rows_host, int x,
+                                                                        void* out, int* err) {
+    CUtensorMap map;
+    if (!mlav::make_kv_gather_map(&map, kv, slots)) return -2;
+    if (x < 0 || x > 512 || (x % 8) != 0) return -1;
+    GatherRows rows;
+    for (int i = 0; i < 8; ++i) rows.r[i] = rows_host[i];
+    gather_probe_kernel<<<1, 128>>>(map, rows, x, static_cast<uint4*>(out), err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return (int)e;
+    return (int)cudaDeviceSynchronize();
+}
+
+namespace {
+
+// Gather-throughput probe. Every CTA streams `ntile` tiles of 256 scattered
+// latent rows through a 4-stage ring of [256 keys x 64 dims] blocks (9 blocks
+// per tile), the layout the S side of the pair kernel consumes; a consumer
+// warp releases each stage as soon as it lands. The tile's slots are staged
+// in shared memory before its blocks are issued. Methods:
+//   0: cp.async, 8 lanes per key (one 128-byte line per 8 lanes), `nw` warps
+//   1: cp.async, one lane per key (8 slot registers per lane), `nw` warps
+//   2: tile::gather4 issued by the 32 lanes of one warp
+//   3: tile::gather4 issued by one thread
+constexpr int kGStages = 4;
+struct __align__(1024) GatherSmem {
+    unsigned char ring[kGStages][256 * 128];
+    int32_t rows[2][256];
+    uint64_t full[kGStages], empty[kGStages], rows_bar[2];
+    int abort_flag;
+};
+
+__global__ void __launch_bounds__(192, 1)
+gather_rate_kernel(const __grid_constant__ CUtensorMap map, const __nv_bfloat16* kv,
+                   const int32_t* slots, int ntile, int method, int nw, long long* cycles, int* err) {
+    extern __shared__ __align__(1024) unsigned char raw[];
+    unsigned char* base = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+    GatherSmem& g = *reinterpret_cast<GatherSmem*>(base);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nprod = method <= 1 ? nw : 1;
+    if (tid == 0) {
+        for (int i = 0; i < kGStages; ++i) {
+            mbar_init(smem_u32(&g.full[i]), method <= 1 ? 32 * nprod : 1);
+            mbar_init(smem_u32(&g.empty[i]), 1);
+        }
+        g.abort_flag = 0;
+        fence_mbar_init();
+    }
+    // all tiles' slots for this CTA fit two buffers only; preload tile 0 and 1 here
+    __syncthreads();
+    const int32_t* my = slots + (size_t)blockIdx.x * ntile * 256;
+    const long long t0 = clock64();
+    if (warp < nprod) {
+        for (int t = 0; t < ntile; ++t) {
+            // stage this tile's slots (each producer warp keeps its own copy in registers
+            // where needed; the shared copy serves methods 0, 2, 3)
+            __syncwarp();
+            if (warp == 0) {
+                for (int k = lane; k < 256; k += 32) g.rows[t & 1][k] = my[t * 256 + k];
+            }
+            asm volatile("bar.sync 2, %0;" ::"r"(32 * nprod) : "memory");
+            int32_t own[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) own[q] = g.rows[t & 1][32 * q + lane];
+            for (int blk = 0; blk < 9; ++blk) {
+                const int u = t * 9 + blk, st = u % kGStages;
+                if (u >= kGStages && !mbar_wait(smem_u32(&g.empty[st]), ((u / kGStages) - 1) & 1, &g.abort_flag)) {
+                    atomicExch(err, 1);
+                    goto done;
+                }
+                const uint32_t dst0 = smem_u32(g.ring[st]);
+                if (method == 0) {
+                    for (int it = warp; it < 64; it += nprod) {
+                        const int key = it * 4 + (lane >> 3), c = lane & 7;
+                        const int32_t sl = g.rows[t & 1][key];
+                        cp_async_16_zfill_nc(dst0 + sw128_offset(key, c),
+                                             kv + (int64_t)sl * 576 + blk * 64 + c * 8, true);
+                    }
+                    cp_async_mbar_arrive_noinc(smem_u32(&g.full[st]));
+                } else if (method == 1) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        if ((q % nprod) != warp) continue;
+                        const int key = 32 * q + lane;
+                        const __nv_bfloat16* src = kv + (int64_t)own[q] * 576 + blk * 64;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            cp_async_16_zfill_nc(dst0 + sw128_offset(key, c), src + c * 8, true);
+                    }
+                    cp_async_mbar_arrive_noinc(smem_u32(&g.full[st]));
+                } else if (method == 2) {
+                    if (lane == 0) mbar_arrive_expect_tx(smem_u32(&g.full[st]), 256 * 128);
+                    __syncwarp();
+                    for (int v = 0; v < 2; ++v) {
+                        const int gi = lane + 32 * v;
+                        const int32_t* r = &g.rows[t & 1][4 * gi];
+                        tma_gather4(dst0 + gi * 512, &map, blk * 64, r[0], r[1], r[2], r[3], smem_u32(&g.full[st]));
+                    }
+                } else {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(smem_u32(&g.full[st]), 256 * 128);
+                        for (int gi = 0; gi < 64; ++gi) {
+                            const int32_t* r = &g.rows[t & 1][4 * gi];
+                            tma_gather4(dst0 + gi * 512, &map, blk * 64, r[0], r[1], r[2], r[3], smem_u32(&g.full[st]));
+                        }
+                    }
+                    __syncwarp();
+                }
+            }
+        }
+        if (method <= 1) cp_async_wait_all();
+    } else if (warp == 5 && lane == 0) {
+        for (int u = 0; u < ntile * 9; ++u) {
+            const int st = u % kGStages;
+            if (!mbar_wait(smem_u32(&g.full[st]), (u / kGStages) & 1, &g.abort_flag)) {
+                atomicExch(err, 1);
+                break;
+            }
+            mbar_arrive(smem_u32(&g.empty[st]));
+        }
+        cycles[blockIdx.x] = clock64() - t0;
+    }
+done:
+    __syncthreads();
+}
+
+}  // namespace
+
+extern "C" __attribute__((visibility("default"))) int mlav_gather_rate(
+    const void* kv, long long pool, const int32_t* slots, int nblocks, int ntile, int method,
+    int nw, long long* cycles, int* err) {
+    CUtensorMap map;
+    if (!mlav::make_kv_gather_map(&map, kv, pool)) return -2;
+    if (nw < 1 || nw > 4 || method < 0 || method > 3) return -1;
+    const int smem = (int)sizeof(GatherSmem) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(gather_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return (int)e;
+    gather_rate_kernel<<<nblocks, 192, smem>>>(map, static_cast<const __nv_bfloat16*>(kv), slots, ntile,
+                                               method, nw, cycles, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;
     return (int)cudaDeviceSynchronize();

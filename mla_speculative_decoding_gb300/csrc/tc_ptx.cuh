@@ -69,6 +69,13 @@ __device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void* src,
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
                  : "memory");
 }
+// Same copy without a compiler memory barrier, so that independent index
+// loads can be scheduled ahead of it (the destination is only read after an
+// mbarrier wait, and volatile asm statements keep their relative order).
+__device__ __forceinline__ void cp_async_16_zfill_nc(uint32_t dst, const void* src, bool valid) {
+    const uint32_t n = valid ? 16u : 0u;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n));
+}
 // The mbarrier receives one arrival when all of this thread's earlier
 // cp.async copies have landed (the arrival counts toward the expected count).
 __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
@@ -247,6 +254,28 @@ __device__ __forceinline__ void fence_proxy_async_all() {
     asm volatile("fence.proxy.async;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ TMA
+// Adds `bytes` to the phase's expected transaction count and arrives once.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+// Four rows (y0..y3) x one box of columns starting at x of a 2-D tensor map
+// with a one-row box, written as four consecutive box rows at dst (the map's
+// swizzle applied); completion is counted in bytes on the mbarrier. Rows
+// outside the tensor read the fill value (zero).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int32_t x, int32_t y0,
+                                            int32_t y1, int32_t y2, int32_t y3, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
 // ------------------------------------------------------------------ descriptors
 // UMMA shared-memory matrix descriptor (sm_100 family): start address,
 // leading- and stride-dimension byte offsets (all >> 4), version 1, swizzle.
@@ -276,6 +305,13 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool a_mn, 
 // group.
 __host__ __device__ constexpr uint32_t sw128_offset(uint32_t r, uint32_t c) {
     return r * 128u + ((c ^ (r & 7u)) << 4);
+}
+
+// Hardware base-2 exponential (MUFU ex2, flush-to-zero); 2^0 is exactly 1.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

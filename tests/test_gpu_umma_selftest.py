@@ -58,3 +58,29 @@ def test_mnmajor_b(probe, mode, N):
     ok1 = torch.allclose(got1, ref, rtol=1e-4, atol=1e-3)
     print(f"mode {mode} N {N}: variant0 {ok0} variant1 {ok1}")
     assert ok0, f"variant 0 wrong (variant 1 {'right' if ok1 else 'also wrong'})"
+
+
+def test_tma_gather4_rows_and_zero_fill():
+    """tile::gather4 through the KV tensor map: 8 scattered rows x 64 columns land
+    as 128B-swizzled rows; an out-of-range row reads zeros."""
+    lib = ctypes.CDLL(B.build_selftest())
+    f = lib.mlav_gather_probe
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p, ctypes.c_int,
+                  ctypes.c_void_p, ctypes.c_void_p]
+    slots = 1000
+    g = torch.Generator().manual_seed(3)
+    kv = torch.randn(slots, 576, generator=g).to(torch.bfloat16)
+    dkv = kv.cuda()
+    rows = [5, 999, 0, 17, slots, 512, 3, 770]   # one out-of-range row
+    for x in (0, 64, 512):
+        out = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        rc = f(dkv.data_ptr(), slots, (ctypes.c_int * 8)(*rows), x, out.data_ptr(), err.data_ptr())
+        assert rc == 0 and int(err.item()) == 0, rc
+        raw = out.cpu().view(torch.int16).view(8, 8, 8)  # [row][16B chunk][8 bf16]
+        for i, r in enumerate(rows):
+            want = (kv[r, x:x + 64].view(torch.int16).view(8, 8) if r < slots
+                    else torch.zeros(8, 8, dtype=torch.int16))
+            for c in range(8):
+                assert torch.equal(raw[i, c ^ (i % 8)], want[c]), (x, i, c)
