@@ -14,9 +14,9 @@
 //     36 per tile). TMEM: Q's 512 latent dims [0, 256) as the A operand, S
 //     [256, 512). Q's 64 RoPE dims are an A operand in shared memory. K is
 //     streamed in 64-dim blocks of 256 keys (32 KB, 6-stage ring), gathered
-//     from the scattered rows by three warps of 16-byte cp.async copies (eight
-//     lanes per 128-byte row segment; measured faster than TMA gather4 for
-//     this pattern). Eight softmax warps (two per
+//     from the scattered rows by seven warps of 16-byte cp.async copies
+//     (eight lanes per 128-byte row segment; measured faster than TMA gather4
+//     for this pattern). Eight softmax warps (two per
 //     TMEM lane quarter, one per 128-key half) copy S out of TMEM at once
 //     (freeing it for the next tile's MMAs), mask it (tree mask only past the
 //     prefix), exchange the per-row tile maximum, keep a lazily updated
@@ -24,14 +24,16 @@
 //     2^8), and store P as bf16 straight into the O-CTA's shared memory
 //     (distributed shared memory), with the per-row rescale factor.
 //   O-CTA (rank 1): O += P V with TMEM O = [0, 512) (two N = 256 accumulator
-//     chains, one per half of the V dims). V rows are gathered by seven warps
-//     of cp.async copies in 32-key stages (32 KB, 4-stage ring). Four
+//     chains, one per half of the V dims). V rows are gathered by eleven
+//     warps of cp.async copies in 32-key stages (32 KB, 4-stage ring). Four
 //     correction warps apply the rare
 //     rescales to O between tiles and, at the end, normalise O and write the
 //     partial (o, lse).
 //
-// Every wait is bounded; on a timeout a CTA drains its MMAs, frees TMEM,
-// reaches the final cluster barrier and flags MLA_STATUS_TIMEOUT.
+// 16 warps: the producer and MMA warpgroups give registers to the softmax
+// warpgroups (setmaxnreg). Every wait is bounded; on a timeout a CTA drains
+// its MMAs, frees TMEM, reaches the final cluster barrier and flags
+// MLA_STATUS_TIMEOUT.
 #include "partial_tc.cuh"
 #include "tc_ptx.cuh"
 
@@ -42,9 +44,14 @@ using namespace tc;
 
 constexpr int kM = 128;
 constexpr int kNT = 256;          // keys per tile
-constexpr int kThreads = 384;     // 12 warps
-constexpr int kSProd = 3;         // S-side producer warps: 0, 10, 11
-constexpr int kOProd = 7;         // O-side producer warps: 0, 6..11
+constexpr int kThreads = 512;     // 16 warps = 4 warpgroups
+constexpr int kWarpMMA = 4;
+constexpr int kSProd = 7;         // S-side producer warps: 0-3, 5-7
+constexpr int kOProd = 11;        // O-side producer warps: 0-3, 5-7, 12-15
+// Register budget: launched at 128 per thread (512 x 128 = 65,536). S-CTA:
+// warpgroups 0-1 drop to 64, the two softmax warpgroups rise to 192
+// (256 x 64 + 256 x 192 = 65,536). O-CTA: warpgroups 0, 1, 3 drop to 64.
+constexpr int kRegsLow = 64, kRegsSoftmax = 192;
 constexpr int kKStages = 6;
 constexpr uint32_t kKBlock = kNT * 128;        // 256 keys x 64 dims (bf16)
 constexpr int kMetaRing = 4;
@@ -133,7 +140,7 @@ partial_pair_kernel(const PartialArgs a) {
     const int64_t kbase = a.kv_indptr[b];
 
     if (ntiles <= 0) {  // empty split (fixed grid, early exit): lse = -inf, o = 0
-        if (rank == 1 && warp >= 2 && warp < 6) {
+        if (rank == 1 && warp >= 8 && warp < 12) {
             const int grow = rb * kM + 32 * (warp & 3) + lane;
             if (grow < rows_req) {
                 const int64_t pid = ((int64_t)b * rows_req + grow) * a.nsplit + s;
@@ -147,7 +154,7 @@ partial_pair_kernel(const PartialArgs a) {
     }
     if (rank != 0) bad &= ~MLA_STATUS_BAD_INDPTR;  // reported once, by the S-CTA
 
-    if (warp == 1) {
+    if (warp == kWarpMMA) {
         tmem_alloc(smem_u32(&sm.h.tmem_base), 512);
         tmem_relinquish();
     }
@@ -200,14 +207,16 @@ partial_pair_kernel(const PartialArgs a) {
     volatile int* abort_p = &sm.h.abort_flag;
     const uint32_t peer = rank ^ 1u;
 
-    if (rank == 0) {
+    const int wg = warp >> 2;
+    if (rank == 0 && wg < 2) {
+        regs_dec<kRegsLow>();
         SmemS& S = sm.u.s;
-        if (warp == 0 || warp >= 10) {
+        if (warp != kWarpMMA) {
             // ------------------------------------------------ S producers: K blocks
             // Warp 0 stages each tile's pool rows (and the key-validity bits
-            // for the softmax); warps 0, 10, 11 split the 16-byte copies, eight
-            // lanes per 128-byte row segment.
-            const int pw = warp == 0 ? 0 : warp - 9;  // 0..2
+            // for the softmax); warps 0-3 and 5-7 split the 16-byte copies,
+            // eight lanes per 128-byte row segment.
+            const int pw = warp < kWarpMMA ? warp : warp - 1;  // 0..6
             bool ok = warp_wait(S.q_ready, 0, abort_p);  // the ring doubles as Q staging
             for (int i = 0; ok && i < ntiles; ++i) {
                 const int rb2 = i & 1;
@@ -268,7 +277,7 @@ partial_pair_kernel(const PartialArgs a) {
                 if (lane == 0) mbar_arrive(ba(S.rows_free[rb2]));
             }
             cp_async_wait_all();
-        } else if (warp == 1) {
+        } else {
             // ------------------------------------------------ S MMA issuer
             if (lane == 0) {
                 const uint32_t idesc = make_idesc_bf16(kM, kNT, false, false);
@@ -311,16 +320,20 @@ partial_pair_kernel(const PartialArgs a) {
                 mbar_wait(ba(sm.h.drain), 0, &sm.h.no_abort);
             }
             __syncwarp();
-        } else {
-            // ------------------------------------------------ softmax (8 warps)
+        }
+    } else if (rank == 0) {
+        regs_inc<kRegsSoftmax>();
+        SmemS& S = sm.u.s;
+        {
+            // ------------------------------------------------ softmax (warps 8-15)
             const int quarter = warp & 3;
-            const int half = (warp - 2) >> 2;     // 128-key half of the tile
+            const int half = (warp - 8) >> 2;     // 128-key half of the tile
             const int r = 32 * quarter + lane;     // row = TMEM lane
             const int grow = rb * kM + r;
             const bool row_ok = grow < rows_req;
             const int t = row_ok ? grow / H : 0;
             const uint32_t lb = (uint32_t)(32 * quarter) << 16;
-            const int stid = tid - 64;             // 0..255
+            const int stid = tid - 256;            // 0..255
 
             // Q staging: latent dims into the K ring (padded rows), RoPE dims
             // straight into their swizzled A-operand tile.
@@ -467,13 +480,14 @@ partial_pair_kernel(const PartialArgs a) {
                 mbar_arrive_cluster(mapa_shared(ba(sm.h.fin), peer));
             }
         }
-    } else {
+    } else if (wg != 2) {
+        regs_dec<kRegsLow>();
         SmemO& O = sm.u.o;
-        if (warp == 0 || warp >= 6) {
+        if (warp != kWarpMMA) {
             // ------------------------------------------------ O producers: V rows
-            // Warp 0 stages each tile's pool rows; warps 0, 6..11 split the
-            // 16-byte copies (32 lanes = one half of a 1024-byte V row).
-            const int pw = warp == 0 ? 0 : warp - 5;  // 0..6
+            // Warp 0 stages each tile's pool rows; warps 0-3, 5-7 and 12-15
+            // split the 16-byte copies (32 lanes = one half of a 1024-byte V row).
+            const int pw = warp < kWarpMMA ? warp : (warp < 8 ? warp - 1 : warp - 5);  // 0..10
             bool ok = true;
             for (int i = 0; ok && i < ntiles; ++i) {
                 const int rb2 = i & 1;
@@ -522,7 +536,7 @@ partial_pair_kernel(const PartialArgs a) {
                 if (lane == 0) mbar_arrive(ba(O.rows_free[rb2]));
             }
             cp_async_wait_all();
-        } else if (warp == 1) {
+        } else {
             // ------------------------------------------------ O MMA issuer
             if (lane == 0) {
                 const uint32_t idesc = make_idesc_bf16(kM, 256, false, true);
@@ -575,7 +589,10 @@ partial_pair_kernel(const PartialArgs a) {
                 mbar_wait(ba(sm.h.drain), 0, &sm.h.no_abort);
             }
             __syncwarp();
-        } else {
+        }
+    } else {
+        SmemO& O = sm.u.o;
+        {
             // ------------------------------------------------ correction + epilogue
             const int quarter = warp & 3;
             const int r = 32 * quarter + lane;
@@ -639,7 +656,7 @@ partial_pair_kernel(const PartialArgs a) {
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();  // no CTA leaves while its peer may still touch its shared memory
-    if (warp == 1) {
+    if (warp == kWarpMMA) {
         tc_fence_after();
         tmem_dealloc(tbase, 512);
     }

@@ -396,3 +396,87 @@ extern "C" __attribute__((visibility("default"))) int mlav_gather_rate(
     if (e != cudaSuccess) return (int)e;
     return (int)cudaDeviceSynchronize();
 }
+
+namespace {
+
+// DSMEM bulk-copy throughput: CTA 0 of each 2-CTA cluster sends `nchunk`
+// chunks of `chunk` bytes from its shared memory into CTA 1's, through a
+// 4-slot ring (CTA 1 releases a slot once it has landed, by a remote arrive).
+// Reports cycles per sending CTA. The payload is checked on the receiver.
+struct __align__(1024) BulkSmem {
+    unsigned char buf[4][32768];
+    uint64_t full[4], empty[4];
+    int abort_flag;
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
+bulk_rate_kernel(int chunk, int nchunk, long long* cycles, int* err) {
+    extern __shared__ __align__(1024) unsigned char raw[];
+    unsigned char* base = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+    BulkSmem& b = *reinterpret_cast<BulkSmem*>(base);
+    const uint32_t rank = cluster_ctarank();
+    const int tid = threadIdx.x;
+    for (int i = tid; i < 4 * 32768 / 16; i += 128)
+        reinterpret_cast<uint4*>(b.buf)[i] = make_uint4(rank == 0 ? (uint32_t)i : 0u, 7u, 0, 0);
+    if (tid == 0) {
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(smem_u32(&b.full[i]), 1);
+            mbar_init(smem_u32(&b.empty[i]), 1);
+        }
+        b.abort_flag = 0;
+        fence_mbar_init();
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    cluster_sync_all();
+    if (tid == 0) {
+        const long long t0 = clock64();
+        if (rank == 0) {
+            for (int c = 0; c < nchunk; ++c) {
+                const int st = c & 3;
+                if (c >= 4 && !mbar_wait(smem_u32(&b.empty[st]), ((c >> 2) - 1) & 1, &b.abort_flag)) {
+                    atomicExch(err, 1);
+                    break;
+                }
+                bulk_copy_to_peer(mapa_shared(smem_u32(b.buf[st]), 1), smem_u32(b.buf[st]),
+                                  (uint32_t)chunk, mapa_shared(smem_u32(&b.full[st]), 1));
+            }
+            // the receiver's last release marks the end
+            const int c = nchunk + 3;
+            if (nchunk >= 1) mbar_wait(smem_u32(&b.empty[(nchunk - 1) & 3]), ((nchunk - 1) >> 2) & 1, &b.abort_flag);
+            (void)c;
+            cycles[blockIdx.x / 2] = clock64() - t0;
+        } else {
+            for (int c = 0; c < nchunk; ++c) {
+                const int st = c & 3;
+                mbar_arrive_expect_tx(smem_u32(&b.full[st]), (uint32_t)chunk);
+                if (!mbar_wait(smem_u32(&b.full[st]), (c >> 2) & 1, &b.abort_flag)) {
+                    atomicExch(err, 1);
+                    break;
+                }
+                if (c == nchunk - 1) {
+                    const uint4 v = reinterpret_cast<const uint4*>(b.buf[st])[chunk / 16 - 1];
+                    if (v.y != 7u) atomicExch(err, 2);
+                }
+                mbar_arrive_cluster(mapa_shared(smem_u32(&b.empty[st]), 0));
+            }
+        }
+    }
+    __syncthreads();
+    cluster_sync_all();
+}
+
+}  // namespace
+
+extern "C" __attribute__((visibility("default"))) int mlav_bulk_rate(int nclusters, int chunk,
+                                                                     int nchunk, long long* cycles,
+                                                                     int* err) {
+    if (chunk < 16 || chunk > 32768 || (chunk % 16) != 0 || nchunk < 1 || nclusters < 1) return -1;
+    const int smem = (int)sizeof(BulkSmem) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(bulk_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return (int)e;
+    bulk_rate_kernel<<<2 * nclusters, 128, smem>>>(chunk, nchunk, cycles, err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return (int)e;
+    return (int)cudaDeviceSynchronize();
+}
