@@ -34,6 +34,7 @@ MLA_STATUS_TIMEOUT = 0x40
 
 MLA_PARTIAL_SIMT = 0x1
 MLA_PARTIAL_TC_QUARTER = 0x2
+MLA_PARTIAL_PAIR = 0x4
 D_QK = 576
 D_V = 512
 

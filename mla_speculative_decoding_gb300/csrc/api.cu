@@ -43,7 +43,7 @@ int init_device(int device) {
     } else if (major != 10 || minor != 3) {
         rc = MLA_ERR_UNSUPPORTED;  // the library carries sm_103a code only
     } else if (setup_partial_simt() != cudaSuccess || setup_partial_tc() != cudaSuccess ||
-               setup_partial_pair() != cudaSuccess) {
+               setup_partial_pair() != cudaSuccess || setup_partial_quad() != cudaSuccess) {
         rc = MLA_ERR_CUDA;
     }
     if (rc == MLA_OK) {
@@ -142,8 +142,10 @@ int run_partial(const PartialArgs& a, unsigned flags, int sm_count, cudaStream_t
         e = launch_partial_simt(a, stream);
     else if ((flags & MLA_PARTIAL_TC_QUARTER) && partial_tc_supported(a))
         e = launch_partial_tc(a, sm_count, stream);
-    else
+    else if ((flags & MLA_PARTIAL_PAIR) || a.T * a.H <= 128)
         e = launch_partial_pair(a, stream);
+    else
+        e = launch_partial_quad(a, stream);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -272,7 +274,8 @@ MLAV_API int mla_verify_partial(const void* q, const void* kv_pool, const int32_
                                 anc_mask, T, nsplit, workspace, batch, num_heads, pool_slots,
                                 softmax_scale, workspace_bytes);
     if (rc != MLA_OK) return rc;
-    if (flags & ~(MLA_PARTIAL_SIMT | MLA_PARTIAL_TC_QUARTER)) return MLA_ERR_INVALID_ARG;
+    if (flags & ~(MLA_PARTIAL_SIMT | MLA_PARTIAL_TC_QUARTER | MLA_PARTIAL_PAIR))
+        return MLA_ERR_INVALID_ARG;
     int sms = 0;
     rc = ensure_ready(stream, &sms);
     if (rc != MLA_OK) return rc;

@@ -1,0 +1,758 @@
+// Split-KV partial attention on two pairs of SMs with 2-SM (cta_group::2)
+// tensor-core MMAs: four SMs per 256-row work item.
+//
+// The verify attention of "The Custom sm_120 Verify Kernel..." (Parts VI,
+// VII, IX): every tree-token x head row of a request attends over the
+// request's scattered latent KV rows (prefix unmasked, tree block masked),
+// in a KV-split "partial + reduce" design.
+//
+// Work item = (256-row block of the request's T*H rows, split s, request b),
+// run by a cluster of four CTAs. A pair MMA (M = 256) keeps 128 rows of the
+// accumulator in each SM of the pair and reads half of the B operand's N
+// columns from each SM's shared memory, so every gathered byte feeds 256
+// rows while each SM gathers only half of the tile:
+//
+//   S pair (ranks 0, 1): S = Q K^T for 256-key tiles, M = 256, N = 256
+//     (36 pair MMAs per tile, issued by rank 0). Rank r holds rows
+//     [128r, 128r + 128) of the block (Q's 512 latent dims in TMEM [0, 256)
+//     as the A operand, the 64 RoPE dims in shared memory) and gathers keys
+//     [128r, 128r + 128) of every tile (all 576 dims, 64-dim blocks of 16 KB
+//     in an 8-stage ring). S lands in TMEM [256, 512) of each SM: 128 rows x
+//     256 keys. Eight softmax warps per SM copy S out of TMEM, mask it, keep
+//     a lazily rescaled running maximum, and write P (bf16) into a local
+//     staging tile, which one thread sends to the O partner of the same rows
+//     (rank r + 2) with a bulk shared-memory copy.
+//   O pair (ranks 2, 3): O += P V, M = 256, two N = 256 chains (V dims
+//     [0, 256) and [256, 512)), issued by rank 2; rank 2 + r holds O for rows
+//     [128r, 128r + 128) in TMEM [0, 512) and gathers, for all 256 keys of a
+//     tile, its half of each chain's V columns: 64-dim segments
+//     {2r, 2r + 1, 4 + 2r, 5 + 2r}. P arrives double-buffered, so P of the
+//     next tile is written while this tile's P V runs. Four correction warps
+//     per SM apply the rare rescales to O and write the partial (o, lse).
+//
+// Operand readiness across a pair: each CTA's copies land on its own
+// mbarrier; the odd CTA's MMA warp forwards each completed stage to the
+// even CTA's barrier with a cluster-scope arrive. MMA completion is committed
+// to the barriers of both CTAs of the pair (multicast).
+//
+// Every wait is bounded; on a timeout a CTA drains its MMAs, reaches the
+// final cluster barrier, frees TMEM and flags MLA_STATUS_TIMEOUT.
+#include "partial_tc.cuh"
+#include "tc_ptx.cuh"
+
+namespace mlav {
+namespace {
+
+using namespace tc;
+
+constexpr int kRowsBlk = 256;     // rows per work item
+constexpr int kMh = 128;          // rows per CTA
+constexpr int kNT = 256;          // keys per tile
+constexpr int kNh = 128;          // keys per S-CTA per tile
+constexpr int kThreads = 512;     // 16 warps = 4 warpgroups
+constexpr int kWarpMMA = 4;
+constexpr int kSProd = 7;         // S-side producer warps: 0-3, 5-7
+constexpr int kOProd = 11;        // O-side producer warps: 0-3, 5-7, 12-15
+// Launched at 128 registers per thread (512 x 128 = 65,536). S CTAs:
+// warpgroups 0-1 drop to 72 and the softmax warpgroups rise to 184
+// (256 x 72 + 256 x 184 = 65,536). O CTAs: warpgroups 0, 1, 3 drop to 72.
+constexpr int kRegsLow = 72, kRegsSoftmax = 184;
+constexpr int kKStages = 8;
+constexpr uint32_t kKBlock = kNh * 128;        // 128 keys x 64 dims (bf16) = 16 KB
+constexpr int kMetaRing = 4;
+constexpr int kVKeys = 32;
+constexpr int kVStages = 4;
+constexpr uint32_t kVSub = kVKeys * 128;       // 32 keys x 64 dims = 4 KB
+constexpr uint32_t kVStage = 4 * kVSub;        // [chain][segment][32 keys][64 dims]
+constexpr uint32_t kPBlock = kMh * 128;        // 128 rows x 64 keys (bf16)
+constexpr uint32_t kPBytes = 4 * kPBlock;      // 128 rows x 256 keys
+constexpr uint32_t kPXfer = kPBytes + kMh * 4; // P + per-row rescale factors
+constexpr uint32_t kPSlot = 67584;             // 1024-aligned P slot
+constexpr uint32_t kQStageStride = 1040;       // padded staging row of 512 bf16
+constexpr uint32_t kColQ = 0, kColS = 256;     // S-CTA TMEM map
+constexpr float kRescaleLog2 = 8.0f;
+
+struct SmemS {
+    unsigned char q_rope[kMh * 128];            // [128 rows x 64 dims], 128B-swizzled
+    unsigned char kring[kKStages][kKBlock];     // [128 keys x 64 dims] per stage
+    unsigned char pstage[kPXfer];               // P [4 x (128 rows x 64 keys)] + alpha[128]
+    uint32_t valid[kMetaRing][kNT / 32];
+    int32_t rows[2][kNT];                       // pool rows of the tiles being gathered
+    float mx[2][2][kMh];
+    uint64_t anc[MLA_MAX_TREE];
+    int32_t par[MLA_MAX_TREE];
+    uint64_t k_full[kKStages], k_empty[kKStages];
+    uint64_t meta_full[kMetaRing], meta_free[kMetaRing];
+    uint64_t s_full, s_free, q_ready, q_peer, mx_bar[2], pw_bar[2];
+    uint64_t rows_full[2], rows_free[2];
+    uint64_t p_free[2];
+};
+struct SmemO {
+    unsigned char pbuf[2][kPSlot];              // P + alpha, one slot per tile parity
+    unsigned char vring[kVStages][kVStage];
+    int32_t rows[2][kNT];
+    float fin_m[kMh];
+    float fin_l[2][kMh];
+    uint64_t v_full[kVStages], v_empty[kVStages];
+    uint64_t p_full[2], o_gate[2], o_done[2], fin;
+    uint64_t rows_full[2], rows_free[2];
+};
+struct Header {
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int no_abort;
+};
+struct __align__(1024) SmemQuad {
+    union {
+        SmemS s;
+        SmemO o;
+    } u;
+    Header h;
+};
+
+constexpr size_t kSmemBytes = sizeof(SmemQuad) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kMh * kQStageStride <= kKStages * kKBlock + kPXfer,
+              "Q staging must fit in the K ring and the P staging tile");
+static_assert(kPXfer <= kPSlot && kPSlot % 1024 == 0, "P slot");
+
+__device__ __forceinline__ uint32_t ba(const uint64_t& b) { return smem_u32(&b); }
+
+__device__ __forceinline__ bool warp_wait(const uint64_t& bar, uint32_t parity,
+                                          volatile int* abort) {
+    const bool ok = mbar_wait(ba(bar), parity, abort);
+    return __all_sync(0xffffffffu, ok);
+}
+__device__ __forceinline__ bool warp_wait_cluster(const uint64_t& bar, uint32_t parity,
+                                                  volatile int* abort) {
+    const bool ok = mbar_wait_cluster(ba(bar), parity, abort);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Pool rows of one 256-key tile (and, for the softmax, their validity bits).
+// Returns MLA_STATUS_BAD_SLOT if a slot was out of range (that key is masked).
+__device__ __forceinline__ int stage_rows(const PartialArgs& a, int64_t kbase, int j0, int ke,
+                                          int lane, int32_t* rows, uint32_t* valid) {
+    int bad = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const int j = j0 + 32 * q + lane;
+        int32_t v = -1;
+        if (j < ke) {
+            v = a.kv_indices[kbase + j];
+            if (v < 0 || (int64_t)v >= a.pool_slots) {
+                bad |= MLA_STATUS_BAD_SLOT;
+                v = -1;
+            }
+        }
+        rows[32 * q + lane] = v;
+        if (valid != nullptr) {
+            const uint32_t w = __ballot_sync(0xffffffffu, v >= 0);
+            if (lane == q) valid[q] = w;
+        }
+    }
+    return bad;
+}
+
+__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
+partial_quad_kernel(const PartialArgs a) {
+    extern __shared__ __align__(1024) unsigned char raw[];
+    unsigned char* base = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+    SmemQuad& sm = *reinterpret_cast<SmemQuad*>(base);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool sside = rank < 2;
+    const uint32_t hr = rank & 1u;            // row half (and B-operand half) of this CTA
+    const int rb = blockIdx.x >> 2;
+    const int s = blockIdx.y, b = blockIdx.z;
+    const int T = a.T, H = a.H, rows_req = T * H;
+    const int row0 = rb * kRowsBlk + (int)hr * kMh;  // first request row of this CTA
+
+    int Lb, K;
+    int bad = request_keys(a, b, Lb, K);
+    int kb, ke;
+    split_range(K, a.nsplit, s, kb, ke);
+    const int ntiles = (ke - kb + kNT - 1) / kNT;
+    const int64_t kbase = a.kv_indptr[b];
+
+    if (ntiles <= 0) {  // empty split (fixed grid, early exit): lse = -inf, o = 0
+        if (!sside && warp >= 8 && warp < 12) {
+            const int grow = row0 + 32 * (warp & 3) + lane;
+            if (grow < rows_req) {
+                const int64_t pid = ((int64_t)b * rows_req + grow) * a.nsplit + s;
+                float4* o = reinterpret_cast<float4*>(a.o_part + pid * kDv);
+                for (int c = 0; c < kDv / 4; ++c) o[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                a.lse_part[pid] = -INFINITY;
+            }
+        }
+        if (rank == 0 && tid == 0) status_or(a.status, bad);
+        return;
+    }
+    if (rank != 0) bad &= ~MLA_STATUS_BAD_INDPTR;  // reported once
+
+    if (warp == kWarpMMA) {  // both CTAs of each pair allocate together
+        tmem_alloc_pair(smem_u32(&sm.h.tmem_base), 512);
+        tmem_relinquish_pair();
+    }
+    if (tid == 0) {
+        mbar_init(ba(sm.h.drain), 1);
+        if (sside) {
+            SmemS& S = sm.u.s;
+            for (int i = 0; i < kKStages; ++i) {
+                mbar_init(ba(S.k_full[i]), 32 * kSProd + (rank == 0 ? 1 : 0));
+                mbar_init(ba(S.k_empty[i]), 1);
+            }
+            for (int i = 0; i < kMetaRing; ++i) {
+                mbar_init(ba(S.meta_full[i]), 1);
+                mbar_init(ba(S.meta_free[i]), 256);
+            }
+            mbar_init(ba(S.s_full), 1);
+            mbar_init(ba(S.s_free), 16);
+            mbar_init(ba(S.q_ready), 256);
+            mbar_init(ba(S.q_peer), 1);
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(ba(S.mx_bar[i]), 256);
+                mbar_init(ba(S.pw_bar[i]), 256);
+                mbar_init(ba(S.rows_full[i]), 1);
+                mbar_init(ba(S.rows_free[i]), kSProd);
+                mbar_init(ba(S.p_free[i]), 1);
+            }
+        } else {
+            SmemO& O = sm.u.o;
+            for (int i = 0; i < kVStages; ++i) {
+                mbar_init(ba(O.v_full[i]), 32 * kOProd + (rank == 2 ? 1 : 0));
+                mbar_init(ba(O.v_empty[i]), 1);
+            }
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(ba(O.p_full[i]), 1);
+                mbar_init(ba(O.o_gate[i]), 8);
+                mbar_init(ba(O.o_done[i]), 1);
+                mbar_init(ba(O.rows_full[i]), 1);
+                mbar_init(ba(O.rows_free[i]), kOProd);
+            }
+            mbar_init(ba(O.fin), 256);
+        }
+        sm.h.abort_flag = 0;
+        sm.h.no_abort = 0;
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // every CTA's barriers exist before any remote arrive
+    tc_fence_after();
+    const uint32_t tbase = sm.h.tmem_base;
+    volatile int* abort_p = &sm.h.abort_flag;
+
+    const int wg = warp >> 2;
+    if (sside && wg < 2) {
+        regs_dec<kRegsLow>();
+        SmemS& S = sm.u.s;
+        if (warp != kWarpMMA) {
+            // ------------------------------------------------ S producers: K blocks
+            // Warp 0 stages each tile's pool rows (all 256, with validity bits
+            // for the softmax); the seven producer warps copy this CTA's 128
+            // keys, eight lanes per 128-byte row segment.
+            const int pw = warp < kWarpMMA ? warp : warp - 1;  // 0..6
+            bool ok = warp_wait(S.q_ready, 0, abort_p);  // the ring doubles as Q staging
+            for (int i = 0; ok && i < ntiles; ++i) {
+                const int rb2 = i & 1;
+                if (pw == 0) {
+                    if (i >= 2 && !warp_wait(S.rows_free[rb2], ((i >> 1) - 1) & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    const int mi = i % kMetaRing;
+                    if (i >= kMetaRing && !warp_wait(S.meta_free[mi], ((i / kMetaRing) - 1) & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    bad |= stage_rows(a, kbase, kb + i * kNT, ke, lane, S.rows[rb2], S.valid[mi]);
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(ba(S.meta_full[mi]));
+                        mbar_arrive(ba(S.rows_full[rb2]));
+                    }
+                }
+                if (!warp_wait(S.rows_full[rb2], (i >> 1) & 1, abort_p)) {
+                    ok = false;
+                    break;
+                }
+                const int32_t* my_rows = S.rows[rb2] + hr * kNh;
+                for (int kbk = 0; kbk < kDqk / 64; ++kbk) {
+                    const int g = i * (kDqk / 64) + kbk;
+                    const int st = g % kKStages;
+                    if (g >= kKStages && !warp_wait(S.k_empty[st], ((g / kKStages) - 1) & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst0 = smem_u32(S.kring[st]);
+                    for (int it = pw; it < kNh / 4; it += kSProd) {
+                        const int key = it * 4 + (lane >> 3), c = lane & 7;
+                        const int32_t slot = my_rows[key];
+                        const __nv_bfloat16* src =
+                            a.kv + (slot >= 0 ? (int64_t)slot * kDqk : 0) + kbk * 64 + c * 8;
+                        cp_async_16_zfill_nc(dst0 + sw128_offset(key, c), src, slot >= 0);
+                    }
+                    cp_async_mbar_arrive_noinc(ba(S.k_full[st]));
+                }
+                if (!ok) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ba(S.rows_free[rb2]));
+            }
+            cp_async_wait_all();
+        } else if (rank == 0) {
+            // ------------------------------------------------ S MMA issuer (pair)
+            if (lane == 0) {
+                const uint32_t idesc = make_idesc_bf16(kRowsBlk, kNT, false, false);
+                bool ok = mbar_wait(ba(S.q_ready), 0, abort_p) &&
+                          mbar_wait_cluster(ba(S.q_peer), 0, abort_p);
+                fence_proxy_async_smem();
+                tc_fence_after();
+                const uint32_t dS = tbase + kColS;
+                const uint32_t qr = smem_u32(S.q_rope);
+                for (int i = 0; ok && i < ntiles; ++i) {
+                    if (i >= 1 && !mbar_wait_cluster(ba(S.s_free), (i - 1) & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int kbk = 0; kbk < kDqk / 64; ++kbk) {
+                        const int g = i * (kDqk / 64) + kbk;
+                        const int st = g % kKStages;
+                        if (!mbar_wait_cluster(ba(S.k_full[st]), (g / kKStages) & 1, abort_p)) {
+                            ok = false;
+                            break;
+                        }
+                        fence_proxy_async_smem();
+                        tc_fence_after();
+                        const uint32_t kt = smem_u32(S.kring[st]);
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint64_t bd = make_sdesc(kt + ks * 32, 16, 1024, kSwizzle128B);
+                            const uint32_t acc = (kbk | ks) ? 1u : 0u;
+                            if (kbk < 8)
+                                mma_ts_pair(dS, tbase + kColQ + kbk * 32 + ks * 8, bd, idesc, acc);
+                            else
+                                mma_ss_pair(dS, make_sdesc(qr + ks * 32, 16, 1024, kSwizzle128B), bd,
+                                            idesc, acc);
+                        }
+                        mma_commit_pair_mc(ba(S.k_empty[st]), 0x3);
+                    }
+                    if (ok) mma_commit_pair_mc(ba(S.s_full), 0x3);
+                }
+                mma_commit_pair_mc(ba(sm.h.drain), 0x1);
+                mbar_wait(ba(sm.h.drain), 0, &sm.h.no_abort);
+            }
+            __syncwarp();
+        } else {
+            // ------------------------------------------------ rank 1: forward readiness to rank 0
+            if (lane == 0) {
+                bool ok = mbar_wait(ba(S.q_ready), 0, abort_p);
+                tc_fence_after();
+                tc_fence_before();
+                if (ok) mbar_arrive_cluster(mapa_shared(ba(S.q_peer), 0));
+                const int nfill = ntiles * (kDqk / 64);
+                for (int g = 0; ok && g < nfill; ++g) {
+                    const int st = g % kKStages;
+                    if (!mbar_wait(ba(S.k_full[st]), (g / kKStages) & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive_cluster(mapa_shared(ba(S.k_full[st]), 0));
+                }
+            }
+            __syncwarp();
+        }
+    } else if (sside) {
+        regs_inc<kRegsSoftmax>();
+        SmemS& S = sm.u.s;
+        {
+            // ------------------------------------------------ softmax (warps 8-15)
+            const int quarter = warp & 3;
+            const int half = (warp - 8) >> 2;     // 128-key half of the tile
+            const int r = 32 * quarter + lane;     // row = TMEM lane
+            const int grow = row0 + r;
+            const bool row_ok = grow < rows_req;
+            const int t = row_ok ? grow / H : 0;
+            const uint32_t lb = (uint32_t)(32 * quarter) << 16;
+            const int stid = tid - 256;            // 0..255
+            const uint32_t orank = 2u + hr;        // O partner holding the same rows
+
+            // Q staging: latent dims into the K ring (padded rows), RoPE dims
+            // straight into their swizzled A-operand tile.
+            {
+                const uint32_t stage0 = smem_u32(S.kring[0]);
+                const __nv_bfloat16* q0 = a.q + ((int64_t)b * rows_req + row0) * kDqk;
+                for (int f = stid; f < kMh * (kDqk / 8); f += 256) {
+                    const int rr = f / (kDqk / 8), c = f % (kDqk / 8);
+                    const bool v = row0 + rr < rows_req;
+                    const __nv_bfloat16* src = v ? q0 + (int64_t)rr * kDqk + c * 8 : a.q;
+                    const uint32_t dst = c < 64 ? stage0 + rr * kQStageStride + c * 16
+                                                : smem_u32(S.q_rope) + sw128_offset(rr, c - 64);
+                    cp_async_16_zfill(dst, src, v);
+                }
+                if (stid < T) {
+                    if (a.anc_mask != nullptr)
+                        S.anc[stid] = a.anc_mask[(int64_t)b * T + stid];
+                    else
+                        S.par[stid] = a.tree_parent[(int64_t)b * T + stid];
+                }
+                cp_async_wait_all();
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                if (stid == 0 && a.anc_mask == nullptr) bad |= build_anc_serial(S.par, T, S.anc);
+                if (half == 0) {
+                    const unsigned char* row = S.kring[0] + r * kQStageStride;
+#pragma unroll 1
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t w[32];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(row + c * 128 + u * 16);
+                            w[4 * u] = v.x;
+                            w[4 * u + 1] = v.y;
+                            w[4 * u + 2] = v.z;
+                            w[4 * u + 3] = v.w;
+                        }
+                        tmem_st32(tbase + lb + kColQ + c * 32, w);
+                    }
+                    tmem_wait_st();
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                mbar_arrive(ba(S.q_ready));
+            }
+            const uint64_t anc_t = S.anc[t];
+            const uint32_t p_local = smem_u32(S.pstage);
+            float* alpha_local = reinterpret_cast<float*>(S.pstage + kPBytes);
+            const uint32_t sfree0 = mapa_shared(ba(S.s_free), 0);
+            float m_ref = -INFINITY, l_part = 0.f;
+            bool ok = true;
+            for (int i = 0; i < ntiles; ++i) {
+                if (!warp_wait(S.s_full, i & 1, abort_p)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float sc[128];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t w[32];
+                    tmem_ld32(tbase + lb + kColS + half * 128 + c * 32, w);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) sc[c * 32 + u] = __uint_as_float(w[u]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(sfree0);
+                const int mi = i % kMetaRing;
+                if (!warp_wait(S.meta_full[mi], (i / kMetaRing) & 1, abort_p)) {
+                    ok = false;
+                    break;
+                }
+                uint32_t vw[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) vw[q] = row_ok ? S.valid[mi][4 * half + q] : 0u;
+                mbar_arrive(ba(S.meta_free[mi]));
+                const int k0 = kb + i * kNT + 128 * half;
+                if (k0 + 128 > Lb) {  // this half reaches the tree keys
+#pragma unroll
+                    for (int c = 0; c < 128; ++c) {
+                        const int u = k0 + c - Lb;
+                        if (u >= 0 && !(u < T && ((anc_t >> u) & 1ull))) vw[c >> 5] &= ~(1u << (c & 31));
+                    }
+                }
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    sc[c] = ((vw[c >> 5] >> (c & 31)) & 1u) ? sc[c] * a.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, sc[c]);
+                }
+                S.mx[i & 1][half][r] = mx;
+                // The staging tile is rewritten below: the previous tile's
+                // bulk copy must have read it (ordered through mx_bar).
+                if (stid == 0 && i >= 1) bulk_wait_read<0>();
+                mbar_arrive(ba(S.mx_bar[i & 1]));
+                if (!warp_wait(S.mx_bar[i & 1], (i >> 1) & 1, abort_p)) {
+                    ok = false;
+                    break;
+                }
+                const float mt = fmaxf(mx, S.mx[i & 1][half ^ 1][r]);
+                float alpha = 1.f;
+                if (mt > -INFINITY) {
+                    if (m_ref == -INFINITY) {
+                        m_ref = mt;
+                    } else if (mt > m_ref + kRescaleLog2) {
+                        alpha = ex2_approx(m_ref - mt);
+                        m_ref = mt;
+                        l_part *= alpha;
+                    }
+                }
+                // P (bf16) -> local staging tile (the O pair's A-operand layout).
+                float psum = 0.f;
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+                    const uint32_t pb = p_local + (2 * half + blk) * kPBlock;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int k = blk * 64 + c * 8 + 2 * u;
+                            const float p0 = sc[k] > -INFINITY ? ex2_approx(sc[k] - m_ref) : 0.f;
+                            const float p1 = sc[k + 1] > -INFINITY ? ex2_approx(sc[k + 1] - m_ref) : 0.f;
+                            psum += p0 + p1;
+                            w[u] = pack_bf16x2(p0, p1);
+                        }
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + sw128_offset(r, c)),
+                                     "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                                     : "memory");
+                    }
+                }
+                l_part += psum;
+                if (half == 0) alpha_local[r] = alpha;
+                fence_proxy_async_smem();
+                mbar_arrive(ba(S.pw_bar[i & 1]));
+                if (stid == 0) {
+                    const int slot = i & 1;
+                    bool ok1 = mbar_wait(ba(S.pw_bar[slot]), (i >> 1) & 1, abort_p);
+                    if (ok1 && i >= 2) ok1 = mbar_wait_cluster(ba(S.p_free[slot]), ((i - 2) >> 1) & 1, abort_p);
+                    if (ok1) {
+                        const uint32_t dst = mapa_shared(smem_u32(sm.u.o.pbuf[slot]), orank);
+                        const uint32_t bar = mapa_shared(ba(sm.u.o.p_full[slot]), orank);
+                        mbar_arrive_expect_tx_cluster(bar, kPXfer);
+#pragma unroll
+                        for (int blk = 0; blk < 4; ++blk)
+                            bulk_copy_to_peer(dst + blk * kPBlock, p_local + blk * kPBlock, kPBlock, bar);
+                        bulk_copy_to_peer(dst + kPBytes, p_local + kPBytes, kMh * 4, bar);
+                        bulk_commit();
+                    } else {
+                        ok = false;
+                    }
+                }
+                if (!ok) break;
+            }
+            if (stid == 0) bulk_wait_all();
+            if (ok) {
+                if (half == 0) {
+                    st_cluster_f32(mapa_shared(smem_u32(&sm.u.o.fin_m[r]), orank), m_ref);
+                    st_cluster_f32(mapa_shared(smem_u32(&sm.u.o.fin_l[0][r]), orank), l_part);
+                } else {
+                    st_cluster_f32(mapa_shared(smem_u32(&sm.u.o.fin_l[1][r]), orank), l_part);
+                }
+                mbar_arrive_cluster(mapa_shared(ba(sm.u.o.fin), orank));
+            }
+        }
+    } else if (wg != 2) {
+        regs_dec<kRegsLow>();
+        SmemO& O = sm.u.o;
+        if (warp != kWarpMMA) {
+            // ------------------------------------------------ O producers: V segments
+            // Warp 0 stages each tile's pool rows; warps 0-3, 5-7 and 12-15
+            // copy, for 32 keys per stage, this CTA's four 64-dim segments
+            // (eight lanes per 128-byte segment).
+            const int pw = warp < kWarpMMA ? warp : (warp < 8 ? warp - 1 : warp - 5);  // 0..10
+            bool ok = true;
+            for (int i = 0; ok && i < ntiles; ++i) {
+                const int rb2 = i & 1;
+                if (pw == 0) {
+                    if (i >= 2 && !warp_wait(O.rows_free[rb2], ((i >> 1) - 1) & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    (void)stage_rows(a, kbase, kb + i * kNT, ke, lane, O.rows[rb2], nullptr);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(ba(O.rows_full[rb2]));
+                }
+                if (!warp_wait(O.rows_full[rb2], (i >> 1) & 1, abort_p)) {
+                    ok = false;
+                    break;
+                }
+                for (int q = 0; q < kNT / kVKeys; ++q) {
+                    const int g = i * (kNT / kVKeys) + q;
+                    const int st = g % kVStages;
+                    if (g >= kVStages && !warp_wait(O.v_empty[st], ((g / kVStages) - 1) & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst0 = smem_u32(O.vring[st]);
+                    for (int it = pw; it < kVKeys * 4 * 8 / 32; it += kOProd) {
+                        const int idx = it * 32 + lane;
+                        const int chunk = idx & 7, pair = idx >> 3;
+                        const int kl = pair >> 2, sel = pair & 3;   // key in stage; (chain, segment)
+                        const int seg = 4 * (sel >> 1) + 2 * (int)hr + (sel & 1);
+                        const int32_t slot = O.rows[rb2][kVKeys * q + kl];
+                        const __nv_bfloat16* src =
+                            a.kv + (slot >= 0 ? (int64_t)slot * kDqk : 0) + seg * 64 + chunk * 8;
+                        cp_async_16_zfill_nc(dst0 + sel * kVSub + sw128_offset(kl, chunk), src, slot >= 0);
+                    }
+                    cp_async_mbar_arrive_noinc(ba(O.v_full[st]));
+                }
+                if (!ok) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ba(O.rows_free[rb2]));
+            }
+            cp_async_wait_all();
+        } else if (rank == 2) {
+            // ------------------------------------------------ O MMA issuer (pair)
+            if (lane == 0) {
+                const uint32_t idesc = make_idesc_bf16(kRowsBlk, 256, false, true);
+                bool ok = true;
+                for (int i = 0; ok && i < ntiles; ++i) {
+                    const int slot = i & 1;
+                    if (!mbar_wait_cluster(ba(O.o_gate[slot]), (i >> 1) & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_after();
+                    const uint32_t p0 = smem_u32(O.pbuf[slot]);
+                    for (int q = 0; q < kNT / kVKeys; ++q) {
+                        const int g = i * (kNT / kVKeys) + q;
+                        const int st = g % kVStages;
+                        if (!mbar_wait_cluster(ba(O.v_full[st]), (g / kVStages) & 1, abort_p)) {
+                            ok = false;
+                            break;
+                        }
+                        fence_proxy_async_smem();
+                        tc_fence_after();
+                        const uint32_t vs = smem_u32(O.vring[st]);
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const int kg = q * kVKeys + kk * 16;  // key within the tile
+                            const uint64_t ad = make_sdesc(p0 + (kg >> 6) * kPBlock + ((kg & 63) >> 4) * 32,
+                                                           16, 1024, kSwizzle128B);
+#pragma unroll
+                            for (int hv = 0; hv < 2; ++hv) {
+                                const uint64_t bd = make_sdesc(vs + hv * 2 * kVSub + kk * 2048, kVSub,
+                                                               1024, kSwizzle128B);
+                                mma_ss_pair(tbase + hv * 256, ad, bd, idesc,
+                                            (i > 0 || q > 0 || kk > 0) ? 1u : 0u);
+                            }
+                        }
+                        mma_commit_pair_mc(ba(O.v_empty[st]), 0xC);
+                    }
+                    if (!ok) break;
+                    mma_commit_pair_mc(ba(O.o_done[slot]), 0xC);
+                    // P of tile i - 1 is no longer read: its slot takes tile i + 1.
+                    if (i >= 1 && i + 1 < ntiles) {
+                        if (!mbar_wait(ba(O.o_done[slot ^ 1]), ((i - 1) >> 1) & 1, abort_p)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_cluster(mapa_shared(ba(sm.u.s.p_free[slot ^ 1]), 0));
+                        mbar_arrive_cluster(mapa_shared(ba(sm.u.s.p_free[slot ^ 1]), 1));
+                    }
+                }
+                mma_commit_pair_mc(ba(sm.h.drain), 0x4);
+                mbar_wait(ba(sm.h.drain), 0, &sm.h.no_abort);
+            }
+            __syncwarp();
+        } else {
+            // ------------------------------------------------ rank 3: forward V readiness to rank 2
+            if (lane == 0) {
+                const int nfill = ntiles * (kNT / kVKeys);
+                for (int g = 0; g < nfill; ++g) {
+                    const int st = g % kVStages;
+                    if (!mbar_wait(ba(O.v_full[st]), (g / kVStages) & 1, abort_p)) break;
+                    fence_proxy_async_smem();
+                    mbar_arrive_cluster(mapa_shared(ba(O.v_full[st]), 2));
+                }
+            }
+            __syncwarp();
+        }
+    } else {
+        SmemO& O = sm.u.o;
+        {
+            // ------------------------------------------------ correction + epilogue
+            const int quarter = warp & 3;
+            const int r = 32 * quarter + lane;
+            const int grow = row0 + r;
+            const bool row_ok = grow < rows_req;
+            const uint32_t lb = (uint32_t)(32 * quarter) << 16;
+            bool ok = true;
+            for (int i = 0; i < ntiles; ++i) {
+                const int slot = i & 1;
+                if (!warp_wait(O.p_full[slot], (i >> 1) & 1, abort_p)) {
+                    ok = false;
+                    break;
+                }
+                const float alpha = reinterpret_cast<const float*>(O.pbuf[slot] + kPBytes)[r];
+                if (__any_sync(0xffffffffu, alpha != 1.f) && i > 0) {
+                    if (!warp_wait(O.o_done[slot ^ 1], ((i - 1) >> 1) & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c0 = 0; c0 < 512; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(tbase + lb + c0, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
+                        tmem_st32(tbase + lb + c0, o);
+                    }
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(ba(O.o_gate[slot]), 2));
+            }
+            if (ok) ok = warp_wait_cluster(O.fin, 0, abort_p);
+            if (ok) ok = warp_wait(O.o_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort_p);
+            tc_fence_after();
+            if (ok) {
+                const float l = O.fin_l[0][r] + O.fin_l[1][r];
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const int64_t pid = ((int64_t)b * rows_req + (row_ok ? grow : 0)) * a.nsplit + s;
+                float4* dst = reinterpret_cast<float4*>(a.o_part + pid * kDv);
+#pragma unroll 1
+                for (int c0 = 0; c0 < 512; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(tbase + lb + c0, o);
+                    tmem_wait_ld();
+                    if (row_ok) {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            dst[c0 / 4 + u] = make_float4(
+                                __uint_as_float(o[4 * u]) * inv, __uint_as_float(o[4 * u + 1]) * inv,
+                                __uint_as_float(o[4 * u + 2]) * inv, __uint_as_float(o[4 * u + 3]) * inv);
+                    }
+                }
+                if (row_ok)
+                    a.lse_part[pid] = l > 0.f ? (O.fin_m[r] + log2f(l)) * kLn2 : -INFINITY;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // no CTA leaves while another may still touch its shared memory
+    if (warp == kWarpMMA) {
+        tc_fence_after();
+        tmem_dealloc_pair(tbase, 512);
+    }
+    if (sm.h.abort_flag) bad |= MLA_STATUS_TIMEOUT;
+    status_or(a.status, bad);
+}
+
+}  // namespace
+
+cudaError_t setup_partial_quad() {
+    return cudaFuncSetAttribute(partial_quad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kSmemBytes);
+}
+
+cudaError_t launch_partial_quad(const PartialArgs& a, cudaStream_t stream) {
+    const int rows_req = a.T * a.H;
+    const int nrb = (rows_req + kRowsBlk - 1) / kRowsBlk;
+    dim3 grid(4 * nrb, a.nsplit, a.batch);
+    partial_quad_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace mlav

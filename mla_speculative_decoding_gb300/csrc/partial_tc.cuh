@@ -14,4 +14,9 @@ cudaError_t setup_partial_tc();
 cudaError_t launch_partial_pair(const PartialArgs& a, cudaStream_t stream);
 cudaError_t setup_partial_pair();
 
+// Two-pair kernel (four SMs per 256-row block, 2-SM MMAs): the default for
+// requests with more than 128 rows.
+cudaError_t launch_partial_quad(const PartialArgs& a, cudaStream_t stream);
+cudaError_t setup_partial_quad();
+
 }  // namespace mlav

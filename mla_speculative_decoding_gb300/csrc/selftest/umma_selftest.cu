@@ -480,3 +480,145 @@ extern "C" __attribute__((visibility("default"))) int mlav_bulk_rate(int ncluste
     if (e != cudaSuccess) return (int)e;
     return (int)cudaDeviceSynchronize();
 }
+
+namespace {
+
+// CTA-pair (cta_group::2) layout self-test. A cluster of two CTAs computes
+// D = A * B with M = 256, K = 64: CTA r holds A rows [128r, 128r + 128) and
+// B rows (N) [r N/2, (r + 1) N/2), each in the same 128-byte-swizzled layouts
+// as the single-CTA probe; CTA 0 issues the MMAs and commits to the
+// mbarrier of both CTAs; each CTA reads its 128 rows of D from its own TMEM.
+//   mode 0: A smem K-major, B smem K-major      (N = 128 or 256)
+//   mode 1: A in TMEM,      B smem K-major      (N = 128)
+//   mode 2: A smem K-major, B smem MN-major     (N = 256)
+// Both CTAs allocate 256 columns. addr[r] receives CTA r's allocation result.
+// `reps` > 1 repeats the MMA sequence (rate measurement); cycles[0] is CTA 0's
+// issue-to-commit time.
+struct __align__(1024) PairSmem {
+    unsigned char a[128 * 128];  // [128 rows][64 bf16]
+    unsigned char b[128 * 128];  // K-major [N/2][64] or MN-major [N/2 / 64][64 k][64 n]
+    uint64_t bar;
+    uint32_t tmem;
+    int abort_flag;
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
+pair_probe_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __restrict__ B,
+                  float* __restrict__ D, int N, int mode, int reps, uint32_t* addr,
+                  long long* cycles, int* err) {
+    extern __shared__ __align__(1024) unsigned char raw[];
+    unsigned char* base = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+    PairSmem& sm = *reinterpret_cast<PairSmem*>(base);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const uint32_t rank = cluster_ctarank();
+    const bool a_tmem = mode == 1;
+    const bool b_mn = mode == 2;
+    const int nh = N / 2;
+    constexpr uint32_t kAcolP = 128;
+
+    const __nv_bfloat16* Ar = A + (size_t)rank * 128 * 64;
+    for (int i = tid; i < 128 * 8; i += 128) {
+        const int r = i >> 3, c = i & 7;
+        *reinterpret_cast<uint4*>(sm.a + sw128_offset(r, c)) =
+            *reinterpret_cast<const uint4*>(Ar + r * 64 + c * 8);
+    }
+    if (!b_mn) {
+        const __nv_bfloat16* Br = B + (size_t)rank * nh * 64;
+        for (int i = tid; i < nh * 8; i += 128) {
+            const int n = i >> 3, c = i & 7;
+            *reinterpret_cast<uint4*>(sm.b + sw128_offset(n, c)) =
+                *reinterpret_cast<const uint4*>(Br + n * 64 + c * 8);
+        }
+    } else {
+        // B is [64 k][N]; this CTA holds columns [rank * nh, rank * nh + nh).
+        const int nchunks = nh / 8;
+        for (int i = tid; i < 64 * nchunks; i += 128) {
+            const int k = i / nchunks, n0 = (i % nchunks) * 8;
+            *reinterpret_cast<uint4*>(sm.b + (n0 / 64) * (64 * 128) + sw128_offset(k, (n0 % 64) / 8)) =
+                *reinterpret_cast<const uint4*>(B + k * N + rank * nh + n0);
+        }
+    }
+    fence_proxy_async_smem();
+    if (warp == 0) {
+        tmem_alloc_pair(smem_u32(&sm.tmem), 256);
+        tmem_relinquish_pair();
+    }
+    if (tid == 0) {
+        mbar_init(smem_u32(&sm.bar), 1);
+        sm.abort_flag = 0;
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t my_addr = sm.tmem;
+    if (tid == 0) addr[rank] = my_addr;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    if (a_tmem) {
+        uint32_t w[32];
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(Ar + tid * 64);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i] = src[i];
+        tmem_st32(my_addr + lane_base + kAcolP, w);
+        tmem_wait_st();
+    }
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+
+    if (rank == 0 && tid == 0) {
+        const uint32_t idesc = make_idesc_bf16(256, N, false, b_mn);
+        const uint32_t a0 = smem_u32(sm.a), b0 = smem_u32(sm.b);
+        const long long t0 = clock64();
+        for (int rep = 0; rep < reps; ++rep) {
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t bd = b_mn ? make_sdesc(b0 + ks * 2048, 64 * 128, 1024, kSwizzle128B)
+                                         : make_sdesc(b0 + ks * 32, 16, 1024, kSwizzle128B);
+                if (a_tmem)
+                    mma_ts_pair(my_addr, my_addr + kAcolP + ks * 8, bd, idesc, ks > 0);
+                else
+                    mma_ss_pair(my_addr, make_sdesc(a0 + ks * 32, 16, 1024, kSwizzle128B), bd, idesc,
+                                ks > 0);
+            }
+        }
+        mma_commit_pair_mc(smem_u32(&sm.bar), (uint16_t)3);
+        if (mbar_wait(smem_u32(&sm.bar), 0, &sm.abort_flag)) cycles[0] = clock64() - t0;
+    }
+    const bool ok = mbar_wait(smem_u32(&sm.bar), 0, &sm.abort_flag);
+    tc_fence_after();
+    if (ok) {
+        for (int c0 = 0; c0 < N; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(my_addr + lane_base + c0, r);
+            tmem_wait_ld();
+            float* drow = D + (size_t)(rank * 128 + tid) * N + c0;
+            for (int j = 0; j < 32; ++j) drow[j] = __uint_as_float(r[j]);
+        }
+    } else if (tid == 0) {
+        atomicExch(err, 1 + (int)rank);
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    if (warp == 0) tmem_dealloc_pair(my_addr, 256);
+}
+
+}  // namespace
+
+extern "C" __attribute__((visibility("default"))) int mlav_pair_probe(
+    const void* A, const void* B, float* D, int N, int mode, int reps, uint32_t* addr,
+    long long* cycles, int* err) {
+    if (mode < 0 || mode > 2 || reps < 1 || reps > 4096) return -1;
+    if (mode == 0 && N != 128 && N != 256) return -1;
+    if (mode == 1 && N != 128) return -1;
+    if (mode == 2 && N != 256) return -1;
+    const int smem = (int)sizeof(PairSmem) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(pair_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return (int)e;
+    pair_probe_kernel<<<2, 128, smem>>>(static_cast<const __nv_bfloat16*>(A),
+                                        static_cast<const __nv_bfloat16*>(B), D, N, mode, reps, addr,
+                                        cycles, err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return (int)e;
+    return (int)cudaDeviceSynchronize();
+}

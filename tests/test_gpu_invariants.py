@@ -10,18 +10,19 @@ from tests.gpu_util import compare, host_out, oracle_ref, run_gpu, status
 from workloads import make_inputs
 
 pytestmark = pytest.mark.gpu
-PATHS = [0, mv.MLA_PARTIAL_SIMT, mv.MLA_PARTIAL_TC_QUARTER]
+PATHS = [0, mv.MLA_PARTIAL_PAIR, mv.MLA_PARTIAL_SIMT, mv.MLA_PARTIAL_TC_QUARTER]
 
 
 def _bits(d):
     return (d.out.cpu().view(torch.int16).numpy().copy(), d.lse.cpu().numpy().copy())
 
 
+@pytest.mark.parametrize("T", [16, 40])
 @pytest.mark.parametrize("flags", PATHS)
-def test_placement_invariance_bitwise(flags):
+def test_placement_invariance_bitwise(flags, T):
     """Scattered vs contiguous slots (same logical content): identical bits,
     because the reduction order depends only on logical key order."""
-    kw = dict(batch=2, num_heads=8, prefix=[9000, 3100], T=16, tree="random", pool_slots=60000,
+    kw = dict(batch=2, num_heads=8, prefix=[9000, 3100], T=T, tree="random", pool_slots=60000,
               nsplit=64, seed=11)
     a = run_gpu(make_inputs(placement="scattered", **kw), flags=flags)
     c = run_gpu(make_inputs(placement="contiguous", **kw), flags=flags)
@@ -30,9 +31,10 @@ def test_placement_invariance_bitwise(flags):
     assert np.array_equal(oa, oc) and np.array_equal(la, lc)
 
 
+@pytest.mark.parametrize("T", [8, 24])
 @pytest.mark.parametrize("flags", PATHS)
-def test_batch_equals_separate_calls_bitwise(flags):
-    kw = dict(num_heads=8, T=8, tree="random", pool_slots=20000, nsplit=16, seed=12)
+def test_batch_equals_separate_calls_bitwise(flags, T):
+    kw = dict(num_heads=8, T=T, tree="random", pool_slots=20000, nsplit=16, seed=12)
     inp = make_inputs(batch=3, prefix=[2000, 0, 777], **kw)
     d = run_gpu(inp, flags=flags)
     ob, lb = _bits(d)
@@ -50,9 +52,10 @@ def test_batch_equals_separate_calls_bitwise(flags):
         assert np.array_equal(l, lb[b * per:(b + 1) * per])
 
 
+@pytest.mark.parametrize("T", [8, 24])
 @pytest.mark.parametrize("flags", PATHS)
-def test_head_permutation_bitwise(flags):
-    inp = make_inputs(batch=1, num_heads=16, prefix=[1500], T=8, tree="random", pool_slots=8192,
+def test_head_permutation_bitwise(flags, T):
+    inp = make_inputs(batch=1, num_heads=16, prefix=[1500], T=T, tree="random", pool_slots=8192,
                       nsplit=8, seed=13)
     o, l = _bits(run_gpu(inp, flags=flags))
     perm = np.random.default_rng(0).permutation(16)
@@ -61,17 +64,19 @@ def test_head_permutation_bitwise(flags):
     assert np.array_equal(o2, o[:, perm]) and np.array_equal(l2, l[:, perm])
 
 
+@pytest.mark.parametrize("T", [16, 48])
 @pytest.mark.parametrize("flags", PATHS)
-def test_inline_vs_prebuilt_mask_bitwise(flags):
-    inp = make_inputs(batch=2, num_heads=8, prefix=[3000, 10], T=16, tree="random",
+def test_inline_vs_prebuilt_mask_bitwise(flags, T):
+    inp = make_inputs(batch=2, num_heads=8, prefix=[3000, 10], T=T, tree="random",
                       pool_slots=8192, nsplit=32, seed=14)
     a = _bits(run_gpu(inp, flags=flags, use_anc=True))
     b = _bits(run_gpu(inp, flags=flags, use_anc=False))
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
-def test_split_count_invariance():
-    inp = make_inputs(batch=1, num_heads=8, prefix=[6000], T=16, tree="random", pool_slots=8192,
+@pytest.mark.parametrize("T", [16, 32])
+def test_split_count_invariance(T):
+    inp = make_inputs(batch=1, num_heads=8, prefix=[6000], T=T, tree="random", pool_slots=8192,
                       nsplit=1, seed=15)
     res = {}
     for ns in (1, 4, 64):
@@ -82,17 +87,19 @@ def test_split_count_invariance():
         assert np.max(np.abs(res[ns][0] - res[1][0])) <= 2e-2 * np.abs(res[1][0]).max()
 
 
+@pytest.mark.parametrize("T", [16, 32])
 @pytest.mark.parametrize("flags", PATHS)
-def test_paths_agree(flags):
-    inp = make_inputs(batch=2, num_heads=8, prefix=[5000, 1234], T=16, tree="random",
+def test_paths_agree(flags, T):
+    inp = make_inputs(batch=2, num_heads=8, prefix=[5000, 1234], T=T, tree="random",
                       pool_slots=16384, nsplit=16, seed=16)
     out, lse = host_out(run_gpu(inp, flags=flags))
     ref_out, ref_lse = oracle_ref(inp)
     compare(out, lse, ref_out, ref_lse)
 
 
-def test_deterministic_repeat():
-    inp = make_inputs(batch=2, num_heads=8, prefix=[5000, 1234], T=16, tree="random",
+@pytest.mark.parametrize("T", [16, 32])
+def test_deterministic_repeat(T):
+    inp = make_inputs(batch=2, num_heads=8, prefix=[5000, 1234], T=T, tree="random",
                       pool_slots=16384, nsplit=64, seed=17)
     d = run_gpu(inp)
     a = _bits(d)
@@ -103,10 +110,11 @@ def test_deterministic_repeat():
         assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
-def test_cuda_graph_capture_and_replay():
+@pytest.mark.parametrize("T", [16, 32])
+def test_cuda_graph_capture_and_replay(T):
     """The whole verify step (build + partial + combine) is captured in one CUDA
     graph; replays match eager bit for bit and follow new input contents."""
-    inp = make_inputs(batch=2, num_heads=8, prefix=[4000, 900], T=16, tree="random",
+    inp = make_inputs(batch=2, num_heads=8, prefix=[4000, 900], T=T, tree="random",
                       pool_slots=16384, nsplit=64, seed=18)
     d = run_gpu(inp)  # eager (also runs the one-time set-up outside capture)
     eager = _bits(d)

@@ -2,7 +2,9 @@
 
 Every test calls the C ABI (through the thin binding) on seeded inputs and
 compares with the oracle run on the same inputs. Both kernel paths are
-covered: the default (tensor-core where supported) and the CUDA-core one.
+covered: the default (the four-SM 2-SM-MMA kernel for requests of more
+than 128 rows, the two-SM kernel otherwise), the two-SM kernel forced, the
+single-SM tensor-core kernel and the CUDA-core one.
 """
 
 import numpy as np
@@ -14,7 +16,7 @@ from tests.gpu_util import config_cached, compare, host_out, oracle_ref, run_gpu
 from workloads import make_config, make_inputs
 
 pytestmark = pytest.mark.gpu
-PATHS = [0, mv.MLA_PARTIAL_SIMT, mv.MLA_PARTIAL_TC_QUARTER]
+PATHS = [0, mv.MLA_PARTIAL_PAIR, mv.MLA_PARTIAL_SIMT, mv.MLA_PARTIAL_TC_QUARTER]
 
 
 @pytest.mark.parametrize("flags", PATHS)
@@ -60,6 +62,14 @@ CASES = [
     (3, 8, [0, 129, 5], 16, "star", 64),    # more splits than keys in some requests
     (1, 8, [300], 16, "random", 128),       # maximum split count
     (4, 32, [64, 0, 1, 4000], 4, "random", 16),
+    # more than 128 rows per request: 256-row blocks, full and ragged
+    (1, 16, [1000], 16, "random", 7),       # exactly one 256-row block
+    (2, 8, [333, 2049], 24, "random", 5),   # 192 rows: second half of the block partly empty
+    (1, 24, [700], 16, "random", 3),        # 384 rows: second block half empty
+    (1, 128, [5000], 2, "chain", 9),        # 256 rows from 128 heads
+    (3, 8, [0, 129, 5], 33, "star", 64),    # 264 rows: 8 rows in the last block; empty splits
+    (1, 3, [2500], 43, "random", 11),       # 129 rows: one row past the two-SM kernel's range
+    (1, 64, [0], 64, "chain", 4),           # 4096 rows, no prefix, maximum tree
 ]
 
 
@@ -101,14 +111,15 @@ def test_zero_query_closed_form_on_gpu():
     compare(out, lse, ref_out, ref_lse, "q = 0")
 
 
+@pytest.mark.parametrize("heads", [4, 32])
 @pytest.mark.parametrize("flags", PATHS)
-def test_growing_scores_force_rescaling(flags):
+def test_growing_scores_force_rescaling(flags, heads):
     """Scores that grow along the key order (about 48 nats over the prefix)
     make the running maximum overtake the lazy-rescale threshold (2^8, i.e.
     5.5 nats) many times. Magnitudes stay where fp32 scores can meet the 1e-3
     lse bound."""
     from workloads import bf16_bits_to_f32, f32_to_bf16_bits
-    inp = make_inputs(batch=1, num_heads=4, prefix=[3000], T=8, tree="random", pool_slots=4096,
+    inp = make_inputs(batch=1, num_heads=heads, prefix=[3000], T=8, tree="random", pool_slots=4096,
                       nsplit=3, seed=41, placement="contiguous")
     q = np.abs(bf16_bits_to_f32(inp.q))
     inp.q = f32_to_bf16_bits(q)
