@@ -51,8 +51,9 @@ constexpr int kNT = 256;          // keys per tile
 constexpr int kNh = 128;          // keys per S-CTA per tile
 constexpr int kThreads = 512;     // 16 warps = 4 warpgroups
 constexpr int kWarpMMA = 4;
-constexpr int kSProd = 7;         // S-side producer warps: 0-3, 5-7
-constexpr int kOProd = 11;        // O-side producer warps: 0-3, 5-7, 12-15
+constexpr int kWarpCtl = 7;       // P sender (S CTAs) / P slot release (O pair)
+constexpr int kSProd = 6;         // S-side producer warps: 0-3, 5, 6
+constexpr int kOProd = 10;        // O-side producer warps: 0-3, 5, 6, 12-15
 // Launched at 128 registers per thread (512 x 128 = 65,536). S CTAs:
 // warpgroups 0-1 drop to 72 and the softmax warpgroups rise to 184
 // (256 x 72 + 256 x 184 = 65,536). O CTAs: warpgroups 0, 1, 3 drop to 72.
@@ -60,6 +61,7 @@ constexpr int kRegsLow = 72, kRegsSoftmax = 184;
 constexpr int kKStages = 8;
 constexpr uint32_t kKBlock = kNh * 128;        // 128 keys x 64 dims (bf16) = 16 KB
 constexpr int kMetaRing = 4;
+constexpr int kRowsRing = 4;       // pool-row staging, two tiles ahead of the copies
 constexpr int kVKeys = 32;
 constexpr int kVStages = 4;
 constexpr uint32_t kVSub = kVKeys * 128;       // 32 keys x 64 dims = 4 KB
@@ -77,25 +79,25 @@ struct SmemS {
     unsigned char kring[kKStages][kKBlock];     // [128 keys x 64 dims] per stage
     unsigned char pstage[kPXfer];               // P [4 x (128 rows x 64 keys)] + alpha[128]
     uint32_t valid[kMetaRing][kNT / 32];
-    int32_t rows[2][kNT];                       // pool rows of the tiles being gathered
+    int32_t rows[kRowsRing][kNT];               // pool rows of the tiles being gathered
     float mx[2][2][kMh];
     uint64_t anc[MLA_MAX_TREE];
     int32_t par[MLA_MAX_TREE];
     uint64_t k_full[kKStages], k_empty[kKStages];
     uint64_t meta_full[kMetaRing], meta_free[kMetaRing];
-    uint64_t s_full, s_free, q_ready, q_peer, mx_bar[2], pw_bar[2];
-    uint64_t rows_full[2], rows_free[2];
+    uint64_t s_full, s_free, q_ready, q_peer, mx_bar[2], pw_bar[2], pstage_free;
+    uint64_t rows_full[kRowsRing], rows_free[kRowsRing];
     uint64_t p_free[2];
 };
 struct SmemO {
     unsigned char pbuf[2][kPSlot];              // P + alpha, one slot per tile parity
     unsigned char vring[kVStages][kVStage];
-    int32_t rows[2][kNT];
+    int32_t rows[kRowsRing][kNT];
     float fin_m[kMh];
     float fin_l[2][kMh];
     uint64_t v_full[kVStages], v_empty[kVStages];
     uint64_t p_full[2], o_gate[2], o_done[2], fin;
-    uint64_t rows_full[2], rows_free[2];
+    uint64_t rows_full[kRowsRing], rows_free[kRowsRing];
 };
 struct Header {
     uint64_t drain;
@@ -135,20 +137,22 @@ __device__ __forceinline__ bool warp_wait_cluster(const uint64_t& bar, uint32_t 
 __device__ __forceinline__ int stage_rows(const PartialArgs& a, int64_t kbase, int j0, int ke,
                                           int lane, int32_t* rows, uint32_t* valid) {
     int bad = 0;
+    int32_t v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {  // all eight loads in flight together
+        const int j = j0 + 32 * q + lane;
+        v[q] = j < ke ? __ldg(a.kv_indices + kbase + j) : -1;
+    }
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-        const int j = j0 + 32 * q + lane;
-        int32_t v = -1;
-        if (j < ke) {
-            v = a.kv_indices[kbase + j];
-            if (v < 0 || (int64_t)v >= a.pool_slots) {
-                bad |= MLA_STATUS_BAD_SLOT;
-                v = -1;
-            }
+        if (v[q] < -1 || (v[q] >= 0 && (int64_t)v[q] >= a.pool_slots) ||
+            (v[q] == -1 && j0 + 32 * q + lane < ke)) {
+            bad |= MLA_STATUS_BAD_SLOT;
+            v[q] = -1;
         }
-        rows[32 * q + lane] = v;
+        rows[32 * q + lane] = v[q];
         if (valid != nullptr) {
-            const uint32_t w = __ballot_sync(0xffffffffu, v >= 0);
+            const uint32_t w = __ballot_sync(0xffffffffu, v[q] >= 0);
             if (lane == q) valid[q] = w;
         }
     }
@@ -208,15 +212,18 @@ partial_quad_kernel(const PartialArgs a) {
                 mbar_init(ba(S.meta_free[i]), 256);
             }
             mbar_init(ba(S.s_full), 1);
-            mbar_init(ba(S.s_free), 16);
+            mbar_init(ba(S.s_free), 8 + (rank == 0 ? 1 : 0));
+            mbar_init(ba(S.pstage_free), 1);
             mbar_init(ba(S.q_ready), 256);
             mbar_init(ba(S.q_peer), 1);
             for (int i = 0; i < 2; ++i) {
                 mbar_init(ba(S.mx_bar[i]), 256);
                 mbar_init(ba(S.pw_bar[i]), 256);
+                mbar_init(ba(S.p_free[i]), 1);
+            }
+            for (int i = 0; i < kRowsRing; ++i) {
                 mbar_init(ba(S.rows_full[i]), 1);
                 mbar_init(ba(S.rows_free[i]), kSProd);
-                mbar_init(ba(S.p_free[i]), 1);
             }
         } else {
             SmemO& O = sm.u.o;
@@ -228,6 +235,8 @@ partial_quad_kernel(const PartialArgs a) {
                 mbar_init(ba(O.p_full[i]), 1);
                 mbar_init(ba(O.o_gate[i]), 8);
                 mbar_init(ba(O.o_done[i]), 1);
+            }
+            for (int i = 0; i < kRowsRing; ++i) {
                 mbar_init(ba(O.rows_full[i]), 1);
                 mbar_init(ba(O.rows_free[i]), kOProd);
             }
@@ -248,37 +257,19 @@ partial_quad_kernel(const PartialArgs a) {
     if (sside && wg < 2) {
         regs_dec<kRegsLow>();
         SmemS& S = sm.u.s;
-        if (warp != kWarpMMA) {
+        if (warp != kWarpMMA && warp != kWarpCtl) {
             // ------------------------------------------------ S producers: K blocks
-            // Warp 0 stages each tile's pool rows (all 256, with validity bits
-            // for the softmax); the seven producer warps copy this CTA's 128
-            // keys, eight lanes per 128-byte row segment.
-            const int pw = warp < kWarpMMA ? warp : warp - 1;  // 0..6
+            // The six producer warps copy this CTA's 128 keys of each tile,
+            // eight lanes per 128-byte row segment.
+            const int pw = warp < kWarpMMA ? warp : warp - 1;  // 0..5
             bool ok = warp_wait(S.q_ready, 0, abort_p);  // the ring doubles as Q staging
             for (int i = 0; ok && i < ntiles; ++i) {
-                const int rb2 = i & 1;
-                if (pw == 0) {
-                    if (i >= 2 && !warp_wait(S.rows_free[rb2], ((i >> 1) - 1) & 1, abort_p)) {
-                        ok = false;
-                        break;
-                    }
-                    const int mi = i % kMetaRing;
-                    if (i >= kMetaRing && !warp_wait(S.meta_free[mi], ((i / kMetaRing) - 1) & 1, abort_p)) {
-                        ok = false;
-                        break;
-                    }
-                    bad |= stage_rows(a, kbase, kb + i * kNT, ke, lane, S.rows[rb2], S.valid[mi]);
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(ba(S.meta_full[mi]));
-                        mbar_arrive(ba(S.rows_full[rb2]));
-                    }
-                }
-                if (!warp_wait(S.rows_full[rb2], (i >> 1) & 1, abort_p)) {
+                const int rs = i % kRowsRing;
+                if (!warp_wait(S.rows_full[rs], (i / kRowsRing) & 1, abort_p)) {
                     ok = false;
                     break;
                 }
-                const int32_t* my_rows = S.rows[rb2] + hr * kNh;
+                const int32_t* my_rows = S.rows[rs] + hr * kNh;
                 for (int kbk = 0; kbk < kDqk / 64; ++kbk) {
                     const int g = i * (kDqk / 64) + kbk;
                     const int st = g % kKStages;
@@ -298,9 +289,56 @@ partial_quad_kernel(const PartialArgs a) {
                 }
                 if (!ok) break;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(ba(S.rows_free[rb2]));
+                if (lane == 0) mbar_arrive(ba(S.rows_free[rs]));
             }
             cp_async_wait_all();
+        } else if (warp == kWarpCtl) {
+            // ------------------------------------------------ tile metadata + P sender
+            // The warp stages each tile's pool rows (all 256, with validity
+            // bits for the softmax) two tiles ahead of the copies; lane 0 sends
+            // each tile's P (and rescale factors) from the staging tile to the
+            // O partner's slot once that slot is free, then hands the staging
+            // tile back to the softmax.
+            auto stage = [&](int j) -> bool {
+                const int rs = j % kRowsRing, mi = j % kMetaRing;
+                if (j >= kRowsRing && !warp_wait(S.rows_free[rs], ((j / kRowsRing) - 1) & 1, abort_p))
+                    return false;
+                if (j >= kMetaRing && !warp_wait(S.meta_free[mi], ((j / kMetaRing) - 1) & 1, abort_p))
+                    return false;
+                bad |= stage_rows(a, kbase, kb + j * kNT, ke, lane, S.rows[rs], S.valid[mi]);
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(ba(S.meta_full[mi]));
+                    mbar_arrive(ba(S.rows_full[rs]));
+                }
+                return true;
+            };
+            const uint32_t p_local = smem_u32(S.pstage);
+            const uint32_t orank = 2u + hr;
+            bool ok = stage(0) && (ntiles < 2 || stage(1));
+            for (int i = 0; ok && i < ntiles; ++i) {
+                if (i + 2 < ntiles && !stage(i + 2)) break;
+                int sent = 1;
+                if (lane == 0) {
+                    const int slot = i & 1;
+                    sent = mbar_wait(ba(S.pw_bar[slot]), (i >> 1) & 1, abort_p);
+                    if (sent && i >= 2) sent = mbar_wait_cluster(ba(S.p_free[slot]), ((i - 2) >> 1) & 1, abort_p);
+                    if (sent) {
+                        const uint32_t dst = mapa_shared(smem_u32(sm.u.o.pbuf[slot]), orank);
+                        const uint32_t bar = mapa_shared(ba(sm.u.o.p_full[slot]), orank);
+                        mbar_arrive_expect_tx_remote(bar, kPXfer);
+#pragma unroll
+                        for (int blk = 0; blk < 4; ++blk)
+                            bulk_copy_to_peer(dst + blk * kPBlock, p_local + blk * kPBlock, kPBlock, bar);
+                        bulk_copy_to_peer(dst + kPBytes, p_local + kPBytes, kMh * 4, bar);
+                        bulk_commit();
+                        bulk_wait_read<0>();
+                        mbar_arrive(ba(S.pstage_free));
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, sent, 0) != 0;
+            }
+            if (lane == 0) bulk_wait_all();
         } else if (rank == 0) {
             // ------------------------------------------------ S MMA issuer (pair)
             if (lane == 0) {
@@ -344,27 +382,44 @@ partial_quad_kernel(const PartialArgs a) {
                 mma_commit_pair_mc(ba(sm.h.drain), 0x1);
                 mbar_wait(ba(sm.h.drain), 0, &sm.h.no_abort);
             }
-            __syncwarp();
         } else {
             // ------------------------------------------------ rank 1: forward readiness to rank 0
+            // One thread polls (without blocking) the two event streams rank 0
+            // needs from this CTA: filled K stages and released S tiles.
             if (lane == 0) {
                 bool ok = mbar_wait(ba(S.q_ready), 0, abort_p);
                 tc_fence_after();
                 tc_fence_before();
-                if (ok) mbar_arrive_cluster(mapa_shared(ba(S.q_peer), 0));
+                if (ok) mbar_arrive_remote(mapa_shared(ba(S.q_peer), 0));
                 const int nfill = ntiles * (kDqk / 64);
-                for (int g = 0; ok && g < nfill; ++g) {
-                    const int st = g % kKStages;
-                    if (!mbar_wait(ba(S.k_full[st]), (g / kKStages) & 1, abort_p)) {
-                        ok = false;
-                        break;
+                const uint32_t sfree_peer = mapa_shared(ba(S.s_free), 0);
+                int g = 0, i = 0;
+                uint64_t t_last = globaltimer_ns();
+                while (ok && (g < nfill || i < ntiles)) {
+                    bool prog = false;
+                    if (g < nfill && mbar_test_wait(ba(S.k_full[g % kKStages]), (g / kKStages) & 1)) {
+                        fence_proxy_async_smem();
+                        mbar_arrive_remote(mapa_shared(ba(S.k_full[g % kKStages]), 0));
+                        ++g;
+                        prog = true;
                     }
-                    fence_proxy_async_smem();
-                    mbar_arrive_cluster(mapa_shared(ba(S.k_full[st]), 0));
+                    if (i < ntiles && mbar_test_wait(ba(S.s_free), i & 1)) {
+                        tc_fence_after();
+                        tc_fence_before();
+                        mbar_arrive_remote(sfree_peer);
+                        ++i;
+                        prog = true;
+                    }
+                    if (prog) {
+                        t_last = globaltimer_ns();
+                    } else if (*abort_p || globaltimer_ns() - t_last > 2000000000ull) {
+                        *abort_p = 1;
+                        ok = false;
+                    }
                 }
             }
-            __syncwarp();
         }
+        __syncwarp();
     } else if (sside) {
         regs_inc<kRegsSoftmax>();
         SmemS& S = sm.u.s;
@@ -427,7 +482,6 @@ partial_quad_kernel(const PartialArgs a) {
             const uint64_t anc_t = S.anc[t];
             const uint32_t p_local = smem_u32(S.pstage);
             float* alpha_local = reinterpret_cast<float*>(S.pstage + kPBytes);
-            const uint32_t sfree0 = mapa_shared(ba(S.s_free), 0);
             float m_ref = -INFINITY, l_part = 0.f;
             bool ok = true;
             for (int i = 0; i < ntiles; ++i) {
@@ -437,17 +491,19 @@ partial_quad_kernel(const PartialArgs a) {
                 }
                 tc_fence_after();
                 float sc[128];
+                {
+                    uint32_t w[4][32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t w[32];
-                    tmem_ld32(tbase + lb + kColS + half * 128 + c * 32, w);
+                    for (int c = 0; c < 4; ++c) tmem_ld32(tbase + lb + kColS + half * 128 + c * 32, w[c]);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) sc[c * 32 + u] = __uint_as_float(w[u]);
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int u = 0; u < 32; ++u) sc[c * 32 + u] = __uint_as_float(w[c][u]);
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(sfree0);
+                if (lane == 0) mbar_arrive(ba(S.s_free));
                 const int mi = i % kMetaRing;
                 if (!warp_wait(S.meta_full[mi], (i / kMetaRing) & 1, abort_p)) {
                     ok = false;
@@ -472,9 +528,6 @@ partial_quad_kernel(const PartialArgs a) {
                     mx = fmaxf(mx, sc[c]);
                 }
                 S.mx[i & 1][half][r] = mx;
-                // The staging tile is rewritten below: the previous tile's
-                // bulk copy must have read it (ordered through mx_bar).
-                if (stid == 0 && i >= 1) bulk_wait_read<0>();
                 mbar_arrive(ba(S.mx_bar[i & 1]));
                 if (!warp_wait(S.mx_bar[i & 1], (i >> 1) & 1, abort_p)) {
                     ok = false;
@@ -491,7 +544,12 @@ partial_quad_kernel(const PartialArgs a) {
                         l_part *= alpha;
                     }
                 }
-                // P (bf16) -> local staging tile (the O pair's A-operand layout).
+                // P (bf16) -> local staging tile (the O pair's A-operand layout),
+                // once the previous tile's P has been read out of it.
+                if (i >= 1 && !warp_wait(S.pstage_free, (i - 1) & 1, abort_p)) {
+                    ok = false;
+                    break;
+                }
                 float psum = 0.f;
 #pragma unroll
                 for (int blk = 0; blk < 2; ++blk) {
@@ -516,26 +574,7 @@ partial_quad_kernel(const PartialArgs a) {
                 if (half == 0) alpha_local[r] = alpha;
                 fence_proxy_async_smem();
                 mbar_arrive(ba(S.pw_bar[i & 1]));
-                if (stid == 0) {
-                    const int slot = i & 1;
-                    bool ok1 = mbar_wait(ba(S.pw_bar[slot]), (i >> 1) & 1, abort_p);
-                    if (ok1 && i >= 2) ok1 = mbar_wait_cluster(ba(S.p_free[slot]), ((i - 2) >> 1) & 1, abort_p);
-                    if (ok1) {
-                        const uint32_t dst = mapa_shared(smem_u32(sm.u.o.pbuf[slot]), orank);
-                        const uint32_t bar = mapa_shared(ba(sm.u.o.p_full[slot]), orank);
-                        mbar_arrive_expect_tx_cluster(bar, kPXfer);
-#pragma unroll
-                        for (int blk = 0; blk < 4; ++blk)
-                            bulk_copy_to_peer(dst + blk * kPBlock, p_local + blk * kPBlock, kPBlock, bar);
-                        bulk_copy_to_peer(dst + kPBytes, p_local + kPBytes, kMh * 4, bar);
-                        bulk_commit();
-                    } else {
-                        ok = false;
-                    }
-                }
-                if (!ok) break;
             }
-            if (stid == 0) bulk_wait_all();
             if (ok) {
                 if (half == 0) {
                     st_cluster_f32(mapa_shared(smem_u32(&sm.u.o.fin_m[r]), orank), m_ref);
@@ -549,25 +588,15 @@ partial_quad_kernel(const PartialArgs a) {
     } else if (wg != 2) {
         regs_dec<kRegsLow>();
         SmemO& O = sm.u.o;
-        if (warp != kWarpMMA) {
+        if (warp != kWarpMMA && warp != kWarpCtl) {
             // ------------------------------------------------ O producers: V segments
-            // Warp 0 stages each tile's pool rows; warps 0-3, 5-7 and 12-15
-            // copy, for 32 keys per stage, this CTA's four 64-dim segments
-            // (eight lanes per 128-byte segment).
-            const int pw = warp < kWarpMMA ? warp : (warp < 8 ? warp - 1 : warp - 5);  // 0..10
+            // Warps 0-3, 5, 6 and 12-15 copy, for 32 keys per stage, this
+            // CTA's four 64-dim segments (eight lanes per 128-byte segment).
+            const int pw = warp < kWarpMMA ? warp : (warp < 8 ? warp - 1 : warp - 6);  // 0..9
             bool ok = true;
             for (int i = 0; ok && i < ntiles; ++i) {
-                const int rb2 = i & 1;
-                if (pw == 0) {
-                    if (i >= 2 && !warp_wait(O.rows_free[rb2], ((i >> 1) - 1) & 1, abort_p)) {
-                        ok = false;
-                        break;
-                    }
-                    (void)stage_rows(a, kbase, kb + i * kNT, ke, lane, O.rows[rb2], nullptr);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(ba(O.rows_full[rb2]));
-                }
-                if (!warp_wait(O.rows_full[rb2], (i >> 1) & 1, abort_p)) {
+                const int rs = i % kRowsRing;
+                if (!warp_wait(O.rows_full[rs], (i / kRowsRing) & 1, abort_p)) {
                     ok = false;
                     break;
                 }
@@ -584,7 +613,7 @@ partial_quad_kernel(const PartialArgs a) {
                         const int chunk = idx & 7, pair = idx >> 3;
                         const int kl = pair >> 2, sel = pair & 3;   // key in stage; (chain, segment)
                         const int seg = 4 * (sel >> 1) + 2 * (int)hr + (sel & 1);
-                        const int32_t slot = O.rows[rb2][kVKeys * q + kl];
+                        const int32_t slot = O.rows[rs][kVKeys * q + kl];
                         const __nv_bfloat16* src =
                             a.kv + (slot >= 0 ? (int64_t)slot * kDqk : 0) + seg * 64 + chunk * 8;
                         cp_async_16_zfill_nc(dst0 + sel * kVSub + sw128_offset(kl, chunk), src, slot >= 0);
@@ -593,9 +622,36 @@ partial_quad_kernel(const PartialArgs a) {
                 }
                 if (!ok) break;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(ba(O.rows_free[rb2]));
+                if (lane == 0) mbar_arrive(ba(O.rows_free[rs]));
             }
             cp_async_wait_all();
+        } else if (warp == kWarpCtl) {
+            // ------------------------------------------------ tile rows + P slot release
+            // The warp stages each tile's pool rows two tiles ahead of the
+            // copies; on rank 2, lane 0 frees P slots: once P V of tile i is
+            // complete, its slot may take tile i + 2.
+            auto stage = [&](int j) -> bool {
+                const int rs = j % kRowsRing;
+                if (j >= kRowsRing && !warp_wait(O.rows_free[rs], ((j / kRowsRing) - 1) & 1, abort_p))
+                    return false;
+                (void)stage_rows(a, kbase, kb + j * kNT, ke, lane, O.rows[rs], nullptr);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ba(O.rows_full[rs]));
+                return true;
+            };
+            bool ok = stage(0) && (ntiles < 2 || stage(1));
+            for (int i = 0; ok && i < ntiles; ++i) {
+                if (i + 2 < ntiles && !stage(i + 2)) break;
+                int rel = 1;
+                if (rank == 2 && lane == 0 && i + 2 < ntiles) {
+                    rel = mbar_wait(ba(O.o_done[i & 1]), (i >> 1) & 1, abort_p);
+                    if (rel) {
+                        mbar_arrive_remote(mapa_shared(ba(sm.u.s.p_free[i & 1]), 0));
+                        mbar_arrive_remote(mapa_shared(ba(sm.u.s.p_free[i & 1]), 1));
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, rel, 0) != 0;
+            }
         } else if (rank == 2) {
             // ------------------------------------------------ O MMA issuer (pair)
             if (lane == 0) {
@@ -637,20 +693,10 @@ partial_quad_kernel(const PartialArgs a) {
                     }
                     if (!ok) break;
                     mma_commit_pair_mc(ba(O.o_done[slot]), 0xC);
-                    // P of tile i - 1 is no longer read: its slot takes tile i + 1.
-                    if (i >= 1 && i + 1 < ntiles) {
-                        if (!mbar_wait(ba(O.o_done[slot ^ 1]), ((i - 1) >> 1) & 1, abort_p)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_cluster(mapa_shared(ba(sm.u.s.p_free[slot ^ 1]), 0));
-                        mbar_arrive_cluster(mapa_shared(ba(sm.u.s.p_free[slot ^ 1]), 1));
-                    }
                 }
                 mma_commit_pair_mc(ba(sm.h.drain), 0x4);
                 mbar_wait(ba(sm.h.drain), 0, &sm.h.no_abort);
             }
-            __syncwarp();
         } else {
             // ------------------------------------------------ rank 3: forward V readiness to rank 2
             if (lane == 0) {
@@ -659,11 +705,11 @@ partial_quad_kernel(const PartialArgs a) {
                     const int st = g % kVStages;
                     if (!mbar_wait(ba(O.v_full[st]), (g / kVStages) & 1, abort_p)) break;
                     fence_proxy_async_smem();
-                    mbar_arrive_cluster(mapa_shared(ba(O.v_full[st]), 2));
+                    mbar_arrive_remote(mapa_shared(ba(O.v_full[st]), 2));
                 }
             }
-            __syncwarp();
         }
+        __syncwarp();
     } else {
         SmemO& O = sm.u.o;
         {
@@ -700,7 +746,7 @@ partial_quad_kernel(const PartialArgs a) {
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(mapa_shared(ba(O.o_gate[slot]), 2));
+                if (lane == 0) mbar_arrive_remote(mapa_shared(ba(O.o_gate[slot]), 2));
             }
             if (ok) ok = warp_wait_cluster(O.fin, 0, abort_p);
             if (ok) ok = warp_wait(O.o_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort_p);

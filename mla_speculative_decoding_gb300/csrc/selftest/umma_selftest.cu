@@ -287,15 +287,19 @@ struct __align__(1024) GatherSmem {
 
 __global__ void __launch_bounds__(192, 1)
 gather_rate_kernel(const __grid_constant__ CUtensorMap map, const __nv_bfloat16* kv,
-                   const int32_t* slots, int ntile, int method, int nw, long long* cycles, int* err) {
+                   const int32_t* slots, int ntile, int method, int nw, int tma_rows, long long* cycles,
+                   int* err) {
     extern __shared__ __align__(1024) unsigned char raw[];
     unsigned char* base = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
     GatherSmem& g = *reinterpret_cast<GatherSmem*>(base);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nprod = method <= 1 ? nw : 1;
+    // method 4: warps 0..nw-1 copy keys [0, 256 - tma_rows) with cp.async (as
+    // method 0) while warp 4 issues gather4 for the last tma_rows keys.
+    const int nprod = (method <= 1 || method == 4) ? nw : 1;
+    const int cp_keys = method == 4 ? 256 - tma_rows : 256;
     if (tid == 0) {
         for (int i = 0; i < kGStages; ++i) {
-            mbar_init(smem_u32(&g.full[i]), method <= 1 ? 32 * nprod : 1);
+            mbar_init(smem_u32(&g.full[i]), method <= 1 ? 32 * nprod : method == 4 ? 32 * nprod + 1 : 1);
             mbar_init(smem_u32(&g.empty[i]), 1);
         }
         g.abort_flag = 0;
@@ -305,7 +309,27 @@ gather_rate_kernel(const __grid_constant__ CUtensorMap map, const __nv_bfloat16*
     __syncthreads();
     const int32_t* my = slots + (size_t)blockIdx.x * ntile * 256;
     const long long t0 = clock64();
-    if (warp < nprod) {
+    if (method == 4 && warp == 4) {
+        if (lane == 0) {
+            for (int t = 0; t < ntile; ++t) {
+                // the rows of tile t are read straight from global memory here
+                for (int blk = 0; blk < 9; ++blk) {
+                    const int u = t * 9 + blk, st = u % kGStages;
+                    if (u >= kGStages && !mbar_wait(smem_u32(&g.empty[st]), ((u / kGStages) - 1) & 1, &g.abort_flag)) {
+                        atomicExch(err, 1);
+                        break;
+                    }
+                    const uint32_t dst0 = smem_u32(g.ring[st]);
+                    mbar_arrive_expect_tx(smem_u32(&g.full[st]), (uint32_t)tma_rows * 128u);
+                    for (int k0 = cp_keys; k0 < 256; k0 += 4) {
+                        const int32_t* r = my + t * 256 + k0;
+                        tma_gather4(dst0 + k0 * 128, &map, blk * 64, r[0], r[1], r[2], r[3], smem_u32(&g.full[st]));
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp < nprod) {
         for (int t = 0; t < ntile; ++t) {
             // stage this tile's slots (each producer warp keeps its own copy in registers
             // where needed; the shared copy serves methods 0, 2, 3)
@@ -324,8 +348,8 @@ gather_rate_kernel(const __grid_constant__ CUtensorMap map, const __nv_bfloat16*
                     goto done;
                 }
                 const uint32_t dst0 = smem_u32(g.ring[st]);
-                if (method == 0) {
-                    for (int it = warp; it < 64; it += nprod) {
+                if (method == 0 || method == 4) {
+                    for (int it = warp; it < cp_keys / 4; it += nprod) {
                         const int key = it * 4 + (lane >> 3), c = lane & 7;
                         const int32_t sl = g.rows[t & 1][key];
                         cp_async_16_zfill_nc(dst0 + sw128_offset(key, c),
@@ -383,15 +407,16 @@ done:
 
 extern "C" __attribute__((visibility("default"))) int mlav_gather_rate(
     const void* kv, long long pool, const int32_t* slots, int nblocks, int ntile, int method,
-    int nw, long long* cycles, int* err) {
+    int nw, int tma_rows, long long* cycles, int* err) {
     CUtensorMap map;
     if (!mlav::make_kv_gather_map(&map, kv, pool)) return -2;
-    if (nw < 1 || nw > 4 || method < 0 || method > 3) return -1;
+    if (nw < 1 || nw > 4 || method < 0 || method > 4) return -1;
+    if (method == 4 && (tma_rows < 4 || tma_rows > 252 || tma_rows % 4 != 0)) return -1;
     const int smem = (int)sizeof(GatherSmem) + 1024;
     cudaError_t e = cudaFuncSetAttribute(gather_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return (int)e;
     gather_rate_kernel<<<nblocks, 192, smem>>>(map, static_cast<const __nv_bfloat16*>(kv), slots, ntile,
-                                               method, nw, cycles, err);
+                                               method, nw, tma_rows, cycles, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;
     return (int)cudaDeviceSynchronize();
@@ -489,9 +514,10 @@ namespace {
 // as the single-CTA probe; CTA 0 issues the MMAs and commits to the
 // mbarrier of both CTAs; each CTA reads its 128 rows of D from its own TMEM.
 //   mode 0: A smem K-major, B smem K-major      (N = 128 or 256)
-//   mode 1: A in TMEM,      B smem K-major      (N = 128)
+//   mode 1: A in TMEM,      B smem K-major      (N = 128 or 256)
 //   mode 2: A smem K-major, B smem MN-major     (N = 256)
-// Both CTAs allocate 256 columns. addr[r] receives CTA r's allocation result.
+// The pair allocates 512 columns together (D at column 0, A at column 256).
+// addr[r] receives CTA r's copy of the allocation result.
 // `reps` > 1 repeats the MMA sequence (rate measurement); cycles[0] is CTA 0's
 // issue-to-commit time.
 struct __align__(1024) PairSmem {
@@ -514,7 +540,7 @@ pair_probe_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __re
     const bool a_tmem = mode == 1;
     const bool b_mn = mode == 2;
     const int nh = N / 2;
-    constexpr uint32_t kAcolP = 128;
+    constexpr uint32_t kAcolP = 256;
 
     const __nv_bfloat16* Ar = A + (size_t)rank * 128 * 64;
     for (int i = tid; i < 128 * 8; i += 128) {
@@ -540,7 +566,7 @@ pair_probe_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __re
     }
     fence_proxy_async_smem();
     if (warp == 0) {
-        tmem_alloc_pair(smem_u32(&sm.tmem), 256);
+        tmem_alloc_pair(smem_u32(&sm.tmem), 512);
         tmem_relinquish_pair();
     }
     if (tid == 0) {
@@ -600,7 +626,7 @@ pair_probe_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __re
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();
-    if (warp == 0) tmem_dealloc_pair(my_addr, 256);
+    if (warp == 0) tmem_dealloc_pair(my_addr, 512);
 }
 
 }  // namespace
@@ -610,7 +636,7 @@ extern "C" __attribute__((visibility("default"))) int mlav_pair_probe(
     long long* cycles, int* err) {
     if (mode < 0 || mode > 2 || reps < 1 || reps > 4096) return -1;
     if (mode == 0 && N != 128 && N != 256) return -1;
-    if (mode == 1 && N != 128) return -1;
+    if (mode == 1 && N != 128 && N != 256) return -1;
     if (mode == 2 && N != 256) return -1;
     const int smem = (int)sizeof(PairSmem) + 1024;
     cudaError_t e = cudaFuncSetAttribute(pair_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

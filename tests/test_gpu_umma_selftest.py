@@ -84,3 +84,38 @@ def test_tma_gather4_rows_and_zero_fill():
                     else torch.zeros(8, 8, dtype=torch.int16))
             for c in range(8):
                 assert torch.equal(raw[i, c ^ (i % 8)], want[c]), (x, i, c)
+
+
+@pytest.fixture(scope="module")
+def pair_probe():
+    lib = ctypes.CDLL(B.build_selftest())
+    f = lib.mlav_pair_probe
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p] * 3
+    return f
+
+
+@pytest.mark.parametrize("mode,N", [(0, 128), (0, 256), (1, 128), (1, 256), (2, 256)])
+def test_cta_pair_mma(pair_probe, mode, N):
+    """2-SM MMA (cta_group::2, M = 256) as the four-SM kernel uses it: A rows
+    split across the pair (shared memory or TMEM), B's N columns split across
+    the pair (K-major or MN-major), commit multicast to both CTAs, each CTA
+    reading its 128 rows of D; the pair's allocation result is the same in
+    both CTAs."""
+    g = torch.Generator().manual_seed(7 * mode + N)
+    A = torch.randn(256, 64, generator=g).to(torch.bfloat16)
+    Bm = torch.randn(N, 64, generator=g).to(torch.bfloat16) if mode in (0, 1) else \
+        torch.randn(64, N, generator=g).to(torch.bfloat16)
+    dA, dB = A.cuda(), Bm.cuda()
+    D = torch.full((256, N), float("nan"), dtype=torch.float32, device="cuda")
+    addr = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+    cyc = torch.zeros(1, dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = pair_probe(dA.data_ptr(), dB.data_ptr(), D.data_ptr(), N, mode, 1, addr.data_ptr(),
+                    cyc.data_ptr(), err.data_ptr())
+    assert rc == 0, f"pair probe launch failed: {rc}"
+    assert int(err.item()) == 0, "pair probe wait timed out"
+    a = addr.cpu().tolist()
+    assert a[0] == a[1], f"allocation differs between the CTAs of the pair: {a}"
+    ref = A.double() @ (Bm.double().T if mode in (0, 1) else Bm.double())
+    torch.testing.assert_close(D.cpu().double(), ref, rtol=1e-4, atol=1e-3)
