@@ -53,6 +53,7 @@ constexpr int kThreads = 512;     // 16 warps = 4 warpgroups
 constexpr int kWarpMMA = 4;
 constexpr int kWarpCtl = 7;       // P sender (S CTAs) / P slot release (O pair)
 constexpr int kSProd = 6;         // S-side producer warps: 0-3, 5, 6
+constexpr int kSGroup = 2;        // producer warps per K stage (stages go round-robin to groups)
 constexpr int kOProd = 10;        // O-side producer warps: 0-3, 5, 6, 12-15
 // Launched at 128 registers per thread (512 x 128 = 65,536). S CTAs:
 // warpgroups 0-1 drop to 72 and the softmax warpgroups rise to 184
@@ -204,7 +205,7 @@ partial_quad_kernel(const PartialArgs a) {
         if (sside) {
             SmemS& S = sm.u.s;
             for (int i = 0; i < kKStages; ++i) {
-                mbar_init(ba(S.k_full[i]), 32 * kSProd + (rank == 0 ? 1 : 0));
+                mbar_init(ba(S.k_full[i]), 32 * kSGroup + (rank == 0 ? 1 : 0));
                 mbar_init(ba(S.k_empty[i]), 1);
             }
             for (int i = 0; i < kMetaRing; ++i) {
@@ -212,7 +213,7 @@ partial_quad_kernel(const PartialArgs a) {
                 mbar_init(ba(S.meta_free[i]), 256);
             }
             mbar_init(ba(S.s_full), 1);
-            mbar_init(ba(S.s_free), 8 + (rank == 0 ? 1 : 0));
+            mbar_init(ba(S.s_free), 16);  // rank 0's: the softmax warps of both S CTAs
             mbar_init(ba(S.pstage_free), 1);
             mbar_init(ba(S.q_ready), 256);
             mbar_init(ba(S.q_peer), 1);
@@ -223,7 +224,7 @@ partial_quad_kernel(const PartialArgs a) {
             }
             for (int i = 0; i < kRowsRing; ++i) {
                 mbar_init(ba(S.rows_full[i]), 1);
-                mbar_init(ba(S.rows_free[i]), kSProd);
+                mbar_init(ba(S.rows_free[i]), (kDqk / 64) * kSGroup);
             }
         } else {
             SmemO& O = sm.u.o;
@@ -259,35 +260,31 @@ partial_quad_kernel(const PartialArgs a) {
         SmemS& S = sm.u.s;
         if (warp != kWarpMMA && warp != kWarpCtl) {
             // ------------------------------------------------ S producers: K blocks
-            // The six producer warps copy this CTA's 128 keys of each tile,
-            // eight lanes per 128-byte row segment.
+            // The six producer warps form three groups of two; stage g (this
+            // CTA's 128 keys x 64 dims of one tile) is copied by group g mod 3,
+            // eight lanes per 128-byte row segment, so that stages complete
+            // independently of one another.
             const int pw = warp < kWarpMMA ? warp : warp - 1;  // 0..5
+            const int grp = pw / kSGroup, gw = pw % kSGroup;
+            constexpr int kNGroups = kSProd / kSGroup;
             bool ok = warp_wait(S.q_ready, 0, abort_p);  // the ring doubles as Q staging
-            for (int i = 0; ok && i < ntiles; ++i) {
+            const int nfill = ntiles * (kDqk / 64);
+            for (int g = grp; ok && g < nfill; g += kNGroups) {
+                const int i = g / (kDqk / 64), kbk = g % (kDqk / 64);
                 const int rs = i % kRowsRing;
-                if (!warp_wait(S.rows_full[rs], (i / kRowsRing) & 1, abort_p)) {
-                    ok = false;
-                    break;
-                }
+                const int st = g % kKStages;
+                if (!warp_wait(S.rows_full[rs], (i / kRowsRing) & 1, abort_p)) break;
+                if (g >= kKStages && !warp_wait(S.k_empty[st], ((g / kKStages) - 1) & 1, abort_p)) break;
                 const int32_t* my_rows = S.rows[rs] + hr * kNh;
-                for (int kbk = 0; kbk < kDqk / 64; ++kbk) {
-                    const int g = i * (kDqk / 64) + kbk;
-                    const int st = g % kKStages;
-                    if (g >= kKStages && !warp_wait(S.k_empty[st], ((g / kKStages) - 1) & 1, abort_p)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t dst0 = smem_u32(S.kring[st]);
-                    for (int it = pw; it < kNh / 4; it += kSProd) {
-                        const int key = it * 4 + (lane >> 3), c = lane & 7;
-                        const int32_t slot = my_rows[key];
-                        const __nv_bfloat16* src =
-                            a.kv + (slot >= 0 ? (int64_t)slot * kDqk : 0) + kbk * 64 + c * 8;
-                        cp_async_16_zfill_nc(dst0 + sw128_offset(key, c), src, slot >= 0);
-                    }
-                    cp_async_mbar_arrive_noinc(ba(S.k_full[st]));
+                const uint32_t dst0 = smem_u32(S.kring[st]);
+                for (int it = gw; it < kNh / 4; it += kSGroup) {
+                    const int key = it * 4 + (lane >> 3), c = lane & 7;
+                    const int32_t slot = my_rows[key];
+                    const __nv_bfloat16* src =
+                        a.kv + (slot >= 0 ? (int64_t)slot * kDqk : 0) + kbk * 64 + c * 8;
+                    cp_async_16_zfill_nc(dst0 + sw128_offset(key, c), src, slot >= 0);
                 }
-                if (!ok) break;
+                cp_async_mbar_arrive_noinc(ba(S.k_full[st]));
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ba(S.rows_free[rs]));
             }
@@ -341,6 +338,9 @@ partial_quad_kernel(const PartialArgs a) {
             if (lane == 0) bulk_wait_all();
         } else if (rank == 0) {
             // ------------------------------------------------ S MMA issuer (pair)
+            // The issue loop is kept free of per-MMA descriptor construction
+            // and branches: a pair MMA takes about 128 cycles, and any work the
+            // issuing thread does between MMAs is lost tensor time.
             if (lane == 0) {
                 const uint32_t idesc = make_idesc_bf16(kRowsBlk, kNT, false, false);
                 bool ok = mbar_wait(ba(S.q_ready), 0, abort_p) &&
@@ -348,34 +348,43 @@ partial_quad_kernel(const PartialArgs a) {
                 fence_proxy_async_smem();
                 tc_fence_after();
                 const uint32_t dS = tbase + kColS;
-                const uint32_t qr = smem_u32(S.q_rope);
+                const uint64_t kdesc0 = make_sdesc(smem_u32(S.kring[0]), 16, 1024, kSwizzle128B);
+                const uint64_t qrdesc = make_sdesc(smem_u32(S.q_rope), 16, 1024, kSwizzle128B);
+                const uint32_t kfull0 = ba(S.k_full[0]), kempty0 = ba(S.k_empty[0]);
+                int st = 0;
+                uint32_t ph = 0;
                 for (int i = 0; ok && i < ntiles; ++i) {
                     if (i >= 1 && !mbar_wait_cluster(ba(S.s_free), (i - 1) & 1, abort_p)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+#pragma unroll 1
                     for (int kbk = 0; kbk < kDqk / 64; ++kbk) {
-                        const int g = i * (kDqk / 64) + kbk;
-                        const int st = g % kKStages;
-                        if (!mbar_wait_cluster(ba(S.k_full[st]), (g / kKStages) & 1, abort_p)) {
+                        if (!mbar_wait_cluster(kfull0 + 8 * st, ph, abort_p)) {
                             ok = false;
                             break;
                         }
                         fence_proxy_async_smem();
                         tc_fence_after();
-                        const uint32_t kt = smem_u32(S.kring[st]);
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            const uint64_t bd = make_sdesc(kt + ks * 32, 16, 1024, kSwizzle128B);
-                            const uint32_t acc = (kbk | ks) ? 1u : 0u;
-                            if (kbk < 8)
-                                mma_ts_pair(dS, tbase + kColQ + kbk * 32 + ks * 8, bd, idesc, acc);
-                            else
-                                mma_ss_pair(dS, make_sdesc(qr + ks * 32, 16, 1024, kSwizzle128B), bd,
-                                            idesc, acc);
+                        const uint64_t bd = kdesc0 + (uint64_t)(st * (kKBlock >> 4));
+                        if (kbk < 8) {  // latent dims: A = Q from TMEM
+                            const uint32_t aa = tbase + kColQ + kbk * 32;
+                            mma_ts_pair(dS, aa, bd, idesc, kbk > 0 ? 1u : 0u);
+                            mma_ts_pair(dS, aa + 8, bd + 2, idesc, 1u);
+                            mma_ts_pair(dS, aa + 16, bd + 4, idesc, 1u);
+                            mma_ts_pair(dS, aa + 24, bd + 6, idesc, 1u);
+                        } else {        // RoPE dims: A = Q's RoPE tile in shared memory
+                            mma_ss_pair(dS, qrdesc, bd, idesc, 1u);
+                            mma_ss_pair(dS, qrdesc + 2, bd + 2, idesc, 1u);
+                            mma_ss_pair(dS, qrdesc + 4, bd + 4, idesc, 1u);
+                            mma_ss_pair(dS, qrdesc + 6, bd + 6, idesc, 1u);
                         }
-                        mma_commit_pair_mc(ba(S.k_empty[st]), 0x3);
+                        mma_commit_pair_mc(kempty0 + 8 * st, 0x3);
+                        if (++st == kKStages) {
+                            st = 0;
+                            ph ^= 1u;
+                        }
                     }
                     if (ok) mma_commit_pair_mc(ba(S.s_full), 0x3);
                 }
@@ -384,38 +393,19 @@ partial_quad_kernel(const PartialArgs a) {
             }
         } else {
             // ------------------------------------------------ rank 1: forward readiness to rank 0
-            // One thread polls (without blocking) the two event streams rank 0
-            // needs from this CTA: filled K stages and released S tiles.
+            // Copies complete on this CTA's own barriers; rank 0's MMA issuer
+            // learns of each filled K stage through this thread.
             if (lane == 0) {
                 bool ok = mbar_wait(ba(S.q_ready), 0, abort_p);
                 tc_fence_after();
                 tc_fence_before();
                 if (ok) mbar_arrive_remote(mapa_shared(ba(S.q_peer), 0));
                 const int nfill = ntiles * (kDqk / 64);
-                const uint32_t sfree_peer = mapa_shared(ba(S.s_free), 0);
-                int g = 0, i = 0;
-                uint64_t t_last = globaltimer_ns();
-                while (ok && (g < nfill || i < ntiles)) {
-                    bool prog = false;
-                    if (g < nfill && mbar_test_wait(ba(S.k_full[g % kKStages]), (g / kKStages) & 1)) {
-                        fence_proxy_async_smem();
-                        mbar_arrive_remote(mapa_shared(ba(S.k_full[g % kKStages]), 0));
-                        ++g;
-                        prog = true;
-                    }
-                    if (i < ntiles && mbar_test_wait(ba(S.s_free), i & 1)) {
-                        tc_fence_after();
-                        tc_fence_before();
-                        mbar_arrive_remote(sfree_peer);
-                        ++i;
-                        prog = true;
-                    }
-                    if (prog) {
-                        t_last = globaltimer_ns();
-                    } else if (*abort_p || globaltimer_ns() - t_last > 2000000000ull) {
-                        *abort_p = 1;
-                        ok = false;
-                    }
+                for (int g = 0; ok && g < nfill; ++g) {
+                    const int st = g % kKStages;
+                    if (!mbar_wait(ba(S.k_full[st]), (g / kKStages) & 1, abort_p)) break;
+                    fence_proxy_async_smem();
+                    mbar_arrive_remote(mapa_shared(ba(S.k_full[st]), 0));
                 }
             }
         }
@@ -480,6 +470,7 @@ partial_quad_kernel(const PartialArgs a) {
                 mbar_arrive(ba(S.q_ready));
             }
             const uint64_t anc_t = S.anc[t];
+            const uint32_t sfree0 = mapa_shared(ba(S.s_free), 0);
             const uint32_t p_local = smem_u32(S.pstage);
             float* alpha_local = reinterpret_cast<float*>(S.pstage + kPBytes);
             float m_ref = -INFINITY, l_part = 0.f;
@@ -503,7 +494,7 @@ partial_quad_kernel(const PartialArgs a) {
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(ba(S.s_free));
+                if (lane == 0) mbar_arrive_remote(sfree0);
                 const int mi = i % kMetaRing;
                 if (!warp_wait(S.meta_full[mi], (i / kMetaRing) & 1, abort_p)) {
                     ok = false;
@@ -654,8 +645,15 @@ partial_quad_kernel(const PartialArgs a) {
             }
         } else if (rank == 2) {
             // ------------------------------------------------ O MMA issuer (pair)
+            // Descriptors are precomputed; the loop only adds offsets.
             if (lane == 0) {
                 const uint32_t idesc = make_idesc_bf16(kRowsBlk, 256, false, true);
+                const uint64_t pdesc0 = make_sdesc(smem_u32(O.pbuf[0]), 16, 1024, kSwizzle128B);
+                const uint64_t vdesc0 = make_sdesc(smem_u32(O.vring[0]), kVSub, 1024, kSwizzle128B);
+                const uint32_t vfull0 = ba(O.v_full[0]), vempty0 = ba(O.v_empty[0]);
+                const uint32_t d0 = tbase, d1 = tbase + 256;
+                int st = 0;
+                uint32_t ph = 0;
                 bool ok = true;
                 for (int i = 0; ok && i < ntiles; ++i) {
                     const int slot = i & 1;
@@ -665,31 +663,28 @@ partial_quad_kernel(const PartialArgs a) {
                     }
                     fence_proxy_async_smem();
                     tc_fence_after();
-                    const uint32_t p0 = smem_u32(O.pbuf[slot]);
+                    const uint64_t pd = pdesc0 + (uint64_t)(slot * (kPSlot >> 4));
+#pragma unroll 1
                     for (int q = 0; q < kNT / kVKeys; ++q) {
-                        const int g = i * (kNT / kVKeys) + q;
-                        const int st = g % kVStages;
-                        if (!mbar_wait_cluster(ba(O.v_full[st]), (g / kVStages) & 1, abort_p)) {
+                        if (!mbar_wait_cluster(vfull0 + 8 * st, ph, abort_p)) {
                             ok = false;
                             break;
                         }
                         fence_proxy_async_smem();
                         tc_fence_after();
-                        const uint32_t vs = smem_u32(O.vring[st]);
-#pragma unroll
-                        for (int kk = 0; kk < 2; ++kk) {
-                            const int kg = q * kVKeys + kk * 16;  // key within the tile
-                            const uint64_t ad = make_sdesc(p0 + (kg >> 6) * kPBlock + ((kg & 63) >> 4) * 32,
-                                                           16, 1024, kSwizzle128B);
-#pragma unroll
-                            for (int hv = 0; hv < 2; ++hv) {
-                                const uint64_t bd = make_sdesc(vs + hv * 2 * kVSub + kk * 2048, kVSub,
-                                                               1024, kSwizzle128B);
-                                mma_ss_pair(tbase + hv * 256, ad, bd, idesc,
-                                            (i > 0 || q > 0 || kk > 0) ? 1u : 0u);
-                            }
+                        const uint64_t vd = vdesc0 + (uint64_t)(st * (kVStage >> 4));
+                        // keys q*32 .. q*32+31 of the tile: P block q/2, 32-byte K steps
+                        const uint64_t ad = pd + (uint64_t)((q >> 1) * (kPBlock >> 4) + (q & 1) * 4);
+                        const uint32_t acc0 = (i > 0 || q > 0) ? 1u : 0u;
+                        mma_ss_pair(d0, ad, vd, idesc, acc0);
+                        mma_ss_pair(d1, ad, vd + (2 * kVSub >> 4), idesc, acc0);
+                        mma_ss_pair(d0, ad + 2, vd + (2048 >> 4), idesc, 1u);
+                        mma_ss_pair(d1, ad + 2, vd + ((2 * kVSub + 2048) >> 4), idesc, 1u);
+                        mma_commit_pair_mc(vempty0 + 8 * st, 0xC);
+                        if (++st == kVStages) {
+                            st = 0;
+                            ph ^= 1u;
                         }
-                        mma_commit_pair_mc(ba(O.v_empty[st]), 0xC);
                     }
                     if (!ok) break;
                     mma_commit_pair_mc(ba(O.o_done[slot]), 0xC);

@@ -285,7 +285,7 @@ struct __align__(1024) GatherSmem {
     int abort_flag;
 };
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(512, 1)
 gather_rate_kernel(const __grid_constant__ CUtensorMap map, const __nv_bfloat16* kv,
                    const int32_t* slots, int ntile, int method, int nw, int tma_rows, long long* cycles,
                    int* err) {
@@ -388,7 +388,7 @@ gather_rate_kernel(const __grid_constant__ CUtensorMap map, const __nv_bfloat16*
             }
         }
         if (method <= 1) cp_async_wait_all();
-    } else if (warp == 5 && lane == 0) {
+    } else if (warp == 15 && lane == 0) {
         for (int u = 0; u < ntile * 9; ++u) {
             const int st = u % kGStages;
             if (!mbar_wait(smem_u32(&g.full[st]), (u / kGStages) & 1, &g.abort_flag)) {
@@ -410,12 +410,12 @@ extern "C" __attribute__((visibility("default"))) int mlav_gather_rate(
     int nw, int tma_rows, long long* cycles, int* err) {
     CUtensorMap map;
     if (!mlav::make_kv_gather_map(&map, kv, pool)) return -2;
-    if (nw < 1 || nw > 4 || method < 0 || method > 4) return -1;
+    if (nw < 1 || nw > 12 || (method != 0 && nw > 4) || method < 0 || method > 4) return -1;
     if (method == 4 && (tma_rows < 4 || tma_rows > 252 || tma_rows % 4 != 0)) return -1;
     const int smem = (int)sizeof(GatherSmem) + 1024;
     cudaError_t e = cudaFuncSetAttribute(gather_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return (int)e;
-    gather_rate_kernel<<<nblocks, 192, smem>>>(map, static_cast<const __nv_bfloat16*>(kv), slots, ntile,
+    gather_rate_kernel<<<nblocks, 512, smem>>>(map, static_cast<const __nv_bfloat16*>(kv), slots, ntile,
                                                method, nw, tma_rows, cycles, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;
@@ -523,15 +523,39 @@ namespace {
 struct __align__(1024) PairSmem {
     unsigned char a[128 * 128];  // [128 rows][64 bf16]
     unsigned char b[128 * 128];  // K-major [N/2][64] or MN-major [N/2 / 64][64 k][64 n]
-    uint64_t bar;
+    uint64_t bar, tick;
     uint32_t tmem;
     int abort_flag;
 };
 
+template <bool kATmem, int kVar>
+__device__ __forceinline__ void pair_issue(uint32_t taddr, uint32_t acol, uint32_t a0, uint32_t b0,
+                                           bool b_mn, uint32_t idesc, int reps, uint32_t tick) {
+    const uint64_t bd0 = b_mn ? make_sdesc(b0, 64 * 128, 1024, kSwizzle128B)
+                              : make_sdesc(b0, 16, 1024, kSwizzle128B);
+    const uint64_t bstep = b_mn ? (2048 >> 4) : (32 >> 4);
+    const uint64_t ad0 = make_sdesc(a0, 16, 1024, kSwizzle128B);
+    for (int rep = 0; rep < reps; ++rep) {
+        if (kVar == 2) {
+            (void)mbar_test_wait(tick, 0);
+            fence_proxy_async_smem();
+            tc_fence_after();
+        }
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            if (kATmem)
+                mma_ts_pair(taddr, taddr + acol + ks * 8, bd0 + bstep * ks, idesc, ks > 0);
+            else
+                mma_ss_pair(taddr, ad0 + 2 * ks, bd0 + bstep * ks, idesc, ks > 0);
+        }
+        if (kVar >= 1) mma_commit_pair_mc(tick, (uint16_t)3);
+    }
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
 pair_probe_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __restrict__ B,
-                  float* __restrict__ D, int N, int mode, int reps, uint32_t* addr,
-                  long long* cycles, int* err) {
+                  float* __restrict__ D, int N, int mode, int reps, int commit_every,
+                  uint32_t* addr, long long* cycles, int* err) {
     extern __shared__ __align__(1024) unsigned char raw[];
     unsigned char* base = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
     PairSmem& sm = *reinterpret_cast<PairSmem*>(base);
@@ -571,6 +595,7 @@ pair_probe_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __re
     }
     if (tid == 0) {
         mbar_init(smem_u32(&sm.bar), 1);
+        mbar_init(smem_u32(&sm.tick), 1);
         sm.abort_flag = 0;
         fence_mbar_init();
     }
@@ -596,16 +621,18 @@ pair_probe_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __re
         const uint32_t idesc = make_idesc_bf16(256, N, false, b_mn);
         const uint32_t a0 = smem_u32(sm.a), b0 = smem_u32(sm.b);
         const long long t0 = clock64();
-        for (int rep = 0; rep < reps; ++rep) {
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t bd = b_mn ? make_sdesc(b0 + ks * 2048, 64 * 128, 1024, kSwizzle128B)
-                                         : make_sdesc(b0 + ks * 32, 16, 1024, kSwizzle128B);
-                if (a_tmem)
-                    mma_ts_pair(my_addr, my_addr + kAcolP + ks * 8, bd, idesc, ks > 0);
-                else
-                    mma_ss_pair(my_addr, make_sdesc(a0 + ks * 32, 16, 1024, kSwizzle128B), bd, idesc,
-                                ks > 0);
-            }
+        // Issue variants (selected outside the loop): 0 plain; 1 commit after
+        // every 4 MMAs; 2 per 4 MMAs an mbarrier test, the proxy and tcgen05
+        // fences and a commit (the partial kernel's per-stage work).
+        const int var = commit_every;
+        if (a_tmem) {
+            if (var == 0) pair_issue<true, 0>(my_addr, kAcolP, a0, b0, b_mn, idesc, reps, smem_u32(&sm.tick));
+            else if (var == 1) pair_issue<true, 1>(my_addr, kAcolP, a0, b0, b_mn, idesc, reps, smem_u32(&sm.tick));
+            else pair_issue<true, 2>(my_addr, kAcolP, a0, b0, b_mn, idesc, reps, smem_u32(&sm.tick));
+        } else {
+            if (var == 0) pair_issue<false, 0>(my_addr, kAcolP, a0, b0, b_mn, idesc, reps, smem_u32(&sm.tick));
+            else if (var == 1) pair_issue<false, 1>(my_addr, kAcolP, a0, b0, b_mn, idesc, reps, smem_u32(&sm.tick));
+            else pair_issue<false, 2>(my_addr, kAcolP, a0, b0, b_mn, idesc, reps, smem_u32(&sm.tick));
         }
         mma_commit_pair_mc(smem_u32(&sm.bar), (uint16_t)3);
         if (mbar_wait(smem_u32(&sm.bar), 0, &sm.abort_flag)) cycles[0] = clock64() - t0;
@@ -632,8 +659,8 @@ pair_probe_kernel(const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __re
 }  // namespace
 
 extern "C" __attribute__((visibility("default"))) int mlav_pair_probe(
-    const void* A, const void* B, float* D, int N, int mode, int reps, uint32_t* addr,
-    long long* cycles, int* err) {
+    const void* A, const void* B, float* D, int N, int mode, int reps, int commit_every,
+    uint32_t* addr, long long* cycles, int* err) {
     if (mode < 0 || mode > 2 || reps < 1 || reps > 4096) return -1;
     if (mode == 0 && N != 128 && N != 256) return -1;
     if (mode == 1 && N != 128 && N != 256) return -1;
@@ -642,8 +669,8 @@ extern "C" __attribute__((visibility("default"))) int mlav_pair_probe(
     cudaError_t e = cudaFuncSetAttribute(pair_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return (int)e;
     pair_probe_kernel<<<2, 128, smem>>>(static_cast<const __nv_bfloat16*>(A),
-                                        static_cast<const __nv_bfloat16*>(B), D, N, mode, reps, addr,
-                                        cycles, err);
+                                        static_cast<const __nv_bfloat16*>(B), D, N, mode, reps,
+                                        commit_every, addr, cycles, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;
     return (int)cudaDeviceSynchronize();

@@ -91,7 +91,7 @@ def pair_probe():
     lib = ctypes.CDLL(B.build_selftest())
     f = lib.mlav_pair_probe
     f.restype = ctypes.c_int
-    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p] * 3
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 + [ctypes.c_void_p] * 3
     return f
 
 
@@ -111,7 +111,7 @@ def test_cta_pair_mma(pair_probe, mode, N):
     addr = torch.full((2,), -1, dtype=torch.int32, device="cuda")
     cyc = torch.zeros(1, dtype=torch.int64, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    rc = pair_probe(dA.data_ptr(), dB.data_ptr(), D.data_ptr(), N, mode, 1, addr.data_ptr(),
+    rc = pair_probe(dA.data_ptr(), dB.data_ptr(), D.data_ptr(), N, mode, 1, 0, addr.data_ptr(),
                     cyc.data_ptr(), err.data_ptr())
     assert rc == 0, f"pair probe launch failed: {rc}"
     assert int(err.item()) == 0, "pair probe wait timed out"
