@@ -32,13 +32,22 @@
 //
 // Operand readiness across a pair: each CTA's copies land on its own
 // mbarrier; the odd CTA's MMA warp forwards each completed stage to the
-// even CTA's barrier with a cluster-scope arrive. MMA completion is committed
-// to the barriers of both CTAs of the pair (multicast).
+// even CTA's barrier with a remote arrive. MMA completion is committed to
+// the barriers of both CTAs of the pair (multicast). Barriers that only
+// signal completed work (landed copies, finished TMEM reads, completed
+// MMAs) use default (CTA-scope) arrive and wait semantics, which cost far
+// less than cluster-scope release/acquire; the one hand-over of data stored
+// into another CTA's shared memory (the final row maxima and sums) uses
+// cluster scope.
 //
 // Every wait is bounded; on a timeout a CTA drains its MMAs, reaches the
 // final cluster barrier, frees TMEM and flags MLA_STATUS_TIMEOUT.
 #include "partial_tc.cuh"
 #include "tc_ptx.cuh"
+
+#ifndef PREFETCH_ROW
+#define PREFETCH_ROW(p) prefetch_l2_bulk((p), kDqk * 2)
+#endif
 
 namespace mlav {
 namespace {
@@ -49,17 +58,22 @@ constexpr int kRowsBlk = 256;     // rows per work item
 constexpr int kMh = 128;          // rows per CTA
 constexpr int kNT = 256;          // keys per tile
 constexpr int kNh = 128;          // keys per S-CTA per tile
-constexpr int kThreads = 512;     // 16 warps = 4 warpgroups
+constexpr int kThreads = 640;     // 20 warps = 5 warpgroups
 constexpr int kWarpMMA = 4;
 constexpr int kWarpCtl = 7;       // P sender (S CTAs) / P slot release (O pair)
-constexpr int kSProd = 6;         // S-side producer warps: 0-3, 5, 6
+constexpr int kSProd = 10;        // S-side producer warps: 0-3, 5, 6, 16-19
 constexpr int kSGroup = 2;        // producer warps per K stage (stages go round-robin to groups)
-constexpr int kOProd = 10;        // O-side producer warps: 0-3, 5, 6, 12-15
-// Launched at 128 registers per thread (512 x 128 = 65,536). S CTAs:
-// warpgroups 0-1 drop to 72 and the softmax warpgroups rise to 184
-// (256 x 72 + 256 x 184 = 65,536). O CTAs: warpgroups 0, 1, 3 drop to 72.
-constexpr int kRegsLow = 72, kRegsSoftmax = 184;
+constexpr int kOProd = 14;        // O-side producer warps: 0-3, 5, 6, 12-19
+// Launched at 96 registers per thread (640 x 96 = 61,440). S CTAs:
+// warpgroups 0, 1, 4 drop to 48 and the softmax warpgroups (2, 3) rise to
+// 168 (384 x 48 + 256 x 168 = 61,440). O CTAs: warpgroups 0, 1, 3, 4 drop
+// to 48; the correction warpgroup keeps 96.
+constexpr int kRegsLow = 48, kRegsSoftmax = 168;
 constexpr int kKStages = 8;
+// A producer group waits for the release of the stage one lap back; with more
+// groups than stages it could pass a whole lap (parity aliasing) and reuse a
+// stage still in use.
+static_assert(kSProd / kSGroup <= kKStages, "producer groups must not exceed the K stages");
 constexpr uint32_t kKBlock = kNh * 128;        // 128 keys x 64 dims (bf16) = 16 KB
 constexpr int kMetaRing = 4;
 constexpr int kRowsRing = 4;       // pool-row staging, two tiles ahead of the copies
@@ -87,7 +101,7 @@ struct SmemS {
     uint64_t k_full[kKStages], k_empty[kKStages];
     uint64_t meta_full[kMetaRing], meta_free[kMetaRing];
     uint64_t s_full, s_free, q_ready, q_peer, mx_bar[2], pw_bar[2], pstage_free;
-    uint64_t rows_full[kRowsRing], rows_free[kRowsRing];
+    uint64_t rows_full[kRowsRing];
     uint64_t p_free[2];
 };
 struct SmemO {
@@ -122,6 +136,9 @@ static_assert(kPXfer <= kPSlot && kPSlot % 1024 == 0, "P slot");
 
 __device__ __forceinline__ uint32_t ba(const uint64_t& b) { return smem_u32(&b); }
 
+// Whole warps park in try_wait; the single-thread hand-over roles (MMA
+// issuers, forwarders, the P sender and slot release) poll with
+// mbar_wait_spin, since their resume latency is on a pipeline's critical path.
 __device__ __forceinline__ bool warp_wait(const uint64_t& bar, uint32_t parity,
                                           volatile int* abort) {
     const bool ok = mbar_wait(ba(bar), parity, abort);
@@ -210,7 +227,7 @@ partial_quad_kernel(const PartialArgs a) {
             }
             for (int i = 0; i < kMetaRing; ++i) {
                 mbar_init(ba(S.meta_full[i]), 1);
-                mbar_init(ba(S.meta_free[i]), 256);
+                mbar_init(ba(S.meta_free[i]), 8);   // one arrival per softmax warp
             }
             mbar_init(ba(S.s_full), 1);
             mbar_init(ba(S.s_free), 16);  // rank 0's: the softmax warps of both S CTAs
@@ -218,13 +235,12 @@ partial_quad_kernel(const PartialArgs a) {
             mbar_init(ba(S.q_ready), 256);
             mbar_init(ba(S.q_peer), 1);
             for (int i = 0; i < 2; ++i) {
-                mbar_init(ba(S.mx_bar[i]), 256);
-                mbar_init(ba(S.pw_bar[i]), 256);
+                mbar_init(ba(S.mx_bar[i]), 8);
+                mbar_init(ba(S.pw_bar[i]), 8);
                 mbar_init(ba(S.p_free[i]), 1);
             }
             for (int i = 0; i < kRowsRing; ++i) {
                 mbar_init(ba(S.rows_full[i]), 1);
-                mbar_init(ba(S.rows_free[i]), (kDqk / 64) * kSGroup);
             }
         } else {
             SmemO& O = sm.u.o;
@@ -255,25 +271,29 @@ partial_quad_kernel(const PartialArgs a) {
     volatile int* abort_p = &sm.h.abort_flag;
 
     const int wg = warp >> 2;
-    if (sside && wg < 2) {
+    if (sside && wg != 2 && wg != 3) {
         regs_dec<kRegsLow>();
         SmemS& S = sm.u.s;
         if (warp != kWarpMMA && warp != kWarpCtl) {
             // ------------------------------------------------ S producers: K blocks
-            // The six producer warps form three groups of two; stage g (this
-            // CTA's 128 keys x 64 dims of one tile) is copied by group g mod 3,
+            // The ten producer warps form five groups of two; stage g (this
+            // CTA's 128 keys x 64 dims of one tile) is copied by group g mod 5,
             // eight lanes per 128-byte row segment, so that stages complete
             // independently of one another.
-            const int pw = warp < kWarpMMA ? warp : warp - 1;  // 0..5
+            const int pw = warp < kWarpMMA ? warp : (warp < 8 ? warp - 1 : warp - 10);  // 0..9
             const int grp = pw / kSGroup, gw = pw % kSGroup;
             constexpr int kNGroups = kSProd / kSGroup;
             bool ok = warp_wait(S.q_ready, 0, abort_p);  // the ring doubles as Q staging
             const int nfill = ntiles * (kDqk / 64);
+            int seen = -1;  // last tile whose pool rows this warp has waited for
             for (int g = grp; ok && g < nfill; g += kNGroups) {
                 const int i = g / (kDqk / 64), kbk = g % (kDqk / 64);
                 const int rs = i % kRowsRing;
                 const int st = g % kKStages;
-                if (!warp_wait(S.rows_full[rs], (i / kRowsRing) & 1, abort_p)) break;
+                if (i != seen) {
+                    if (!warp_wait(S.rows_full[rs], (i / kRowsRing) & 1, abort_p)) break;
+                    seen = i;
+                }
                 if (g >= kKStages && !warp_wait(S.k_empty[st], ((g / kKStages) - 1) & 1, abort_p)) break;
                 const int32_t* my_rows = S.rows[rs] + hr * kNh;
                 const uint32_t dst0 = smem_u32(S.kring[st]);
@@ -285,8 +305,6 @@ partial_quad_kernel(const PartialArgs a) {
                     cp_async_16_zfill_nc(dst0 + sw128_offset(key, c), src, slot >= 0);
                 }
                 cp_async_mbar_arrive_noinc(ba(S.k_full[st]));
-                __syncwarp();
-                if (lane == 0) mbar_arrive(ba(S.rows_free[rs]));
             }
             cp_async_wait_all();
         } else if (warp == kWarpCtl) {
@@ -296,10 +314,13 @@ partial_quad_kernel(const PartialArgs a) {
             // each tile's P (and rescale factors) from the staging tile to the
             // O partner's slot once that slot is free, then hands the staging
             // tile back to the softmax.
+            // Slot j % 4 last held tile j - 4; the softmax has released that
+            // tile's validity bits only after its S tile was complete, i.e.
+            // after every producer had issued every stage of it, so the pool
+            // rows are free as well.
+            static_assert(kRowsRing == kMetaRing, "rows and metadata share the release");
             auto stage = [&](int j) -> bool {
                 const int rs = j % kRowsRing, mi = j % kMetaRing;
-                if (j >= kRowsRing && !warp_wait(S.rows_free[rs], ((j / kRowsRing) - 1) & 1, abort_p))
-                    return false;
                 if (j >= kMetaRing && !warp_wait(S.meta_free[mi], ((j / kMetaRing) - 1) & 1, abort_p))
                     return false;
                 bad |= stage_rows(a, kbase, kb + j * kNT, ke, lane, S.rows[rs], S.valid[mi]);
@@ -318,8 +339,8 @@ partial_quad_kernel(const PartialArgs a) {
                 int sent = 1;
                 if (lane == 0) {
                     const int slot = i & 1;
-                    sent = mbar_wait(ba(S.pw_bar[slot]), (i >> 1) & 1, abort_p);
-                    if (sent && i >= 2) sent = mbar_wait_cluster(ba(S.p_free[slot]), ((i - 2) >> 1) & 1, abort_p);
+                    sent = mbar_wait_spin(ba(S.pw_bar[slot]), (i >> 1) & 1, abort_p);
+                    if (sent && i >= 2) sent = mbar_wait_spin(ba(S.p_free[slot]), ((i - 2) >> 1) & 1, abort_p);
                     if (sent) {
                         const uint32_t dst = mapa_shared(smem_u32(sm.u.o.pbuf[slot]), orank);
                         const uint32_t bar = mapa_shared(ba(sm.u.o.p_full[slot]), orank);
@@ -343,8 +364,8 @@ partial_quad_kernel(const PartialArgs a) {
             // issuing thread does between MMAs is lost tensor time.
             if (lane == 0) {
                 const uint32_t idesc = make_idesc_bf16(kRowsBlk, kNT, false, false);
-                bool ok = mbar_wait(ba(S.q_ready), 0, abort_p) &&
-                          mbar_wait_cluster(ba(S.q_peer), 0, abort_p);
+                bool ok = mbar_wait_spin(ba(S.q_ready), 0, abort_p) &&
+                          mbar_wait_spin(ba(S.q_peer), 0, abort_p);
                 fence_proxy_async_smem();
                 tc_fence_after();
                 const uint32_t dS = tbase + kColS;
@@ -354,14 +375,14 @@ partial_quad_kernel(const PartialArgs a) {
                 int st = 0;
                 uint32_t ph = 0;
                 for (int i = 0; ok && i < ntiles; ++i) {
-                    if (i >= 1 && !mbar_wait_cluster(ba(S.s_free), (i - 1) & 1, abort_p)) {
+                    if (i >= 1 && !mbar_wait_spin(ba(S.s_free), (i - 1) & 1, abort_p)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
 #pragma unroll 1
                     for (int kbk = 0; kbk < kDqk / 64; ++kbk) {
-                        if (!mbar_wait_cluster(kfull0 + 8 * st, ph, abort_p)) {
+                        if (!mbar_wait_spin(kfull0 + 8 * st, ph, abort_p)) {
                             ok = false;
                             break;
                         }
@@ -396,14 +417,14 @@ partial_quad_kernel(const PartialArgs a) {
             // Copies complete on this CTA's own barriers; rank 0's MMA issuer
             // learns of each filled K stage through this thread.
             if (lane == 0) {
-                bool ok = mbar_wait(ba(S.q_ready), 0, abort_p);
+                bool ok = mbar_wait_spin(ba(S.q_ready), 0, abort_p);
                 tc_fence_after();
                 tc_fence_before();
                 if (ok) mbar_arrive_remote(mapa_shared(ba(S.q_peer), 0));
                 const int nfill = ntiles * (kDqk / 64);
                 for (int g = 0; ok && g < nfill; ++g) {
                     const int st = g % kKStages;
-                    if (!mbar_wait(ba(S.k_full[st]), (g / kKStages) & 1, abort_p)) break;
+                    if (!mbar_wait_spin(ba(S.k_full[st]), (g / kKStages) & 1, abort_p)) break;
                     fence_proxy_async_smem();
                     mbar_arrive_remote(mapa_shared(ba(S.k_full[st]), 0));
                 }
@@ -503,7 +524,8 @@ partial_quad_kernel(const PartialArgs a) {
                 uint32_t vw[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) vw[q] = row_ok ? S.valid[mi][4 * half + q] : 0u;
-                mbar_arrive(ba(S.meta_free[mi]));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ba(S.meta_free[mi]));
                 const int k0 = kb + i * kNT + 128 * half;
                 if (k0 + 128 > Lb) {  // this half reaches the tree keys
 #pragma unroll
@@ -519,7 +541,8 @@ partial_quad_kernel(const PartialArgs a) {
                     mx = fmaxf(mx, sc[c]);
                 }
                 S.mx[i & 1][half][r] = mx;
-                mbar_arrive(ba(S.mx_bar[i & 1]));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ba(S.mx_bar[i & 1]));
                 if (!warp_wait(S.mx_bar[i & 1], (i >> 1) & 1, abort_p)) {
                     ok = false;
                     break;
@@ -564,7 +587,8 @@ partial_quad_kernel(const PartialArgs a) {
                 l_part += psum;
                 if (half == 0) alpha_local[r] = alpha;
                 fence_proxy_async_smem();
-                mbar_arrive(ba(S.pw_bar[i & 1]));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ba(S.pw_bar[i & 1]));
             }
             if (ok) {
                 if (half == 0) {
@@ -581,9 +605,9 @@ partial_quad_kernel(const PartialArgs a) {
         SmemO& O = sm.u.o;
         if (warp != kWarpMMA && warp != kWarpCtl) {
             // ------------------------------------------------ O producers: V segments
-            // Warps 0-3, 5, 6 and 12-15 copy, for 32 keys per stage, this
+            // Warps 0-3, 5, 6 and 12-19 copy, for 32 keys per stage, this
             // CTA's four 64-dim segments (eight lanes per 128-byte segment).
-            const int pw = warp < kWarpMMA ? warp : (warp < 8 ? warp - 1 : warp - 6);  // 0..9
+            const int pw = warp < kWarpMMA ? warp : (warp < 8 ? warp - 1 : warp - 6);  // 0..13
             bool ok = true;
             for (int i = 0; ok && i < ntiles; ++i) {
                 const int rs = i % kRowsRing;
@@ -628,6 +652,14 @@ partial_quad_kernel(const PartialArgs a) {
                 (void)stage_rows(a, kbase, kb + j * kNT, ke, lane, O.rows[rs], nullptr);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ba(O.rows_full[rs]));
+                // This CTA's half of tile j's pool rows into L2, about a tile
+                // before the S pair gathers them (the O pair runs a tile behind
+                // the S pair and stages rows two tiles ahead of itself).
+#pragma unroll
+                for (int q = 0; q < kNT / 64; ++q) {
+                    const int32_t slot = O.rows[rs][hr * (kNT / 2) + 32 * q + lane];
+                    if (slot >= 0) PREFETCH_ROW(a.kv + (int64_t)slot * kDqk);
+                }
                 return true;
             };
             bool ok = stage(0) && (ntiles < 2 || stage(1));
@@ -635,7 +667,7 @@ partial_quad_kernel(const PartialArgs a) {
                 if (i + 2 < ntiles && !stage(i + 2)) break;
                 int rel = 1;
                 if (rank == 2 && lane == 0 && i + 2 < ntiles) {
-                    rel = mbar_wait(ba(O.o_done[i & 1]), (i >> 1) & 1, abort_p);
+                    rel = mbar_wait_spin(ba(O.o_done[i & 1]), (i >> 1) & 1, abort_p);
                     if (rel) {
                         mbar_arrive_remote(mapa_shared(ba(sm.u.s.p_free[i & 1]), 0));
                         mbar_arrive_remote(mapa_shared(ba(sm.u.s.p_free[i & 1]), 1));
@@ -657,7 +689,7 @@ partial_quad_kernel(const PartialArgs a) {
                 bool ok = true;
                 for (int i = 0; ok && i < ntiles; ++i) {
                     const int slot = i & 1;
-                    if (!mbar_wait_cluster(ba(O.o_gate[slot]), (i >> 1) & 1, abort_p)) {
+                    if (!mbar_wait_spin(ba(O.o_gate[slot]), (i >> 1) & 1, abort_p)) {
                         ok = false;
                         break;
                     }
@@ -666,7 +698,7 @@ partial_quad_kernel(const PartialArgs a) {
                     const uint64_t pd = pdesc0 + (uint64_t)(slot * (kPSlot >> 4));
 #pragma unroll 1
                     for (int q = 0; q < kNT / kVKeys; ++q) {
-                        if (!mbar_wait_cluster(vfull0 + 8 * st, ph, abort_p)) {
+                        if (!mbar_wait_spin(vfull0 + 8 * st, ph, abort_p)) {
                             ok = false;
                             break;
                         }
@@ -698,7 +730,7 @@ partial_quad_kernel(const PartialArgs a) {
                 const int nfill = ntiles * (kNT / kVKeys);
                 for (int g = 0; g < nfill; ++g) {
                     const int st = g % kVStages;
-                    if (!mbar_wait(ba(O.v_full[st]), (g / kVStages) & 1, abort_p)) break;
+                    if (!mbar_wait_spin(ba(O.v_full[st]), (g / kVStages) & 1, abort_p)) break;
                     fence_proxy_async_smem();
                     mbar_arrive_remote(mapa_shared(ba(O.v_full[st]), 2));
                 }

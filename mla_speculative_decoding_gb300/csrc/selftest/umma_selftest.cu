@@ -675,3 +675,140 @@ extern "C" __attribute__((visibility("default"))) int mlav_pair_probe(
     if (e != cudaSuccess) return (int)e;
     return (int)cudaDeviceSynchronize();
 }
+
+namespace {
+
+// Round trip of an empty producer/consumer ring (no data): one producer warp
+// signals stage g full, one consumer thread waits for it and releases the
+// stage; the producer waits for the release of stage g - depth before
+// signalling stage g. Measures the signalling latency alone.
+//   prod_mode 0: mbarrier.arrive by lane 0 (count 1)
+//   prod_mode 1: cp.async.mbarrier.arrive.noinc by all 32 lanes (count 32)
+//   cons_mode 0: mbarrier.arrive (count 1)
+//   cons_mode 1: tcgen05.commit (1-CTA) with no MMA in flight
+struct RingSmem {
+    uint64_t full[16], empty[16];
+    uint32_t tmem;
+    int abort_flag;
+};
+
+__global__ void __launch_bounds__(64, 1)
+ring_probe_kernel(int depth, int n, int prod_mode, int cons_mode, long long* cycles, int* err) {
+    __shared__ RingSmem r;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&r.tmem), 32);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int i = 0; i < depth; ++i) {
+            mbar_init(smem_u32(&r.full[i]), prod_mode == 1 ? 32 : 1);
+            mbar_init(smem_u32(&r.empty[i]), 1);
+        }
+        r.abort_flag = 0;
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const long long t0 = clock64();
+    if (warp == 0) {
+        for (int g = 0; g < n; ++g) {
+            const int st = g % depth;
+            if (g >= depth) {
+                const bool ok = mbar_wait(smem_u32(&r.empty[st]), ((g / depth) - 1) & 1, &r.abort_flag);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    if (lane == 0) atomicExch(err, 1);
+                    break;
+                }
+            }
+            if (prod_mode == 1)
+                cp_async_mbar_arrive_noinc(smem_u32(&r.full[st]));
+            else if (lane == 0)
+                mbar_arrive(smem_u32(&r.full[st]));
+            __syncwarp();
+        }
+    } else if (lane == 0) {
+        for (int g = 0; g < n; ++g) {
+            const int st = g % depth;
+            if (!mbar_wait(smem_u32(&r.full[st]), (g / depth) & 1, &r.abort_flag)) {
+                atomicExch(err, 2);
+                break;
+            }
+            if (cons_mode == 1)
+                mma_commit(smem_u32(&r.empty[st]));
+            else
+                mbar_arrive(smem_u32(&r.empty[st]));
+        }
+        cycles[0] = clock64() - t0;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(r.tmem, 32);
+    }
+}
+
+}  // namespace
+
+extern "C" __attribute__((visibility("default"))) int mlav_ring_probe(int depth, int n, int prod_mode,
+                                                                      int cons_mode, long long* cycles,
+                                                                      int* err) {
+    if (depth < 1 || depth > 16 || n < 1 || prod_mode < 0 || prod_mode > 1 || cons_mode < 0 ||
+        cons_mode > 1)
+        return -1;
+    ring_probe_kernel<<<1, 64>>>(depth, n, prod_mode, cons_mode, cycles, err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return (int)e;
+    return (int)cudaDeviceSynchronize();
+}
+
+namespace {
+
+// Cost of single mbarrier operations issued back to back by one thread:
+//   op 0: try_wait.parity on a completed phase
+//   op 1: test_wait.parity on a completed phase
+//   op 2: arrive on a barrier whose phase does not complete (count 8192,
+//         n <= 4096 arrivals; counts must stay within the hardware range
+//         [1, 2^20 - 1])
+//   op 3: try_wait.parity.acquire.cluster on a completed phase
+//   op 4: arrive + try_wait on the next (completing) phase, count 1
+__global__ void __launch_bounds__(32, 1) mbar_cost_kernel(int op, int n, long long* cycles,
+                                                          int* sink) {
+    __shared__ uint64_t bar[2];
+    if (threadIdx.x != 0) return;
+    mbar_init(smem_u32(&bar[0]), 1);
+    mbar_init(smem_u32(&bar[1]), 8192);
+    fence_mbar_init();
+    mbar_arrive(smem_u32(&bar[0]));  // phase 0 of bar[0] completes
+    int acc = 0;
+    const long long t0 = clock64();
+    if (op == 0) {
+        for (int i = 0; i < n; ++i) acc += mbar_try_wait(smem_u32(&bar[0]), 0) ? 1 : 0;
+    } else if (op == 1) {
+        for (int i = 0; i < n; ++i) acc += mbar_test_wait(smem_u32(&bar[0]), 0) ? 1 : 0;
+    } else if (op == 2) {
+        for (int i = 0; i < n; ++i) mbar_arrive(smem_u32(&bar[1]));
+    } else if (op == 3) {
+        for (int i = 0; i < n; ++i) acc += mbar_try_wait_cluster(smem_u32(&bar[0]), 0) ? 1 : 0;
+    } else {
+        for (int i = 0; i < n; ++i) {
+            mbar_arrive(smem_u32(&bar[0]));  // phase i + 1 completes
+            acc += mbar_try_wait(smem_u32(&bar[0]), (uint32_t)((i + 1) & 1)) ? 1 : 0;
+        }
+    }
+    cycles[0] = clock64() - t0;
+    sink[0] = acc;
+}
+
+}  // namespace
+
+extern "C" __attribute__((visibility("default"))) int mlav_mbar_cost(int op, int n, long long* cycles,
+                                                                     int* sink) {
+    if (op < 0 || op > 4 || n < 1 || n > 4096) return -1;
+    mbar_cost_kernel<<<1, 32>>>(op, n, cycles, sink);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return (int)e;
+    return (int)cudaDeviceSynchronize();
+}
