@@ -471,6 +471,91 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+# ----------------------------------------------------------------- building-block probes
+def run_probes():
+    """Microbenchmarks of the building blocks the partial kernels rely on
+    (test-only library libmlaselftest.so): 2-SM MMA issue rate, scattered-row
+    gather throughput, mbarrier operation costs and producer/consumer
+    hand-over. Prints one table; not part of the bench contract."""
+    import ctypes
+    import torch
+    from mla_speculative_decoding_gb300 import build as mbuild
+
+    lib = ctypes.CDLL(mbuild.build_selftest())
+    torch.cuda.set_device(0)
+    cyc = torch.zeros(1, dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    # 2-SM MMA (M = 256, K = 16), single accumulator chain, tight issue loop.
+    f = lib.mlav_pair_probe
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 + [ctypes.c_void_p] * 3
+    g = torch.Generator().manual_seed(1)
+    A = torch.randn(256, 64, generator=g).to(torch.bfloat16).cuda()
+    addr = torch.zeros(2, dtype=torch.int32, device="cuda")
+    print("pair MMA (cta_group::2, M=256, K=16), cycles per MMA; peak = 128 (N=256) / 64 (N=128)")
+    for mode, N, label in ((1, 256, "A TMEM, B K-major"), (0, 256, "A smem, B K-major"),
+                           (2, 256, "A smem, B MN-major"), (1, 128, "A TMEM, B K-major")):
+        Bm = (torch.randn(N, 64, generator=g) if mode in (0, 1) else torch.randn(64, N, generator=g))
+        Bm = Bm.to(torch.bfloat16).cuda()
+        D = torch.zeros(256, N, dtype=torch.float32, device="cuda")
+        row = []
+        for var in (0, 2):
+            rc = f(A.data_ptr(), Bm.data_ptr(), D.data_ptr(), N, mode, 256, var, addr.data_ptr(),
+                   cyc.data_ptr(), err.data_ptr())
+            assert rc == 0 and int(err.item()) == 0
+            row.append(int(cyc.item()) / (4 * 256))
+        print(f"  N={N:3d} {label:20s}: plain {row[0]:6.1f}   with per-4-MMA barrier test, fences, commit {row[1]:6.1f}")
+
+    # Scattered 128-byte row segments into shared memory, all SMs.
+    f = lib.mlav_gather_rate
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p] + [ctypes.c_int] * 5 + \
+        [ctypes.c_void_p] * 2
+    pool = 1_200_000
+    kv = torch.randn(pool, 576, device="cuda", dtype=torch.bfloat16)
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    cyc_sm = torch.zeros(nsm, dtype=torch.int64, device="cuda")
+    print("gather: bytes per clock per SM, 256 keys x 9 segments per tile, all SMs")
+    for label, hi in (("rows in HBM (1.2M-slot pool)", pool), ("rows L2-resident (20k slots)", 20000)):
+        rng = np.random.default_rng(0)
+        slots = torch.from_numpy(rng.integers(0, hi, size=nsm * 8 * 256).astype(np.int32)).cuda()
+        parts = []
+        for method, nw, tr in ((0, 2, 0), (0, 4, 0), (0, 8, 0), (0, 12, 0), (2, 1, 0), (4, 4, 32)):
+            for _ in range(2):
+                rc = f(kv.data_ptr(), pool, slots.data_ptr(), nsm, 8, method, nw, tr, cyc_sm.data_ptr(),
+                       err.data_ptr())
+            assert rc == 0 and int(err.item()) == 0
+            c = cyc_sm.float().mean().item()
+            name = {0: f"cp.async x{nw} warps", 2: "TMA gather4", 4: "cp.async x4 + gather4 1/8"}[method]
+            parts.append(f"{name} {8 * 9 * 256 * 128 / c:5.1f}")
+        print(f"  {label}: " + "; ".join(parts))
+
+    # mbarrier operations (one thread) and a producer/consumer ring.
+    f = lib.mlav_mbar_cost
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    names = ["try_wait, phase complete", "test_wait, phase complete", "arrive",
+             "try_wait.acquire.cluster, complete", "arrive + try_wait"]
+    print("mbarrier, cycles per operation (one thread)")
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for op in range(5):
+        rc = f(op, 4096, cyc.data_ptr(), sink.data_ptr())
+        assert rc == 0
+        print(f"  {names[op]:36s} {int(cyc.item()) / 4096:6.1f}")
+    f = lib.mlav_ring_probe
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p] * 2
+    print("empty ring (producer warp -> consumer thread, parking try_wait), cycles per stage")
+    for depth in (1, 8):
+        for pm in (0, 1):
+            for cm in (0, 1):
+                rc = f(depth, 4096, pm, cm, cyc.data_ptr(), err.data_ptr())
+                assert rc == 0 and int(err.item()) == 0
+                print(f"  depth {depth} producer {'cp.async arrive' if pm else 'arrive':15s} "
+                      f"consumer {'tcgen05.commit' if cm else 'arrive':14s} {int(cyc.item()) / 4096:6.1f}")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -483,7 +568,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-step-s", type=float, default=4.0)
+    ap.add_argument("--probes", action="store_true",
+                    help="run the building-block microbenchmarks instead of the bench")
     args = ap.parse_args()
+    if args.probes:
+        run_probes()
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     args.flags = 1 if args.simt else 0

@@ -45,10 +45,6 @@
 #include "partial_tc.cuh"
 #include "tc_ptx.cuh"
 
-#ifndef PREFETCH_ROW
-#define PREFETCH_ROW(p) prefetch_l2_bulk((p), kDqk * 2)
-#endif
-
 namespace mlav {
 namespace {
 
@@ -652,14 +648,6 @@ partial_quad_kernel(const PartialArgs a) {
                 (void)stage_rows(a, kbase, kb + j * kNT, ke, lane, O.rows[rs], nullptr);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ba(O.rows_full[rs]));
-                // This CTA's half of tile j's pool rows into L2, about a tile
-                // before the S pair gathers them (the O pair runs a tile behind
-                // the S pair and stages rows two tiles ahead of itself).
-#pragma unroll
-                for (int q = 0; q < kNT / 64; ++q) {
-                    const int32_t slot = O.rows[rs][hr * (kNT / 2) + 32 * q + lane];
-                    if (slot >= 0) PREFETCH_ROW(a.kv + (int64_t)slot * kDqk);
-                }
                 return true;
             };
             bool ok = stage(0) && (ntiles < 2 || stage(1));
