@@ -13,17 +13,18 @@ import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "mla_verify_oracle.c")
+SRCS = [SRC, os.path.join(HERE, "next_rows_oracle.c")]
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libmlaoracle.so")
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
     if (not force and os.path.exists(LIB)
-            and os.path.getmtime(LIB) >= os.path.getmtime(SRC)):
+            and all(os.path.getmtime(LIB) >= os.path.getmtime(f) for f in SRCS)):
         return LIB
     os.makedirs(OUT_DIR, exist_ok=True)
     tmp = LIB + f".tmp{os.getpid()}"
-    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math", SRC, "-o", tmp, "-lm"]
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math", *SRCS, "-o", tmp, "-lm"]
     cmd = base[:1] + ["-fopenmp"] + base[1:]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:

@@ -13,6 +13,14 @@ from .gen import (  # noqa: F401
     VerifyInputs,
     bf16_bits_to_f32,
     f32_to_bf16_bits,
+    SPARSE_DECODE,
+    AcceptInputs,
+    IndexerInputs,
+    RelocateInputs,
+    make_accept_inputs,
     make_config,
+    make_indexer_inputs,
     make_inputs,
+    make_relocate_inputs,
+    make_sparse_decode,
 )

@@ -47,6 +47,12 @@ CONFIGS = {
             tree="random", pool_slots=1_200_000, nsplit=64, seed=4),
 }
 
+# Sparse-MLA decode: each of 16 requests' 64 heads attend over a top-k list of
+# 512 scattered slots (given as the request's prefix) plus the token's own
+# slot (T = 1), split 8 ways over the keys.
+SPARSE_DECODE = dict(name="sparse-decode", batch=16, num_heads=64, prefix="fixed:512", T=1,
+                     tree="chain", pool_slots=1_200_000, nsplit=8, seed=5)
+
 
 def f32_to_bf16_bits(x: np.ndarray, chunk: int = 1 << 24) -> np.ndarray:
     """Round float32 values to bf16 (nearest, ties to even); returns uint16 bits."""
@@ -217,3 +223,122 @@ def make_config(idx: int, placement: str = "scattered", seed: int | None = None,
                        tree=c["tree"], pool_slots=c["pool_slots"], nsplit=c["nsplit"],
                        seed=c["seed"] if seed is None else seed, placement=placement,
                        name=c["name"])
+
+
+def make_sparse_decode(seed: int | None = None, **over):
+    """The sparse-MLA decode workload (see SPARSE_DECODE)."""
+    c = dict(SPARSE_DECODE)
+    c.update(over)
+    return make_inputs(batch=c["batch"], num_heads=c["num_heads"], prefix=c["prefix"], T=c["T"],
+                       tree=c["tree"], pool_slots=c["pool_slots"], nsplit=c["nsplit"],
+                       seed=c["seed"] if seed is None else seed, name=c["name"])
+
+
+# ---------------------------------------------------------------- tree acceptance
+@dataclass
+class AcceptInputs:
+    tree_parent: np.ndarray      # int32 [B, T], parent[0] = -1
+    draft_tokens: np.ndarray     # int32 [B, T], token proposed at each node (node 0: last committed)
+    target_argmax: np.ndarray    # int32 [B, T], the target model's greedy next token after each node
+    out_cache_loc: np.ndarray    # int32 [B, T], KV slot of each node
+
+
+def make_accept_inputs(*, batch, T, tree="random", vocab=32000, match=0.7, pool_slots=1 << 20,
+                       seed=0):
+    """Draft trees with tokens and target choices. At each node, with
+    probability `match` the target's choice is the draft token of one of the
+    node's children (drawn uniformly), else a random token."""
+    rng = np.random.default_rng(seed)
+    par = _draw_tree(rng, tree, batch, T).astype(np.int32)
+    draft = rng.integers(0, vocab, size=(batch, T)).astype(np.int32)
+    target = rng.integers(0, vocab, size=(batch, T)).astype(np.int32)
+    for b in range(batch):
+        for t in range(T):
+            kids = np.nonzero(par[b] == t)[0]
+            if kids.size and rng.random() < match:
+                target[b, t] = draft[b, kids[rng.integers(0, kids.size)]]
+    loc = rng.permutation(pool_slots)[:batch * T].reshape(batch, T).astype(np.int32)
+    return AcceptInputs(par, draft, target, loc)
+
+
+# ---------------------------------------------------------------- KV relocation
+@dataclass
+class RelocateInputs:
+    kv_pool: np.ndarray          # uint16 (bf16 bits) [S, 576]
+    req_to_token: np.ndarray     # int32 [R, stride]
+    req_pool_indices: np.ndarray  # int32 [B]
+    prefix_lens: np.ndarray      # int32 [B]
+    dst_start: np.ndarray        # int32 [B], contiguous free destination range per request
+    progress: np.ndarray         # int32 [B], rows already moved (0)
+
+
+def make_relocate_inputs(*, batch, prefix, pool_slots, seed=0, poison=True, in_place=0):
+    """Scattered live rows in the low part of the pool and, for every request,
+    a contiguous free destination range in the top part. `in_place` rows at
+    the start of request 0 already sit at their destination."""
+    rng = np.random.default_rng(seed)
+    L = _draw_prefix(rng, prefix, batch)
+    total = int(L.sum())
+    if 2 * total > pool_slots:
+        raise ValueError("pool too small")
+    top = pool_slots - total
+    src = rng.permutation(top)[:total].astype(np.int64)
+    dst_start = (top + np.concatenate([[0], np.cumsum(L)[:-1]])).astype(np.int32)
+    if in_place and batch:
+        k = min(in_place, int(L[0]))
+        src[:k] = dst_start[0] + np.arange(k)
+    kv_pool = np.full((pool_slots, D_QK), BF16_NAN if poison else np.uint16(0), dtype=np.uint16)
+    kv_pool[src] = f32_to_bf16_bits(rng.standard_normal((total, D_QK), dtype=np.float32))
+    stride = int(L.max()) if batch else 1
+    req_to_token = np.full((batch, max(stride, 1)), -1, dtype=np.int32)
+    rpi = np.array([batch - 1 - b for b in range(batch)], dtype=np.int32)
+    off = 0
+    for b in range(batch):
+        req_to_token[rpi[b], :L[b]] = src[off:off + L[b]]
+        off += int(L[b])
+    return RelocateInputs(kv_pool, req_to_token, rpi, L.astype(np.int32), dst_start,
+                          np.zeros(batch, dtype=np.int32))
+
+
+# ---------------------------------------------------------------- fp8 paged MQA indexer
+@dataclass
+class IndexerInputs:
+    q: np.ndarray            # uint8 fp8-e4m3 codes [B, H, 128]
+    weights: np.ndarray      # float32 [B, H]
+    kv_blocks: np.ndarray    # uint8 [nblocks, 8448]: 64 x 128 fp8 codes, then 64 fp32 scales
+    block_table: np.ndarray  # int32 [B, max_pages]; -1 past a request's pages
+    seq_lens: np.ndarray     # int32 [B]
+
+
+def _e4m3_codes(rng, shape, emin=4, emax=9):
+    """Random fp8-e4m3 codes with exponent field in [emin, emax] (magnitudes
+    2^-3 .. ~2^3), random sign and mantissa; never the NaN codes."""
+    s = rng.integers(0, 2, size=shape)
+    e = rng.integers(emin, emax + 1, size=shape)
+    m = rng.integers(0, 8, size=shape)
+    return ((s << 7) | (e << 3) | m).astype(np.uint8)
+
+
+def make_indexer_inputs(*, batch, num_heads=64, seq_lens, max_pages, nblocks=None, seed=0):
+    """Queries, per-head weights, paged fp8 keys with per-position fp32 scales
+    and a page table of distinct physical blocks per request."""
+    rng = np.random.default_rng(seed)
+    lens = _draw_prefix(rng, seq_lens, batch).astype(np.int32)
+    pages = (lens + 63) // 64
+    if (pages > max_pages).any():
+        raise ValueError("seq_lens exceed max_pages")
+    need = int(pages.sum())
+    nblocks = nblocks if nblocks is not None else max(need, 1)
+    q = _e4m3_codes(rng, (batch, num_heads, 128))
+    w = (rng.standard_normal((batch, num_heads)) / 8.0).astype(np.float32)
+    kv = np.zeros((nblocks, 8448), dtype=np.uint8)
+    kv[:, :8192] = _e4m3_codes(rng, (nblocks, 8192))
+    scales = rng.uniform(0.5, 2.0, size=(nblocks, 64)).astype(np.float32) / 16.0
+    kv[:, 8192:] = scales.view(np.uint8).reshape(nblocks, 256)
+    perm = rng.permutation(nblocks)
+    bt = np.full((batch, max_pages), -1, dtype=np.int32)
+    off = 0
+    for b in range(batch):
+        bt[b, :pages[b]] = perm[off:off + pages[b]]
+        off += int(pages[b])
+    return IndexerInputs(q, w, kv, bt, lens)
