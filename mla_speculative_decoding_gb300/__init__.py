@@ -3,7 +3,9 @@
 The product is the C-ABI library libmlaverify.so (include/mla_verify.h):
 an index/tree-mask builder kernel, a split-KV partial attention kernel
 (tcgen05/TMEM tensor cores, with a CUDA-core path for other shapes) and a
-log-sum-exp combine kernel. This package is its thin Python binding.
+log-sum-exp combine kernel; beside them (include/mla_decode_steps.h) greedy
+tree acceptance, KV relocation and the fp8 paged indexer logits. This
+package is its thin Python binding.
 """
 
 from .binding import (  # noqa: F401
@@ -24,6 +26,9 @@ from .binding import (  # noqa: F401
     library_path,
     load,
     mla_build_verify_meta,
+    mla_fp8_indexer_logits,
+    mla_kv_relocate,
+    mla_tree_accept,
     mla_verify_attention,
     mla_verify_attention_anc,
     mla_verify_attention_noalloc,

@@ -64,6 +64,13 @@ _SIGS = {
     "mla_verify_noalloc_scratch_bytes": (_c_size, []),
     "mla_verify_attention_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _vp,
                                               _vp, _c_int, _c_int, _c_i64, _c_f32, _vp, _vp]),
+    # include/mla_decode_steps.h
+    "mla_tree_accept": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _vp, _vp, _vp, _vp, _vp,
+                                 _vp]),
+    "mla_kv_relocate": (_c_int, [_vp, _c_i64, _vp, _c_i64, _vp, _vp, _vp, _vp, _c_int, _c_int,
+                                 _vp, _vp]),
+    "mla_fp8_indexer_logits": (_c_int, [_vp, _vp, _vp, _c_i64, _vp, _vp, _c_int, _c_int, _c_int,
+                                        _vp, _vp, _vp]),
 }
 
 _LIB = None
@@ -267,3 +274,54 @@ def mla_verify_attention_noalloc(q, kv_pool, kv_indices, kv_indptr, prefix_lens,
         nsplit, _p(out), _p(lse), batch, H, kv_pool.shape[0], float(softmax_scale), _p(status),
         _stream(stream))
     _check("mla_verify_attention_noalloc", rc)
+
+
+
+# ---------------------------------------------------------------- decode steps (mla_decode_steps.h)
+def mla_tree_accept(tree_parent, draft_tokens, target_argmax, out_cache_loc, commit_len,
+                    accepted_nodes, kept_slots, next_tokens, status, stream=None) -> None:
+    """Greedy acceptance along each request's draft tree; all int32 CUDA
+    tensors, [B, T] inputs and outputs, commit_len [B]."""
+    for name, t in (("tree_parent", tree_parent), ("draft_tokens", draft_tokens),
+                    ("target_argmax", target_argmax), ("out_cache_loc", out_cache_loc),
+                    ("commit_len", commit_len), ("accepted_nodes", accepted_nodes),
+                    ("kept_slots", kept_slots), ("next_tokens", next_tokens), ("status", status)):
+        _want(t, torch.int32, name)
+    B, T = tree_parent.shape
+    rc = load().mla_tree_accept(_p(tree_parent), _p(draft_tokens), _p(target_argmax),
+                                _p(out_cache_loc), B, T, _p(commit_len), _p(accepted_nodes),
+                                _p(kept_slots), _p(next_tokens), _p(status), _stream(stream))
+    _check("mla_tree_accept", rc)
+
+
+def mla_kv_relocate(kv_pool, req_to_token, req_pool_indices, prefix_lens, dst_start, progress,
+                    budget, status, stream=None) -> None:
+    """One relocation call (moves up to `budget` rows per request)."""
+    _want(kv_pool, torch.bfloat16, "kv_pool")
+    for name, t in (("req_to_token", req_to_token), ("req_pool_indices", req_pool_indices),
+                    ("prefix_lens", prefix_lens), ("dst_start", dst_start),
+                    ("progress", progress), ("status", status)):
+        _want(t, torch.int32, name)
+    rc = load().mla_kv_relocate(_p(kv_pool), kv_pool.shape[0], _p(req_to_token),
+                                req_to_token.shape[1], _p(req_pool_indices), _p(prefix_lens),
+                                _p(dst_start), _p(progress), prefix_lens.shape[0], int(budget),
+                                _p(status), _stream(stream))
+    _check("mla_kv_relocate", rc)
+
+
+def mla_fp8_indexer_logits(q, weights, kv_blocks, block_table, seq_lens, logits, status,
+                           stream=None) -> None:
+    """Indexer logits [B, max_pages * 64] (fp32) from fp8-e4m3 bytes q
+    [B, H, 128] (uint8), weights [B, H] fp32, kv_blocks [nblocks, 8448] uint8,
+    block_table [B, max_pages] int32, seq_lens [B] int32."""
+    _want(q, torch.uint8, "q")
+    _want(kv_blocks, torch.uint8, "kv_blocks")
+    _want(weights, torch.float32, "weights")
+    _want(logits, torch.float32, "logits")
+    for name, t in (("block_table", block_table), ("seq_lens", seq_lens), ("status", status)):
+        _want(t, torch.int32, name)
+    B, H, _ = q.shape
+    rc = load().mla_fp8_indexer_logits(_p(q), _p(weights), _p(kv_blocks), kv_blocks.shape[0],
+                                       _p(block_table), _p(seq_lens), B, H, block_table.shape[1],
+                                       _p(logits), _p(status), _stream(stream))
+    _check("mla_fp8_indexer_logits", rc)

@@ -43,7 +43,7 @@ def _sources():
 
 def _deps():
     return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [
-        os.path.join(INCLUDE, "mla_verify.h"), os.path.abspath(__file__)]
+        *sorted(glob.glob(os.path.join(INCLUDE, "*.h"))), os.path.abspath(__file__)]
 
 
 def up_to_date() -> bool:

@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "mla_decode_steps.h"
 #include "partial_tc.cuh"
 
 namespace mlav {
@@ -43,7 +44,8 @@ int init_device(int device) {
     } else if (major != 10 || minor != 3) {
         rc = MLA_ERR_UNSUPPORTED;  // the library carries sm_103a code only
     } else if (setup_partial_simt() != cudaSuccess || setup_partial_tc() != cudaSuccess ||
-               setup_partial_pair() != cudaSuccess || setup_partial_quad() != cudaSuccess) {
+               setup_partial_pair() != cudaSuccess || setup_partial_quad() != cudaSuccess ||
+               setup_fp8_indexer() != cudaSuccess) {
         rc = MLA_ERR_CUDA;
     }
     if (rc == MLA_OK) {
@@ -294,4 +296,66 @@ MLAV_API int mla_verify_combine(const void* workspace, int batch, int T, int num
     rc = ensure_ready(stream, nullptr);
     if (rc != MLA_OK) return rc;
     return run_combine(workspace, batch, T, num_heads, nsplit, out, lse, stream);
+}
+
+// ---------------------------------------------------------------- decode steps
+namespace {
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
+
+MLAV_API int mla_tree_accept(const int32_t* tree_parent, const int32_t* draft_tokens,
+                             const int32_t* target_argmax, const int32_t* out_cache_loc, int batch,
+                             int T, int32_t* commit_len, int32_t* accepted_nodes,
+                             int32_t* kept_slots, int32_t* next_tokens, int32_t* status,
+                             cudaStream_t stream) {
+    if (!tree_parent || !draft_tokens || !target_argmax || !out_cache_loc || !commit_len ||
+        !accepted_nodes || !kept_slots || !next_tokens || !status)
+        return MLA_ERR_INVALID_ARG;
+    if (batch < 1 || batch > 65535 || T < 1 || T > MLA_MAX_TREE) return MLA_ERR_INVALID_ARG;
+    int rc = ensure_ready(stream, nullptr);
+    if (rc != MLA_OK) return rc;
+    return launch_tree_accept(tree_parent, draft_tokens, target_argmax, out_cache_loc, batch, T,
+                              commit_len, accepted_nodes, kept_slots, next_tokens, status,
+                              stream) == cudaSuccess
+               ? MLA_OK
+               : MLA_ERR_CUDA;
+}
+
+MLAV_API int mla_kv_relocate(void* kv_pool, int64_t pool_slots, int32_t* req_to_token,
+                             int64_t req_to_token_stride, const int32_t* req_pool_indices,
+                             const int32_t* prefix_lens, const int32_t* dst_start, int32_t* progress,
+                             int batch, int budget, int32_t* status, cudaStream_t stream) {
+    if (!kv_pool || !req_to_token || !req_pool_indices || !prefix_lens || !dst_start || !progress ||
+        !status || !al16(kv_pool))
+        return MLA_ERR_INVALID_ARG;
+    if (pool_slots < 1 || pool_slots > ((int64_t)1 << 31) || req_to_token_stride < 1 || batch < 1 ||
+        batch > 65535 || budget < 1 || budget > (1 << 20))
+        return MLA_ERR_INVALID_ARG;
+    int rc = ensure_ready(stream, nullptr);
+    if (rc != MLA_OK) return rc;
+    return launch_kv_relocate(kv_pool, pool_slots, req_to_token, req_to_token_stride,
+                              req_pool_indices, prefix_lens, dst_start, progress, batch, budget,
+                              status, stream) == cudaSuccess
+               ? MLA_OK
+               : MLA_ERR_CUDA;
+}
+
+MLAV_API int mla_fp8_indexer_logits(const void* q, const float* weights, const void* kv_blocks,
+                                    int64_t nblocks, const int32_t* block_table,
+                                    const int32_t* seq_lens, int batch, int num_heads,
+                                    int max_pages, float* logits, int32_t* status,
+                                    cudaStream_t stream) {
+    if (!q || !weights || !kv_blocks || !block_table || !seq_lens || !logits || !status ||
+        !al16(q) || !al16(kv_blocks))
+        return MLA_ERR_INVALID_ARG;
+    if (batch < 1 || batch > 65535 || num_heads < 1 || num_heads > MLA_MAX_HEADS || max_pages < 0 ||
+        max_pages > 65535 || nblocks < 0)
+        return MLA_ERR_INVALID_ARG;
+    if (max_pages == 0) return MLA_OK;
+    int rc = ensure_ready(stream, nullptr);
+    if (rc != MLA_OK) return rc;
+    return launch_fp8_indexer(q, weights, kv_blocks, nblocks, block_table, seq_lens, batch,
+                              num_heads, max_pages, logits, status, stream) == cudaSuccess
+               ? MLA_OK
+               : MLA_ERR_CUDA;
 }

@@ -1,0 +1,245 @@
+// Decode steps beside the verify attention: greedy tree acceptance, KV
+// relocation, fp8 paged MQA indexer logits (see mla_decode_steps.h).
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "mla_decode_steps.h"
+
+namespace mlav {
+namespace {
+
+// ---------------------------------------------------------------- tree acceptance
+// One warp per request; lane l holds nodes l and l + 32. Each step ballots
+// the children of the current node whose draft token equals the target's
+// choice there and takes the lowest-numbered one.
+__global__ void __launch_bounds__(32)
+tree_accept_kernel(const int32_t* __restrict__ par, const int32_t* __restrict__ tok,
+                   const int32_t* __restrict__ tgt, const int32_t* __restrict__ loc, int T,
+                   int32_t* __restrict__ commit, int32_t* __restrict__ an, int32_t* __restrict__ ks,
+                   int32_t* __restrict__ nt, int32_t* status) {
+    const int b = blockIdx.x, lane = threadIdx.x;
+    const int64_t base = (int64_t)b * T;
+    int p[2], k[2];
+    bool ok[2];
+    int bad = 0;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int c = lane + 32 * u;
+        p[u] = c < T ? par[base + c] : -2;
+        k[u] = c < T ? tok[base + c] : 0;
+        ok[u] = c < T && (c == 0 ? p[u] == -1 : (p[u] >= 0 && p[u] < c));
+        if (c < T && !ok[u]) bad = MLA_STATUS_BAD_PARENT;
+        if (c < T) an[base + c] = ks[base + c] = nt[base + c] = -1;
+    }
+    __syncwarp();
+    int cur = 0, n = 0;
+    if (lane == 0) ks[base] = loc[base];
+    for (int step = 0; step < T; ++step) {
+        const int want = tgt[base + cur];
+        const unsigned m0 = __ballot_sync(0xffffffffu, lane > 0 && ok[0] && p[0] == cur && k[0] == want);
+        const unsigned m1 = __ballot_sync(0xffffffffu, ok[1] && p[1] == cur && k[1] == want);
+        int nxt;
+        if (m0)
+            nxt = __ffs(m0) - 1;
+        else if (m1)
+            nxt = 32 + __ffs(m1) - 1;
+        else
+            break;
+        if (lane == 0) {
+            an[base + n] = nxt;
+            nt[base + n] = tok[base + nxt];
+            ks[base + n + 1] = loc[base + nxt];
+        }
+        ++n;
+        cur = nxt;
+    }
+    if (lane == 0) {
+        nt[base + n] = tgt[base + cur];
+        commit[b] = n + 1;
+    }
+    bad = __reduce_or_sync(0xffffffffu, bad);
+    if (lane == 0) status_or(status, bad);
+}
+
+// ---------------------------------------------------------------- KV relocation
+constexpr int kRelocRowsPerCta = 64;
+constexpr int kRelocWarps = 8;
+constexpr int kRowVec = kDqk * 2 / 16;  // 72 sixteen-byte pieces per 1152-byte row
+
+__global__ void __launch_bounds__(kRelocWarps * 32)
+kv_relocate_kernel(uint4* __restrict__ kv, int64_t pool_slots, int32_t* __restrict__ r2t,
+                   int64_t stride, const int32_t* __restrict__ rpi, const int32_t* __restrict__ L,
+                   const int32_t* __restrict__ dst, const int32_t* __restrict__ progress, int budget,
+                   int32_t* status) {
+    const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int32_t len = L[b], j0 = progress[b];
+    if (len < 0 || j0 < 0 || j0 > len) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) status_or(status, MLA_STATUS_BAD_PREFIX);
+        return;
+    }
+    const int n = min(budget, len - j0);
+    int32_t* row = r2t + (int64_t)rpi[b] * stride;
+    const int r_end = min(n, (int)(blockIdx.x + 1) * kRelocRowsPerCta);
+    int bad = 0;
+    for (int r = blockIdx.x * kRelocRowsPerCta + warp; r < r_end; r += kRelocWarps) {
+        const int j = j0 + r;
+        const int64_t s = row[j], d = (int64_t)dst[b] + j;
+        if (s < 0 || s >= pool_slots || d < 0 || d >= pool_slots) {
+            bad = MLA_STATUS_BAD_SLOT;
+            continue;
+        }
+        if (s != d) {
+            const uint4* src = kv + s * kRowVec;
+            uint4* out = kv + d * kRowVec;
+            uint4 v[3];
+#pragma unroll
+            for (int u = 0; u < 3; ++u)
+                if (lane + 32 * u < kRowVec) v[u] = __ldg(src + lane + 32 * u);
+#pragma unroll
+            for (int u = 0; u < 3; ++u)
+                if (lane + 32 * u < kRowVec) out[lane + 32 * u] = v[u];
+        }
+        __syncwarp();
+        if (lane == 0) row[j] = (int32_t)d;
+    }
+    if (lane == 0) status_or(status, bad);
+}
+
+__global__ void kv_relocate_progress_kernel(int32_t* progress, const int32_t* L, int batch,
+                                            int budget) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b < batch) {
+        const int32_t len = L[b], j0 = progress[b];
+        if (len >= 0 && j0 >= 0 && j0 <= len) progress[b] = j0 + min(budget, len - j0);
+    }
+}
+
+// ---------------------------------------------------------------- fp8 paged indexer
+// One CTA per (page of 64 positions, request); 128 threads = 64 positions x
+// 2 halves of the 128 dims. Each thread holds its 64 key values and forms
+// the partial dot products with every head's query (broadcast from shared
+// memory); the halves are added, ReLU-weighted and summed over heads in a
+// fixed order, then scaled.
+constexpr int kIxThreads = 128;
+
+__device__ __forceinline__ void fp8x16_to_float(const uint4 v, float* f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)((w[i] >> (16 * h)) & 0xFFFFu);
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+            const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+            f[4 * i + 2 * h] = x.x;
+            f[4 * i + 2 * h + 1] = x.y;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kIxThreads)
+fp8_indexer_kernel(const uint8_t* __restrict__ q, const float* __restrict__ w,
+                   const uint8_t* __restrict__ kv, int64_t nblocks, const int32_t* __restrict__ bt,
+                   const int32_t* __restrict__ lens, int H, int P, float* __restrict__ out,
+                   int32_t* status) {
+    extern __shared__ __align__(16) float ix_smem[];
+    float* qs = ix_smem;                      // [H][128]
+    float* part = qs + H * 128;               // [2][H][64]
+    float* fin = part + 2 * H * 64;           // [2][64]
+    const int p = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+    const int pos = tid & 63, half = tid >> 6;
+    const int32_t len = lens[b];
+    float* o = out + ((int64_t)b * P + p) * 64;
+    if ((int64_t)p * 64 >= len) {             // past the request: no cache reads
+        if (tid < 64) o[tid] = -INFINITY;
+        return;
+    }
+    const int32_t blk = bt[(int64_t)b * P + p];
+    if (blk < 0 || blk >= nblocks) {
+        if (tid < 64) o[tid] = -INFINITY;
+        if (tid == 0) status_or(status, MLA_STATUS_BAD_SLOT);
+        return;
+    }
+    // queries of request b -> fp32 in shared memory
+    const uint4* qv = reinterpret_cast<const uint4*>(q + (int64_t)b * H * 128);
+    for (int i = tid; i < H * 8; i += kIxThreads) fp8x16_to_float(__ldg(qv + i), qs + 16 * i);
+    // this thread's 64 key values
+    const uint8_t* blkp = kv + (int64_t)blk * 8448;
+    const uint4* kvv = reinterpret_cast<const uint4*>(blkp + pos * 128 + half * 64);
+    float k[64];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) fp8x16_to_float(__ldg(kvv + i), k + 16 * i);
+    __syncthreads();
+    for (int h = 0; h < H; ++h) {
+        const float4* qh = reinterpret_cast<const float4*>(qs + h * 128 + half * 64);
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float4 x = qh[i];
+            acc = fmaf(x.x, k[4 * i], acc);
+            acc = fmaf(x.y, k[4 * i + 1], acc);
+            acc = fmaf(x.z, k[4 * i + 2], acc);
+            acc = fmaf(x.w, k[4 * i + 3], acc);
+        }
+        part[(half * H + h) * 64 + pos] = acc;
+    }
+    __syncthreads();
+    // weighted ReLU sum over this thread's half of the heads
+    const int h0 = half * ((H + 1) / 2), h1 = min(H, h0 + (H + 1) / 2);
+    const float* wb = w + (int64_t)b * H;
+    float s = 0.f;
+    for (int h = h0; h < h1; ++h) {
+        const float dot = part[h * 64 + pos] + part[(H + h) * 64 + pos];
+        s = fmaf(__ldg(wb + h), fmaxf(dot, 0.f), s);
+    }
+    fin[half * 64 + pos] = s;
+    __syncthreads();
+    if (half == 0) {
+        float sc;
+        memcpy(&sc, blkp + 8192 + 4 * pos, 4);
+        const bool valid = (int64_t)p * 64 + pos < len;
+        o[pos] = valid ? sc * (fin[pos] + fin[64 + pos]) : -INFINITY;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_tree_accept(const int32_t* par, const int32_t* tok, const int32_t* tgt,
+                               const int32_t* loc, int batch, int T, int32_t* commit, int32_t* an,
+                               int32_t* ks, int32_t* nt, int32_t* status, cudaStream_t stream) {
+    tree_accept_kernel<<<batch, 32, 0, stream>>>(par, tok, tgt, loc, T, commit, an, ks, nt, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_kv_relocate(void* kv, int64_t pool_slots, int32_t* r2t, int64_t stride,
+                               const int32_t* rpi, const int32_t* L, const int32_t* dst,
+                               int32_t* progress, int batch, int budget, int32_t* status,
+                               cudaStream_t stream) {
+    dim3 grid((budget + kRelocRowsPerCta - 1) / kRelocRowsPerCta, batch);
+    kv_relocate_kernel<<<grid, kRelocWarps * 32, 0, stream>>>(
+        static_cast<uint4*>(kv), pool_slots, r2t, stride, rpi, L, dst, progress, budget, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    kv_relocate_progress_kernel<<<(batch + 127) / 128, 128, 0, stream>>>(progress, L, batch, budget);
+    return cudaGetLastError();
+}
+
+size_t fp8_indexer_smem(int H) { return ((size_t)H * 128 + 2 * (size_t)H * 64 + 128) * sizeof(float); }
+
+cudaError_t setup_fp8_indexer() {
+    return cudaFuncSetAttribute(fp8_indexer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)fp8_indexer_smem(MLA_MAX_HEADS));
+}
+
+cudaError_t launch_fp8_indexer(const void* q, const float* w, const void* kv, int64_t nblocks,
+                               const int32_t* bt, const int32_t* lens, int batch, int H, int P,
+                               float* out, int32_t* status, cudaStream_t stream) {
+    dim3 grid(P, batch);
+    fp8_indexer_kernel<<<grid, kIxThreads, fp8_indexer_smem(H), stream>>>(
+        static_cast<const uint8_t*>(q), w, static_cast<const uint8_t*>(kv), nblocks, bt, lens, H, P,
+        out, status);
+    return cudaGetLastError();
+}
+
+}  // namespace mlav
