@@ -400,6 +400,10 @@ def run_ours(args):
         per[idx] = {"us": round(value, 3), "roofline_us": round(roof_us, 3),
                     "frac": round(roof_us / value, 4), "bound": bound}
         result["per_config"] = {str(k): per[k] for k in sorted(per)}
+        try:
+            result["next_rows"] = measure_next_rows(mv, dev, flush, peaks)
+        except Exception as e:
+            result["next_rows"] = {"error": repr(e)}
 
     if rank == 0 and world == 1 and args.cpu_baseline:
         us, sample, threads, dt = time_oracle(inp, target_s=args.cpu_seconds)
@@ -438,6 +442,110 @@ def measure_config(j, mv, dev, flush, peaks, args, steps=10):
     return {"us": round(us, 3), "roofline_us": round(roof, 3), "frac": round(roof / us, 4),
             "bound": bound, "kv_gbps": round(fig["kv_bytes"] / (us * 1e-6) / 1e9, 1),
             "status_ok": ok}
+
+
+def _time_us(fn, flush, steps=10, warm=3):
+    """Mean device time of fn() over `steps` runs, L2 flushed before each
+    (outside the events)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    for _ in range(warm):
+        flush.zero_()
+        fn()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for k in range(steps):
+        flush.zero_()
+        ev[k][0].record(stream)
+        fn()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) * 1e3 for a, b in ev)
+
+
+def measure_next_rows(mv, dev, flush, peaks):
+    """The steps beside the verify attention, each on a workload of the pages'
+    shape: µs per call and the fraction of its roofline (algorithmic bytes at
+    the measured HBM bandwidth, flops at the measured bf16 peak)."""
+    import torch
+    from workloads import (make_accept_inputs, make_indexer_inputs, make_relocate_inputs,
+                           make_sparse_decode)
+    hbm = peaks["hbm_gbs"] * 1e9
+    res = {}
+
+    # f1: sparse-MLA decode (16 requests x 64 heads over 512 top-k slots + self)
+    inp = make_sparse_decode()
+    fig = workload_figures(inp)
+    d = mv.to_device(inp, device=dev)
+    us = _time_us(d.step, flush)
+    roof, bound, _, _ = roofline_us(fig, peaks)
+    res["sparse_decode"] = {"workload": "batch 16, H=64, top-k 512 + self, nsplit 8",
+                            "us": round(us, 2), "roofline_us": round(roof, 3),
+                            "frac": round(roof / us, 4), "bound": bound,
+                            "status_ok": int(d.status.item()) == 0}
+    del d
+
+    # f2: KV relocation, 8 requests x 16384 scattered rows into contiguous ranges, one call
+    x = make_relocate_inputs(batch=8, prefix="fixed:16384", pool_slots=600_000, seed=11,
+                             poison=False)
+    pool = torch.from_numpy(x.kv_pool.view(np.int16)).to(dev).view(torch.bfloat16)
+    r2t0 = torch.from_numpy(x.req_to_token).to(dev)
+    r2t = r2t0.clone()
+    rpi = torch.from_numpy(x.req_pool_indices).to(dev)
+    lens = torch.from_numpy(x.prefix_lens).to(dev)
+    dst = torch.from_numpy(x.dst_start).to(dev)
+    prog = torch.zeros(8, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def reloc():
+        r2t.copy_(r2t0)
+        prog.zero_()
+        mv.mla_kv_relocate(pool, r2t, rpi, lens, dst, prog, 16384, st)
+    t_copy = _time_us(lambda: (r2t.copy_(r2t0), prog.zero_()), flush)
+    us = _time_us(reloc, flush) - t_copy
+    rows = 8 * 16384
+    nbytes = rows * (2 * 1152 + 8)
+    res["kv_relocate"] = {"workload": "8 x 16384 scattered rows, one call", "us": round(us, 2),
+                          "gbps": round(nbytes / (us * 1e-6) / 1e9, 1),
+                          "roofline_us": round(nbytes / hbm * 1e6, 2),
+                          "frac": round(nbytes / hbm * 1e6 / us, 4), "bound": "hbm",
+                          "status_ok": int(st.item()) == 0}
+    del pool
+
+    # f3: greedy acceptance, 64 requests x 64-node trees
+    a = make_accept_inputs(batch=64, T=64, seed=12)
+    tens = [torch.from_numpy(v).to(dev) for v in (a.tree_parent, a.draft_tokens, a.target_argmax,
+                                                  a.out_cache_loc)]
+    outs = [torch.zeros(64, dtype=torch.int32, device=dev)] + \
+        [torch.zeros(64, 64, dtype=torch.int32, device=dev) for _ in range(3)]
+    us = _time_us(lambda: mv.mla_tree_accept(*tens, *outs, st), flush)
+    res["tree_accept"] = {"workload": "64 requests x 64-node trees", "us": round(us, 2),
+                          "bound": "latency"}
+
+    # f4: fp8 indexer, 16 requests x 32768 positions (512 pages) over a 4097-entry table
+    ix = make_indexer_inputs(batch=16, num_heads=64, seq_lens="fixed:32768", max_pages=4097,
+                             seed=13)
+    q = torch.from_numpy(ix.q).to(dev)
+    w = torch.from_numpy(ix.weights).to(dev)
+    kv = torch.from_numpy(ix.kv_blocks).to(dev)
+    bt = torch.from_numpy(ix.block_table).to(dev)
+    sl = torch.from_numpy(ix.seq_lens).to(dev)
+    out = torch.empty(16, 4097 * 64, dtype=torch.float32, device=dev)
+    us = _time_us(lambda: mv.mla_fp8_indexer_logits(q, w, kv, bt, sl, out, st), flush)
+    pages = int(((ix.seq_lens + 63) // 64).sum())
+    nbytes = pages * 8448 + q.numel() + w.numel() * 4 + out.numel() * 4 + bt.numel() * 4
+    flops = 2 * int(ix.seq_lens.sum()) * 64 * 128
+    t_mem = nbytes / hbm * 1e6
+    t_flop = flops / (peaks["bf16_tflops"] * 2 * 1e12) * 1e6   # fp8 tensor rate = 2 x bf16
+    roof = max(t_mem, t_flop)
+    res["fp8_indexer"] = {"workload": "16 x 32768 positions, H=64, 4097-page table",
+                          "us": round(us, 2), "roofline_us": round(roof, 2),
+                          "frac": round(roof / us, 4), "bound": "hbm" if t_mem >= t_flop else "tensor",
+                          "gflops": round(flops / (us * 1e-6) / 1e9, 1),
+                          "status_ok": int(st.item()) == 0}
+    del kv, out
+    torch.cuda.empty_cache()
+    return res
 
 
 # ----------------------------------------------------------------- reference arm
