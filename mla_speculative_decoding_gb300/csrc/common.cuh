@@ -44,6 +44,20 @@ __host__ __device__ inline void split_range(int K, int nsplit, int s, int& beg, 
     end = min(K, beg + chunk);
 }
 
+// Tile-aligned variant for kernels that walk the keys in tiles of `tile`:
+// the ceil(K / tile) tiles are spread as evenly as possible (the first
+// tiles % nsplit splits take one more), so no split carries a mostly empty
+// last tile and the longer work items come first in launch order.
+__host__ __device__ inline void split_range_tiles(int K, int nsplit, int s, int tile, int& beg,
+                                                  int& end) {
+    const int tiles = (K + tile - 1) / tile;
+    const int base = tiles / nsplit, rem = tiles % nsplit;
+    const int t0 = s * base + min(s, rem);
+    const int nt = base + (s < rem ? 1 : 0);
+    beg = min(K, t0 * tile);
+    end = min(K, (t0 + nt) * tile);
+}
+
 __device__ __forceinline__ void status_or(int32_t* st, int bits) {
     if (st != nullptr && bits != 0) atomicOr(st, bits);
 }

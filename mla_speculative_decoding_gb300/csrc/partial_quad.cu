@@ -190,7 +190,7 @@ partial_quad_kernel(const PartialArgs a) {
     int Lb, K;
     int bad = request_keys(a, b, Lb, K);
     int kb, ke;
-    split_range(K, a.nsplit, s, kb, ke);
+    split_range_tiles(K, a.nsplit, s, kNT, kb, ke);
     const int ntiles = (ke - kb + kNT - 1) / kNT;
     const int64_t kbase = a.kv_indptr[b];
 
