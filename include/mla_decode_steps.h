@@ -80,10 +80,14 @@ int mla_kv_relocate(void *kv_pool, int64_t pool_slots, int32_t *req_to_token,
  * block_table[b][p] of kv_blocks [nblocks][8448] (64 x 128 fp8 values, then
  * 64 fp32 scales); q is fp8 e4m3 [batch][num_heads][128], weights fp32
  * [batch][num_heads]. Every other position of logits [batch][max_pages*64]
- * is -inf: the grid is fixed at (max_pages, batch) and pages past a
- * request's length take a fast path without reading the cache, so work
- * scales with the actual lengths. A block index outside [0, nblocks) gives
- * -inf for that page and sets MLA_STATUS_BAD_SLOT. num_heads in [1, 128].
+ * is -inf. The dot products run on the tensor cores (fp8 e4m3 operands, fp32
+ * accumulation; products of two e4m3 values are exact in fp32) in one
+ * persistent launch of one CTA per SM: the 128-position tiles the device
+ * lengths call for are split evenly over the CTAs, so work scales with the
+ * actual lengths while the grid depends on host sizes only. A block index
+ * outside [0, nblocks) gives -inf for that page and sets MLA_STATUS_BAD_SLOT.
+ * num_heads in [1, 128]; nblocks in [0, 2^31); q, kv_blocks and logits
+ * 16-byte aligned (MLA_ERR_INVALID_ARG otherwise).
  */
 int mla_fp8_indexer_logits(const void *q, const float *weights, const void *kv_blocks,
                            int64_t nblocks, const int32_t *block_table, const int32_t *seq_lens,

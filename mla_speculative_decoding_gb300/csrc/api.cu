@@ -346,16 +346,17 @@ MLAV_API int mla_fp8_indexer_logits(const void* q, const float* weights, const v
                                     int max_pages, float* logits, int32_t* status,
                                     cudaStream_t stream) {
     if (!q || !weights || !kv_blocks || !block_table || !seq_lens || !logits || !status ||
-        !al16(q) || !al16(kv_blocks))
+        !al16(q) || !al16(kv_blocks) || !al16(logits))
         return MLA_ERR_INVALID_ARG;
     if (batch < 1 || batch > 65535 || num_heads < 1 || num_heads > MLA_MAX_HEADS || max_pages < 0 ||
-        max_pages > 65535 || nblocks < 0)
+        max_pages > 65535 || nblocks < 0 || nblocks > 0x7fffffffLL)
         return MLA_ERR_INVALID_ARG;
     if (max_pages == 0) return MLA_OK;
-    int rc = ensure_ready(stream, nullptr);
+    int sms = 0;
+    int rc = ensure_ready(stream, &sms);
     if (rc != MLA_OK) return rc;
     return launch_fp8_indexer(q, weights, kv_blocks, nblocks, block_table, seq_lens, batch,
-                              num_heads, max_pages, logits, status, stream) == cudaSuccess
+                              num_heads, max_pages, logits, status, sms, stream) == cudaSuccess
                ? MLA_OK
                : MLA_ERR_CUDA;
 }

@@ -124,7 +124,7 @@ cudaError_t launch_build_meta(const int32_t* req_to_token, int64_t stride, int64
                               int32_t* kv_indices, uint64_t* anc, int32_t* status,
                               cudaStream_t stream);
 
-// Decode steps beside the verify attention (decode_steps.cu).
+// Decode steps beside the verify attention (decode_steps.cu, fp8_indexer.cu).
 cudaError_t launch_tree_accept(const int32_t* par, const int32_t* tok, const int32_t* tgt,
                                const int32_t* loc, int batch, int T, int32_t* commit, int32_t* an,
                                int32_t* ks, int32_t* nt, int32_t* status, cudaStream_t stream);
@@ -135,6 +135,6 @@ cudaError_t launch_kv_relocate(void* kv, int64_t pool_slots, int32_t* r2t, int64
 cudaError_t setup_fp8_indexer();
 cudaError_t launch_fp8_indexer(const void* q, const float* w, const void* kv, int64_t nblocks,
                                const int32_t* bt, const int32_t* lens, int batch, int H, int P,
-                               float* out, int32_t* status, cudaStream_t stream);
+                               float* out, int32_t* status, int grid, cudaStream_t stream);
 
 }  // namespace mlav

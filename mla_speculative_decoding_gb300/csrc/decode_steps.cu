@@ -1,7 +1,5 @@
-// Decode steps beside the verify attention: greedy tree acceptance, KV
-// relocation, fp8 paged MQA indexer logits (see mla_decode_steps.h).
-#include <cuda_fp16.h>
-#include <cuda_fp8.h>
+// Decode steps beside the verify attention: greedy tree acceptance and KV
+// relocation (see mla_decode_steps.h; the fp8 indexer is in fp8_indexer.cu).
 
 #include "common.cuh"
 #include "mla_decode_steps.h"
@@ -115,94 +113,6 @@ __global__ void kv_relocate_progress_kernel(int32_t* progress, const int32_t* L,
     }
 }
 
-// ---------------------------------------------------------------- fp8 paged indexer
-// One CTA per (page of 64 positions, request); 128 threads = 64 positions x
-// 2 halves of the 128 dims. Each thread holds its 64 key values and forms
-// the partial dot products with every head's query (broadcast from shared
-// memory); the halves are added, ReLU-weighted and summed over heads in a
-// fixed order, then scaled.
-constexpr int kIxThreads = 128;
-
-__device__ __forceinline__ void fp8x16_to_float(const uint4 v, float* f) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)((w[i] >> (16 * h)) & 0xFFFFu);
-            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
-            const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-            f[4 * i + 2 * h] = x.x;
-            f[4 * i + 2 * h + 1] = x.y;
-        }
-    }
-}
-
-__global__ void __launch_bounds__(kIxThreads)
-fp8_indexer_kernel(const uint8_t* __restrict__ q, const float* __restrict__ w,
-                   const uint8_t* __restrict__ kv, int64_t nblocks, const int32_t* __restrict__ bt,
-                   const int32_t* __restrict__ lens, int H, int P, float* __restrict__ out,
-                   int32_t* status) {
-    extern __shared__ __align__(16) float ix_smem[];
-    float* qs = ix_smem;                      // [H][128]
-    float* part = qs + H * 128;               // [2][H][64]
-    float* fin = part + 2 * H * 64;           // [2][64]
-    const int p = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-    const int pos = tid & 63, half = tid >> 6;
-    const int32_t len = lens[b];
-    float* o = out + ((int64_t)b * P + p) * 64;
-    if ((int64_t)p * 64 >= len) {             // past the request: no cache reads
-        if (tid < 64) o[tid] = -INFINITY;
-        return;
-    }
-    const int32_t blk = bt[(int64_t)b * P + p];
-    if (blk < 0 || blk >= nblocks) {
-        if (tid < 64) o[tid] = -INFINITY;
-        if (tid == 0) status_or(status, MLA_STATUS_BAD_SLOT);
-        return;
-    }
-    // queries of request b -> fp32 in shared memory
-    const uint4* qv = reinterpret_cast<const uint4*>(q + (int64_t)b * H * 128);
-    for (int i = tid; i < H * 8; i += kIxThreads) fp8x16_to_float(__ldg(qv + i), qs + 16 * i);
-    // this thread's 64 key values
-    const uint8_t* blkp = kv + (int64_t)blk * 8448;
-    const uint4* kvv = reinterpret_cast<const uint4*>(blkp + pos * 128 + half * 64);
-    float k[64];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) fp8x16_to_float(__ldg(kvv + i), k + 16 * i);
-    __syncthreads();
-    for (int h = 0; h < H; ++h) {
-        const float4* qh = reinterpret_cast<const float4*>(qs + h * 128 + half * 64);
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float4 x = qh[i];
-            acc = fmaf(x.x, k[4 * i], acc);
-            acc = fmaf(x.y, k[4 * i + 1], acc);
-            acc = fmaf(x.z, k[4 * i + 2], acc);
-            acc = fmaf(x.w, k[4 * i + 3], acc);
-        }
-        part[(half * H + h) * 64 + pos] = acc;
-    }
-    __syncthreads();
-    // weighted ReLU sum over this thread's half of the heads
-    const int h0 = half * ((H + 1) / 2), h1 = min(H, h0 + (H + 1) / 2);
-    const float* wb = w + (int64_t)b * H;
-    float s = 0.f;
-    for (int h = h0; h < h1; ++h) {
-        const float dot = part[h * 64 + pos] + part[(H + h) * 64 + pos];
-        s = fmaf(__ldg(wb + h), fmaxf(dot, 0.f), s);
-    }
-    fin[half * 64 + pos] = s;
-    __syncthreads();
-    if (half == 0) {
-        float sc;
-        memcpy(&sc, blkp + 8192 + 4 * pos, 4);
-        const bool valid = (int64_t)p * 64 + pos < len;
-        o[pos] = valid ? sc * (fin[pos] + fin[64 + pos]) : -INFINITY;
-    }
-}
-
 }  // namespace
 
 cudaError_t launch_tree_accept(const int32_t* par, const int32_t* tok, const int32_t* tgt,
@@ -222,23 +132,6 @@ cudaError_t launch_kv_relocate(void* kv, int64_t pool_slots, int32_t* r2t, int64
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     kv_relocate_progress_kernel<<<(batch + 127) / 128, 128, 0, stream>>>(progress, L, batch, budget);
-    return cudaGetLastError();
-}
-
-size_t fp8_indexer_smem(int H) { return ((size_t)H * 128 + 2 * (size_t)H * 64 + 128) * sizeof(float); }
-
-cudaError_t setup_fp8_indexer() {
-    return cudaFuncSetAttribute(fp8_indexer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)fp8_indexer_smem(MLA_MAX_HEADS));
-}
-
-cudaError_t launch_fp8_indexer(const void* q, const float* w, const void* kv, int64_t nblocks,
-                               const int32_t* bt, const int32_t* lens, int batch, int H, int P,
-                               float* out, int32_t* status, cudaStream_t stream) {
-    dim3 grid(P, batch);
-    fp8_indexer_kernel<<<grid, kIxThreads, fp8_indexer_smem(H), stream>>>(
-        static_cast<const uint8_t*>(q), w, static_cast<const uint8_t*>(kv), nblocks, bt, lens, H, P,
-        out, status);
     return cudaGetLastError();
 }
 

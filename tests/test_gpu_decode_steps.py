@@ -201,6 +201,64 @@ def test_fp8_indexer_matches_oracle(H, lens):
     _indexer_close(got, ref)
 
 
+@pytest.mark.parametrize("H", [1, 20, 100])
+def test_fp8_indexer_odd_pages_and_lengths_past_the_table(H):
+    """Seven pages: the last 128-position tile holds a single page; the third
+    request is longer than the table, so only its first 448 positions exist."""
+    ix = make_indexer_inputs(batch=3, num_heads=H, seq_lens=[64 * 7, 64 * 5 + 3, 1000],
+                             max_pages=16, seed=30 + H)
+    ix.block_table = np.ascontiguousarray(ix.block_table[:, :7])
+    got, st = _indexer_gpu(ix)
+    ref = oracle.fp8_indexer_logits(ix.q, ix.weights, ix.kv_blocks, ix.block_table, ix.seq_lens)
+    assert st == 0 and got.shape == (3, 448)
+    _indexer_close(got, ref)
+
+
+def test_fp8_indexer_many_short_requests():
+    """300 requests of mixed short lengths (zeros included): each CTA's share
+    spans many requests, so query tiles are reloaded and both query buffers
+    recycled many times."""
+    rng = np.random.default_rng(22)
+    lens = rng.choice([0, 1, 63, 64, 65, 127, 128, 129, 500, 2000], size=300).astype(np.int32)
+    ix = make_indexer_inputs(batch=300, num_heads=64, seq_lens=lens, max_pages=33, seed=22)
+    got, st = _indexer_gpu(ix)
+    ref = oracle.fp8_indexer_logits(ix.q, ix.weights, ix.kv_blocks, ix.block_table, ix.seq_lens)
+    assert st == 0
+    _indexer_close(got, ref)
+
+
+def test_fp8_indexer_long_requests_span_several_windows():
+    """4 requests x 160k positions (5000 tiles): every CTA walks more than 32
+    tiles, crossing producer windows and ring laps; one head keeps the
+    oracle fast."""
+    ix = make_indexer_inputs(batch=4, num_heads=1, seq_lens=[160_000, 159_999, 100_001, 160_000],
+                             max_pages=2500, seed=23)
+    got, st = _indexer_gpu(ix)
+    ref = oracle.fp8_indexer_logits(ix.q, ix.weights, ix.kv_blocks, ix.block_table, ix.seq_lens)
+    assert st == 0
+    _indexer_close(got, ref)
+
+
+def test_fp8_indexer_timed_workload_sampled_pages():
+    """The timed shape (16 requests x 32768 positions, 64 heads, 4097-page
+    table): every position past the lengths is -inf, and two random full
+    pages per request match the oracle run on just those pages (the logits
+    of a page depend only on its block, the request's queries and weights)."""
+    ix = make_indexer_inputs(batch=16, num_heads=64, seq_lens="fixed:32768", max_pages=4097,
+                             seed=13)
+    got, st = _indexer_gpu(ix)
+    assert st == 0
+    assert np.isneginf(got[:, 32768:]).all() and np.isfinite(got[:, :32768]).all()
+    rng = np.random.default_rng(24)
+    pages = np.stack([rng.choice(512, size=2, replace=False) for _ in range(16)]).astype(np.int64)
+    bt = np.take_along_axis(ix.block_table, pages, axis=1).astype(np.int32)
+    ref = oracle.fp8_indexer_logits(ix.q, ix.weights, ix.kv_blocks, bt,
+                                    np.full(16, 128, np.int32))
+    sub = np.stack([np.concatenate([got[b, 64 * p:64 * p + 64] for p in pages[b]])
+                    for b in range(16)])
+    _indexer_close(sub, ref)
+
+
 def test_fp8_indexer_bad_block_is_flagged_and_graph_capturable():
     ix = make_indexer_inputs(batch=2, num_heads=64, seq_lens=[200, 100], max_pages=4, seed=4)
     ix.block_table = ix.block_table.copy()
