@@ -222,6 +222,25 @@ def time_oracle(inp, target_s=10.0, max_rows=None):
 
 
 # ----------------------------------------------------------------- GPU arm
+class L2Flush:
+    """Evicts the inputs from L2 between timed steps: writes a buffer of 4x L2,
+    then reads its first 2x L2, so that L2 ends up holding clean lines of
+    that buffer only (a write-only flush would leave L2 full of dirty lines,
+    whose write-back the next timed kernel would pay for)."""
+
+    DESCRIPTION = ("flushed before every timed step: a 4x L2 buffer written, then 2x L2 of "
+                   "it read back, so no input line and no dirty line stays in L2")
+
+    def __init__(self, l2_bytes, dev):
+        import torch
+        self.l2 = int(l2_bytes)
+        self.buf = torch.empty(max(4 * self.l2, 512 << 20), dtype=torch.uint8, device=dev)
+
+    def __call__(self):
+        self.buf.zero_()
+        self.buf[:2 * self.l2].sum()
+
+
 def run_ours(args):
     import torch
 
@@ -246,7 +265,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
-    flush = torch.empty(max(4 * l2, 512 << 20), dtype=torch.uint8, device=dev)
+    flush = L2Flush(l2, dev)
 
     def one_step(ev=None):
         if ev is not None:
@@ -262,7 +281,7 @@ def run_ours(args):
             ev[3].record(stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         one_step()
     torch.cuda.synchronize()
     assert int(d.status.item()) == 0, "device status word set during warm-up"
@@ -281,7 +300,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     for k in range(args.steps):
-        flush.zero_()
+        flush()
         one_step(evs[k])
     torch.cuda.synchronize()
     barrier(world)
@@ -310,10 +329,10 @@ def run_ours(args):
         ge = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
         for _ in range(3):
-            flush.zero_()
+            flush()
             g.replay()
         for k in range(args.steps):
-            flush.zero_()
+            flush()
             ge[k][0].record(stream)
             g.replay()
             ge[k][1].record(stream)
@@ -334,7 +353,7 @@ def run_ours(args):
     d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
     e2e_us = []
     for k in range(args.warmup + args.steps):
-        flush.zero_()
+        flush()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for name, ht in h_in.items():
@@ -367,7 +386,7 @@ def run_ours(args):
         "config": {"workload": f"config{idx}:{CONFIGS[idx]['name']}", "batch": inp.batch,
                    "heads": inp.num_heads, "prefix_lens": [int(x) for x in inp.prefix_lens][:8],
                    "T": inp.T, "nsplit": inp.nsplit, "pool_slots": inp.pool_slots,
-                   "l2": "flushed before every timed step (buffer of 4x L2 written)",
+                   "l2": L2Flush.DESCRIPTION,
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "kernel": "simt" if args.flags else "default"},
         "kv_gbps": round(fig["kv_bytes"] / (value * 1e-6) / 1e9, 1),
@@ -424,12 +443,12 @@ def measure_config(j, mv, dev, flush, peaks, args, steps=10):
     d = mv.to_device(inp, device=dev)
     stream = torch.cuda.current_stream()
     for _ in range(3):
-        flush.zero_()
+        flush()
         d.step()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
     for k in range(steps):
-        flush.zero_()
+        flush()
         ev[k][0].record(stream)
         d.step()
         ev[k][1].record(stream)
@@ -450,12 +469,12 @@ def _time_us(fn, flush, steps=10, warm=3):
     import torch
     stream = torch.cuda.current_stream()
     for _ in range(warm):
-        flush.zero_()
+        flush()
         fn()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
     for k in range(steps):
-        flush.zero_()
+        flush()
         ev[k][0].record(stream)
         fn()
         ev[k][1].record(stream)
@@ -463,7 +482,10 @@ def _time_us(fn, flush, steps=10, warm=3):
     return statistics.mean(a.elapsed_time(b) * 1e3 for a, b in ev)
 
 
-def measure_next_rows(mv, dev, flush, peaks):
+NEXT_ROWS = ("sparse_decode", "kv_relocate", "tree_accept", "fp8_indexer")
+
+
+def measure_next_rows(mv, dev, flush, peaks, which=NEXT_ROWS):
     """The steps beside the verify attention, each on a workload of the pages'
     shape: µs per call and the fraction of its roofline (algorithmic bytes at
     the measured HBM bandwidth, flops at the measured bf16 peak)."""
@@ -472,80 +494,98 @@ def measure_next_rows(mv, dev, flush, peaks):
                            make_sparse_decode)
     hbm = peaks["hbm_gbs"] * 1e9
     res = {}
-
-    # f1: sparse-MLA decode (16 requests x 64 heads over 512 top-k slots + self)
-    inp = make_sparse_decode()
-    fig = workload_figures(inp)
-    d = mv.to_device(inp, device=dev)
-    us = _time_us(d.step, flush)
-    roof, bound, _, _ = roofline_us(fig, peaks)
-    res["sparse_decode"] = {"workload": "batch 16, H=64, top-k 512 + self, nsplit 8",
-                            "us": round(us, 2), "roofline_us": round(roof, 3),
-                            "frac": round(roof / us, 4), "bound": bound,
-                            "status_ok": int(d.status.item()) == 0}
-    del d
-
-    # f2: KV relocation, 8 requests x 16384 scattered rows into contiguous ranges, one call
-    x = make_relocate_inputs(batch=8, prefix="fixed:16384", pool_slots=600_000, seed=11,
-                             poison=False)
-    pool = torch.from_numpy(x.kv_pool.view(np.int16)).to(dev).view(torch.bfloat16)
-    r2t0 = torch.from_numpy(x.req_to_token).to(dev)
-    r2t = r2t0.clone()
-    rpi = torch.from_numpy(x.req_pool_indices).to(dev)
-    lens = torch.from_numpy(x.prefix_lens).to(dev)
-    dst = torch.from_numpy(x.dst_start).to(dev)
-    prog = torch.zeros(8, dtype=torch.int32, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
 
-    def reloc():
-        r2t.copy_(r2t0)
-        prog.zero_()
-        mv.mla_kv_relocate(pool, r2t, rpi, lens, dst, prog, 16384, st)
-    t_copy = _time_us(lambda: (r2t.copy_(r2t0), prog.zero_()), flush)
-    us = _time_us(reloc, flush) - t_copy
-    rows = 8 * 16384
-    nbytes = rows * (2 * 1152 + 8)
-    res["kv_relocate"] = {"workload": "8 x 16384 scattered rows, one call", "us": round(us, 2),
-                          "gbps": round(nbytes / (us * 1e-6) / 1e9, 1),
-                          "roofline_us": round(nbytes / hbm * 1e6, 2),
-                          "frac": round(nbytes / hbm * 1e6 / us, 4), "bound": "hbm",
-                          "status_ok": int(st.item()) == 0}
-    del pool
+    if "sparse_decode" in which:
+        # f1: sparse-MLA decode (16 requests x 64 heads over 512 top-k slots + self)
+        inp = make_sparse_decode()
+        fig = workload_figures(inp)
+        d = mv.to_device(inp, device=dev)
+        us = _time_us(d.step, flush)
+        roof, bound, _, _ = roofline_us(fig, peaks)
+        res["sparse_decode"] = {"workload": "batch 16, H=64, top-k 512 + self, nsplit 8",
+                                "us": round(us, 2), "roofline_us": round(roof, 3),
+                                "frac": round(roof / us, 4), "bound": bound,
+                                "status_ok": int(d.status.item()) == 0}
+        del d
 
-    # f3: greedy acceptance, 64 requests x 64-node trees
-    a = make_accept_inputs(batch=64, T=64, seed=12)
-    tens = [torch.from_numpy(v).to(dev) for v in (a.tree_parent, a.draft_tokens, a.target_argmax,
-                                                  a.out_cache_loc)]
-    outs = [torch.zeros(64, dtype=torch.int32, device=dev)] + \
-        [torch.zeros(64, 64, dtype=torch.int32, device=dev) for _ in range(3)]
-    us = _time_us(lambda: mv.mla_tree_accept(*tens, *outs, st), flush)
-    res["tree_accept"] = {"workload": "64 requests x 64-node trees", "us": round(us, 2),
-                          "bound": "latency"}
+    if "kv_relocate" in which:
+        # f2: KV relocation, 8 requests x 16384 scattered rows into contiguous ranges, one call
+        x = make_relocate_inputs(batch=8, prefix="fixed:16384", pool_slots=600_000, seed=11,
+                                 poison=False)
+        pool = torch.from_numpy(x.kv_pool.view(np.int16)).to(dev).view(torch.bfloat16)
+        r2t0 = torch.from_numpy(x.req_to_token).to(dev)
+        r2t = r2t0.clone()
+        rpi = torch.from_numpy(x.req_pool_indices).to(dev)
+        lens = torch.from_numpy(x.prefix_lens).to(dev)
+        dst = torch.from_numpy(x.dst_start).to(dev)
+        prog = torch.zeros(8, dtype=torch.int32, device=dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
 
-    # f4: fp8 indexer, 16 requests x 32768 positions (512 pages) over a 4097-entry table
-    ix = make_indexer_inputs(batch=16, num_heads=64, seq_lens="fixed:32768", max_pages=4097,
-                             seed=13)
-    q = torch.from_numpy(ix.q).to(dev)
-    w = torch.from_numpy(ix.weights).to(dev)
-    kv = torch.from_numpy(ix.kv_blocks).to(dev)
-    bt = torch.from_numpy(ix.block_table).to(dev)
-    sl = torch.from_numpy(ix.seq_lens).to(dev)
-    out = torch.empty(16, 4097 * 64, dtype=torch.float32, device=dev)
-    us = _time_us(lambda: mv.mla_fp8_indexer_logits(q, w, kv, bt, sl, out, st), flush)
-    pages = int(((ix.seq_lens + 63) // 64).sum())
-    nbytes = pages * 8448 + q.numel() + w.numel() * 4 + out.numel() * 4 + bt.numel() * 4
-    flops = 2 * int(ix.seq_lens.sum()) * 64 * 128
-    t_mem = nbytes / hbm * 1e6
-    t_flop = flops / (peaks["bf16_tflops"] * 2 * 1e12) * 1e6   # fp8 tensor rate = 2 x bf16
-    roof = max(t_mem, t_flop)
-    res["fp8_indexer"] = {"workload": "16 x 32768 positions, H=64, 4097-page table",
-                          "us": round(us, 2), "roofline_us": round(roof, 2),
-                          "frac": round(roof / us, 4), "bound": "hbm" if t_mem >= t_flop else "tensor",
-                          "gflops": round(flops / (us * 1e-6) / 1e9, 1),
-                          "status_ok": int(st.item()) == 0}
-    del kv, out
+        def reloc():
+            r2t.copy_(r2t0)
+            prog.zero_()
+            mv.mla_kv_relocate(pool, r2t, rpi, lens, dst, prog, 16384, st)
+        t_copy = _time_us(lambda: (r2t.copy_(r2t0), prog.zero_()), flush)
+        us = _time_us(reloc, flush) - t_copy
+        rows = 8 * 16384
+        nbytes = rows * (2 * 1152 + 8)
+        res["kv_relocate"] = {"workload": "8 x 16384 scattered rows, one call", "us": round(us, 2),
+                              "gbps": round(nbytes / (us * 1e-6) / 1e9, 1),
+                              "roofline_us": round(nbytes / hbm * 1e6, 2),
+                              "frac": round(nbytes / hbm * 1e6 / us, 4), "bound": "hbm",
+                              "status_ok": int(st.item()) == 0}
+        del pool
+
+    if "tree_accept" in which:
+        # f3: greedy acceptance, 64 requests x 64-node trees
+        a = make_accept_inputs(batch=64, T=64, seed=12)
+        tens = [torch.from_numpy(v).to(dev) for v in (a.tree_parent, a.draft_tokens, a.target_argmax,
+                                                      a.out_cache_loc)]
+        outs = [torch.zeros(64, dtype=torch.int32, device=dev)] + \
+            [torch.zeros(64, 64, dtype=torch.int32, device=dev) for _ in range(3)]
+        us = _time_us(lambda: mv.mla_tree_accept(*tens, *outs, st), flush)
+        res["tree_accept"] = {"workload": "64 requests x 64-node trees", "us": round(us, 2),
+                              "bound": "latency"}
+
+    if "fp8_indexer" in which:
+        # f4: fp8 indexer, 16 requests x 32768 positions (512 pages) over a 4097-entry table
+        ix = make_indexer_inputs(batch=16, num_heads=64, seq_lens="fixed:32768", max_pages=4097,
+                                 seed=13)
+        q = torch.from_numpy(ix.q).to(dev)
+        w = torch.from_numpy(ix.weights).to(dev)
+        kv = torch.from_numpy(ix.kv_blocks).to(dev)
+        bt = torch.from_numpy(ix.block_table).to(dev)
+        sl = torch.from_numpy(ix.seq_lens).to(dev)
+        out = torch.empty(16, 4097 * 64, dtype=torch.float32, device=dev)
+        us = _time_us(lambda: mv.mla_fp8_indexer_logits(q, w, kv, bt, sl, out, st), flush)
+        pages = int(((ix.seq_lens + 63) // 64).sum())
+        nbytes = pages * 8448 + q.numel() + w.numel() * 4 + out.numel() * 4 + bt.numel() * 4
+        flops = 2 * int(ix.seq_lens.sum()) * 64 * 128
+        t_mem = nbytes / hbm * 1e6
+        t_flop = flops / (peaks["bf16_tflops"] * 2 * 1e12) * 1e6   # fp8 tensor rate = 2 x bf16
+        roof = max(t_mem, t_flop)
+        res["fp8_indexer"] = {"workload": "16 x 32768 positions, H=64, 4097-page table",
+                              "us": round(us, 2), "roofline_us": round(roof, 2),
+                              "frac": round(roof / us, 4), "bound": "hbm" if t_mem >= t_flop else "tensor",
+                              "gflops": round(flops / (us * 1e-6) / 1e9, 1),
+                              "status_ok": int(st.item()) == 0}
+        del kv, out
     torch.cuda.empty_cache()
     return res
+
+
+def run_next_rows(which):
+    import torch
+
+    import mla_speculative_decoding_gb300 as mv
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    mv.mla_verify_init(0)
+    peaks, _ = load_peaks()
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20))
+    flush = L2Flush(l2, dev)
+    print(json.dumps(measure_next_rows(mv, dev, flush, peaks, which)), flush=True)
 
 
 # ----------------------------------------------------------------- reference arm
@@ -580,11 +620,15 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------- building-block probes
-def run_probes():
-    """Microbenchmarks of the building blocks the partial kernels rely on
-    (test-only library libmlaselftest.so): 2-SM MMA issue rate, scattered-row
-    gather throughput, mbarrier operation costs and producer/consumer
-    hand-over. Prints one table; not part of the bench contract."""
+PROBES = ("mma", "gather", "blocks", "mbar")
+
+
+def run_probes(which=PROBES):
+    """Microbenchmarks of the building blocks the kernels rely on (test-only
+    library libmlaselftest.so): 2-SM MMA issue rate, scattered-row gather
+    throughput, contiguous 8 KB block streams by copy method, mbarrier
+    operation costs and producer/consumer hand-over. Prints one table; not
+    part of the bench contract."""
     import ctypes
     import torch
     from mla_speculative_decoding_gb300 import build as mbuild
@@ -594,6 +638,19 @@ def run_probes():
     cyc = torch.zeros(1, dtype=torch.int64, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
 
+    if "mma" in which:
+        _probe_mma(lib, cyc, err)
+    if "gather" in which:
+        _probe_gather(lib, err)
+    if "blocks" in which:
+        _probe_blocks(lib, err)
+    if "mbar" in which:
+        _probe_mbar(lib, cyc, err)
+
+
+def _probe_mma(lib, cyc, err):
+    import ctypes
+    import torch
     # 2-SM MMA (M = 256, K = 16), single accumulator chain, tight issue loop.
     f = lib.mlav_pair_probe
     f.restype = ctypes.c_int
@@ -615,6 +672,11 @@ def run_probes():
             row.append(int(cyc.item()) / (4 * 256))
         print(f"  N={N:3d} {label:20s}: plain {row[0]:6.1f}   with per-4-MMA barrier test, fences, commit {row[1]:6.1f}")
 
+
+
+def _probe_gather(lib, err):
+    import ctypes
+    import torch
     # Scattered 128-byte row segments into shared memory, all SMs.
     f = lib.mlav_gather_rate
     f.restype = ctypes.c_int
@@ -639,6 +701,52 @@ def run_probes():
             parts.append(f"{name} {8 * 9 * 256 * 128 / c:5.1f}")
         print(f"  {label}: " + "; ".join(parts))
 
+    del kv
+    torch.cuda.empty_cache()
+
+
+def _probe_blocks(lib, err):
+    import ctypes
+    import torch
+    # Contiguous 8 KB blocks (the fp8 indexer cache) into a swizzled ring, all SMs.
+    f = lib.mlav_block_rate
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p] + [ctypes.c_int] * 4 + \
+        [ctypes.c_void_p] * 2
+    nblk = 120_000                      # ~1 GB pool
+    kv = torch.zeros(nblk * 8448, dtype=torch.uint8, device="cuda")
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    cyc_sm = torch.zeros(nsm, dtype=torch.int64, device="cuda")
+    ntile = 512
+    rng = np.random.default_rng(1)
+    blocks = torch.from_numpy(rng.integers(0, nblk, size=nsm * ntile * 2).astype(np.int32)).cuda()
+    print("8 KB blocks: bytes per clock per SM (and GB/s over all SMs), 2 blocks per 16 KB stage, "
+          "8-stage ring, all SMs")
+    for method, nw, label in ((0, 1, "TMA 3-D boxes"), (2, 1, "1-D bulk copies"),
+                              (1, 4, "cp.async x4 warps"), (1, 8, "cp.async x8 warps"),
+                              (3, 4, "TMA + cp.async x4 (half each)"),
+                              (3, 8, "TMA + cp.async x8 (half each)"),
+                              (4, 4, "ld.global x4 warps"), (4, 8, "ld.global x8 warps"),
+                              (5, 1, "TMA boxes + 256 B bulk scales"),
+                              (6, 1, "TMA boxes + 256 B TMA scale boxes")):
+        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        for rep in range(2):
+            ev[0].record()
+            rc = f(kv.data_ptr(), nblk, blocks.data_ptr(), nsm, ntile, method, nw, cyc_sm.data_ptr(),
+                   err.data_ptr())
+            ev[1].record()
+        assert rc == 0 and int(err.item()) == 0
+        torch.cuda.synchronize()
+        c = cyc_sm.float().mean().item()
+        gbs = nsm * ntile * 16384 / (ev[0].elapsed_time(ev[1]) * 1e-3) / 1e9
+        print(f"  {label:34s} {ntile * 16384 / c:6.1f} B/clk   {gbs:7.0f} GB/s")
+    del kv
+    torch.cuda.empty_cache()
+
+
+def _probe_mbar(lib, cyc, err):
+    import ctypes
+    import torch
     # mbarrier operations (one thread) and a producer/consumer ring.
     f = lib.mlav_mbar_cost
     f.restype = ctypes.c_int
@@ -676,11 +784,18 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-step-s", type=float, default=4.0)
-    ap.add_argument("--probes", action="store_true",
-                    help="run the building-block microbenchmarks instead of the bench")
+    ap.add_argument("--probes", nargs="*", choices=PROBES, default=None,
+                    help="run these building-block microbenchmarks (all if none named) "
+                         "instead of the bench")
+    ap.add_argument("--next-rows", nargs="*", choices=NEXT_ROWS, default=None,
+                    help="time only these steps beside the verify attention (all if none named) "
+                         "and print their JSON instead of the bench line")
     args = ap.parse_args()
-    if args.probes:
-        run_probes()
+    if args.probes is not None:
+        run_probes(args.probes or PROBES)
+        return
+    if args.next_rows is not None:
+        run_next_rows(args.next_rows or NEXT_ROWS)
         return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -8,7 +8,8 @@
 //   D[position][head] = sum_d k[position][d] * q[head][d]
 // with M = 128 positions (TMEM lane = position), N = heads rounded up to 16,
 // K = 128 (four MMAs of K = 32); the epilogue thread of each lane then forms
-// scale * sum_h w[h] * max(0, D[h]) in a fixed head order. Nothing is
+// scale * sum_h w[h] * max(0, D[h]) in a fixed order (four interleaved
+// partial sums over the heads, then added pairwise). Nothing is
 // reshaped to reach the tensor cores: the indexer's dot products are the
 // contraction, and the kernel stays bound by the cache stream from HBM.
 //
@@ -48,7 +49,8 @@ struct alignas(1024) IxSmem {
     uint8_t a[kIxStages][kIxTile];         // A: page 0 in rows 0-63, page 1 in rows 64-127
     uint8_t bq[2][128 * 128];              // B: query rows, rows >= H zero
     float scale[kIxStages][128];
-    int4 meta[kIxStages];                  // request, tile, good-page mask, length
+    int4 tinfo[64];                        // tile k % 64: request, tile, good-page mask, length
+    int2 tblk[64];                         // tile k % 64: the two pages' blocks
     int2 win[2][33];                       // producer's tile window (request, tile)
     uint64_t full[kIxStages], empty[kIxStages], bfull[2], bempty[2];
     uint64_t accfull[kIxAcc], accempty[kIxAcc], drain;
@@ -163,29 +165,60 @@ fp8_indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
 
     if (warp < kIxEpiWarps) {
         // ------------------------------------------------------------ epilogue
-        // -inf over [128 * tiles_b, 64 * P) of every request, in float4s.
+        // -inf over [128 * tiles_b, 64 * P) of every request, in float4s:
+        // each CTA walks a contiguous share of the output rows.
         {
             const int64_t per = (int64_t)P * 16;
             const int64_t total = (int64_t)batch * per;
-            const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            float4* o4 = reinterpret_cast<float4*>(out);
-            for (int64_t f = (int64_t)blockIdx.x * (kIxEpiWarps * 32) + tid; f < total;
-                 f += (int64_t)gridDim.x * (kIxEpiWarps * 32)) {
-                const int b = (int)(f / per);
-                const int j = (int)(f - (int64_t)b * per);
-                if (j >= 32 * ix_tiles(lens, b, P)) o4[f] = ninf;
+            const int64_t base = total / gridDim.x, rem = total % gridDim.x;
+            const int64_t f1 = (int64_t)blockIdx.x * base + min((int64_t)blockIdx.x, rem) + base +
+                               ((int64_t)blockIdx.x < rem ? 1 : 0);
+            int64_t f = f1 - base - ((int64_t)blockIdx.x < rem ? 1 : 0) + tid;
+            if (f < f1) {
+                const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                float4* o4 = reinterpret_cast<float4*>(out);
+                int b = (int)(f / per);
+                int64_t j = f - (int64_t)b * per;
+                int lim = 32 * ix_tiles(lens, b, P);
+                for (; f < f1; f += kIxEpiWarps * 32) {
+                    if (j >= lim) o4[f] = ninf;
+                    j += kIxEpiWarps * 32;
+                    while (j >= per) {
+                        j -= per;
+                        if (++b < batch) lim = 32 * ix_tiles(lens, b, P);
+                    }
+                }
             }
         }
         const int grp = warp >> 2, quarter = warp & 3;
         const int row = quarter * 32 + lane;              // TMEM lane = tile row
+        // Weights of the current request: up to 64 heads held whole in every
+        // thread (broadcast once per request), more lane-distributed (lane l:
+        // heads l, l + 32, ...) and broadcast per use.
+        constexpr bool kWholeW = NCH <= 2;
+        int wreq = -1;
+        float wl[NCH];
+        float wr[kWholeW ? 32 * NCH : 1];
         for (int k = grp; k < n; k += 2) {
             const int s = k % kIxStages, a = k % kIxAcc;
-            if (!mbar_wait(smem_u32(&S.full[s]), (k / kIxStages) & 1, abort)) break;
-            const int4 m = S.meta[s];
+            if (!mbar_wait_parked(smem_u32(&S.full[s]), (k / kIxStages) & 1, abort)) break;
+            const int4 m = S.tinfo[k & 63];
             const float sc = S.scale[s][row];
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&S.empty[s]));
-            if (!mbar_wait(smem_u32(&S.accfull[a]), (k / kIxAcc) & 1, abort)) break;
+            if (m.x != wreq) {                            // new request: its weights, one load per lane
+                wreq = m.x;
+#pragma unroll
+                for (int c = 0; c < NCH; ++c)
+                    wl[c] = 32 * c + lane < H ? __ldg(w + (int64_t)m.x * H + 32 * c + lane) : 0.f;
+                if constexpr (kWholeW) {
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c)
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) wr[32 * c + j] = __shfl_sync(0xffffffffu, wl[c], j);
+                }
+            }
+            if (!mbar_wait_parked(smem_u32(&S.accfull[a]), (k / kIxAcc) & 1, abort)) break;
             tc_fence_after();
             uint32_t d[NCH][32];
             const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(a * kCols);
@@ -197,16 +230,20 @@ fp8_indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&S.accempty[a]));
-            const float* wb = w + (int64_t)m.x * H;
-            float acc = 0.f;
+            // four partial sums over heads h = 4i + r, added at the end
+            float acc4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < NCH; ++c) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const int h = 32 * c + j;
-                    if (h < H) acc = fmaf(__ldg(wb + h), fmaxf(__uint_as_float(d[c][j]), 0.f), acc);
+                    float wh;
+                    if constexpr (kWholeW) wh = wr[32 * c + j];
+                    else wh = __shfl_sync(0xffffffffu, wl[c], j);
+                    if (32 * c + j < H)
+                        acc4[j & 3] = fmaf(wh, fmaxf(__uint_as_float(d[c][j]), 0.f), acc4[j & 3]);
                 }
             }
+            const float acc = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
             const int pos = 128 * m.y + row;
             if (pos < 64 * P) {
                 const bool ok = pos < m.w && ((m.z >> (row >> 6)) & 1);
@@ -258,42 +295,51 @@ fp8_indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
             const int2 nx = win[cnt];
             wb = nx.x;
             wt = nx.y;
-            for (int i = 0; i < cnt; ++i, ++k) {
-                const int b = __shfl_sync(0xffffffffu, tb, i), t = __shfl_sync(0xffffffffu, tt, i);
-                const int ln = __shfl_sync(0xffffffffu, len, i), mk = __shfl_sync(0xffffffffu, mask, i);
-                const int k0b = __shfl_sync(0xffffffffu, blk0, i), k1b = __shfl_sync(0xffffffffu, blk1, i);
-                if (lane == 0) {
-                    if (b != cur_b) {
+            // The window's tile table, read by lane 0 below and by the MMA and
+            // epilogue roles once the tile's stage is full. Entry k % 64 is
+            // rewritten two windows later, after tile k + 32 was issued; that
+            // needed tile k + 24's stage back (its MMA done), and that MMA
+            // needed the accumulator of tile k + 20 released by the epilogue
+            // group of tile k (same parity, in order): every reader is done.
+            if (lane < cnt) {
+                S.tinfo[(k0 + lane) & 63] = make_int4(tb, tt, mask, len);
+                S.tblk[(k0 + lane) & 63] = make_int2(blk0, blk1);
+            }
+            __syncwarp();
+            if (lane == 0) {
+                for (int i = 0; i < cnt; ++i, ++k) {
+                    const int4 ti = S.tinfo[k & 63];
+                    const int2 tk = S.tblk[k & 63];
+                    if (ti.x != cur_b) {
                         const int jb = nb & 1;
-                        if (nb >= 2 && !mbar_wait(smem_u32(&S.bempty[jb]), ((nb >> 1) - 1) & 1, abort))
+                        if (nb >= 2 && !mbar_wait(smem_u32(&S.bempty[jb]), ((nb >> 1) - 1) & 1, abort)) {
                             ok = false;
-                        if (ok) {
-                            mbar_arrive_expect_tx(smem_u32(&S.bfull[jb]), (uint32_t)H * 128);
-                            tma_load_3d(smem_u32(S.bq[jb]), &qmap, 0, 0, b, smem_u32(&S.bfull[jb]));
-                            cur_b = b;
-                            ++nb;
+                            break;
                         }
+                        mbar_arrive_expect_tx(smem_u32(&S.bfull[jb]), (uint32_t)H * 128);
+                        tma_load_3d(smem_u32(S.bq[jb]), &qmap, 0, 0, ti.x, smem_u32(&S.bfull[jb]));
+                        cur_b = ti.x;
+                        ++nb;
                     }
                     const int s = k % kIxStages, lap = k / kIxStages;
-                    if (ok && lap >= 1 && !mbar_wait(smem_u32(&S.empty[s]), (lap - 1) & 1, abort))
+                    if (lap >= 1 && !mbar_wait(smem_u32(&S.empty[s]), (lap - 1) & 1, abort)) {
                         ok = false;
-                    if (ok) {
-                        S.meta[s] = make_int4(b, t, mk, ln);
-                        const uint32_t fb = smem_u32(&S.full[s]);
-                        mbar_arrive_expect_tx(fb, (uint32_t)__popc(mk) * (kIxPage + 256));
-                        if (mk & 1) {
-                            tma_load_3d(smem_u32(S.a[s]), &kmap, 0, 0, k0b, fb);
-                            bulk_load_g2s(smem_u32(S.scale[s]), kv + (int64_t)k0b * kIxBlock + kIxPage, 256, fb);
-                        }
-                        if (mk & 2) {
-                            tma_load_3d(smem_u32(S.a[s] + kIxPage), &kmap, 0, 0, k1b, fb);
-                            bulk_load_g2s(smem_u32(S.scale[s] + 64), kv + (int64_t)k1b * kIxBlock + kIxPage, 256, fb);
-                        }
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&S.full[s]);
+                    mbar_arrive_expect_tx(fb, (uint32_t)__popc(ti.z) * (kIxPage + 256));
+                    if (ti.z & 1) {
+                        tma_load_3d(smem_u32(S.a[s]), &kmap, 0, 0, tk.x, fb);
+                        bulk_load_g2s(smem_u32(S.scale[s]), kv + (int64_t)tk.x * kIxBlock + kIxPage, 256, fb);
+                    }
+                    if (ti.z & 2) {
+                        tma_load_3d(smem_u32(S.a[s] + kIxPage), &kmap, 0, 0, tk.y, fb);
+                        bulk_load_g2s(smem_u32(S.scale[s] + 64), kv + (int64_t)tk.y * kIxBlock + kIxPage, 256, fb);
                     }
                 }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
             }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            __syncwarp();
         }
         bad = __reduce_or_sync(0xffffffffu, bad);
         if (lane == 0) {
@@ -317,16 +363,16 @@ fp8_indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
         int cur_b = -1, nb = 0, jb = 0;
         for (int k = 0; k < n; ++k) {
             const int s = k % kIxStages, a = k % kIxAcc;
-            if (!mbar_wait_spin(smem_u32(&S.full[s]), (k / kIxStages) & 1, abort)) break;
-            const int b = S.meta[s].x;
+            if (!mbar_wait(smem_u32(&S.full[s]), (k / kIxStages) & 1, abort)) break;
+            const int b = S.tinfo[k & 63].x;
             if (b != cur_b) {
                 if (nb >= 1) mma_commit(smem_u32(&S.bempty[(nb - 1) & 1]));
                 jb = nb & 1;
-                if (!mbar_wait_spin(smem_u32(&S.bfull[jb]), (nb >> 1) & 1, abort)) break;
+                if (!mbar_wait(smem_u32(&S.bfull[jb]), (nb >> 1) & 1, abort)) break;
                 cur_b = b;
                 ++nb;
             }
-            if (k >= kIxAcc && !mbar_wait_spin(smem_u32(&S.accempty[a]), ((k / kIxAcc) - 1) & 1, abort))
+            if (k >= kIxAcc && !mbar_wait(smem_u32(&S.accempty[a]), ((k / kIxAcc) - 1) & 1, abort))
                 break;
             tc_fence_after();
             const uint64_t ad = adesc0 + (uint64_t)s * kStageStep;

@@ -812,3 +812,169 @@ extern "C" __attribute__((visibility("default"))) int mlav_mbar_cost(int op, int
     if (e != cudaSuccess) return (int)e;
     return (int)cudaDeviceSynchronize();
 }
+
+namespace {
+
+// Block-stream probe: every CTA streams `ntile` stages of two random 8 KB
+// blocks of an fp8 indexer cache ([nblk][8448] bytes: 64 rows of 128 bytes,
+// then 256 scale bytes) through an 8-stage ring of 16 KB stages in the
+// 128-byte-swizzled layout; a consumer thread releases each stage as soon as
+// it lands. The CTA's block indices are staged in shared memory first, so
+// only the copies are timed. Methods:
+//   0: two TMA 3-D boxes (64 rows x 128 bytes) per stage, one issuing thread
+//   1: cp.async 16-byte pieces by `nw` warps (all warps share every stage)
+//   2: two 1-D bulk copies of 8 KB per stage (unswizzled), one issuing thread
+//   3: TMA box for the first block, cp.async by `nw` warps for the second
+//   4: ld.global 16-byte loads into registers, then st.shared, `nw` warps
+//      (warp w owns stages u = w mod nw, a whole stage per warp)
+//   5: as 0, plus each block's 256 scale bytes by a 1-D bulk copy
+//   6: as 0, plus each block's 256 scale bytes by a TMA box of an
+//      unswizzled map (rows 64-65 of the block viewed as 66 rows of 128 bytes)
+constexpr int kBStages = 8;
+constexpr int kBMaxIdx = 2048;
+struct __align__(1024) BlockSmem {
+    unsigned char ring[kBStages][16384];
+    unsigned char scale[kBStages][512];
+    int32_t idx[kBMaxIdx];
+    uint64_t full[kBStages], empty[kBStages];
+    int abort_flag;
+};
+
+__global__ void __launch_bounds__(512, 1)
+block_rate_kernel(const __grid_constant__ CUtensorMap map, const __grid_constant__ CUtensorMap smap,
+                  const unsigned char* kv,
+                  const int32_t* blocks, int ntile, int method, int nw, long long* cycles,
+                  int* err) {
+    extern __shared__ __align__(1024) unsigned char raw[];
+    unsigned char* base = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+    BlockSmem& g = *reinterpret_cast<BlockSmem*>(base);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool cp_side = method == 1 || method == 3;
+    if (tid == 0) {
+        const uint32_t cnt = method == 0 || method == 2 || method >= 5 ? 1u
+                             : method == 1          ? 32u * nw
+                             : method == 3          ? 1u + 32u * nw
+                                                    : 1u;
+        for (int i = 0; i < kBStages; ++i) {
+            mbar_init(smem_u32(&g.full[i]), cnt);
+            mbar_init(smem_u32(&g.empty[i]), 1);
+        }
+        g.abort_flag = 0;
+        fence_mbar_init();
+    }
+    for (int i = tid; i < 2 * ntile; i += 512) g.idx[i] = blocks[(size_t)blockIdx.x * ntile * 2 + i];
+    __syncthreads();
+    const long long t0 = clock64();
+    if (warp == 14 && (method == 0 || method == 2 || method == 3 || method >= 5)) {
+        if (lane == 0) {
+            for (int u = 0; u < ntile; ++u) {
+                const int st = u % kBStages;
+                if (u >= kBStages &&
+                    !mbar_wait(smem_u32(&g.empty[st]), ((u / kBStages) - 1) & 1, &g.abort_flag)) {
+                    atomicExch(err, 1);
+                    break;
+                }
+                const uint32_t fb = smem_u32(&g.full[st]), dst = smem_u32(g.ring[st]);
+                const int b0 = g.idx[2 * u], b1 = g.idx[2 * u + 1];
+                if (method == 0) {
+                    mbar_arrive_expect_tx(fb, 16384);
+                    tma_load_3d(dst, &map, 0, 0, b0, fb);
+                    tma_load_3d(dst + 8192, &map, 0, 0, b1, fb);
+                } else if (method >= 5) {
+                    const uint32_t sd = smem_u32(g.scale[st]);
+                    mbar_arrive_expect_tx(fb, 16384 + 512);
+                    tma_load_3d(dst, &map, 0, 0, b0, fb);
+                    if (method == 5)
+                        bulk_load_g2s(sd, kv + (int64_t)b0 * 8448 + 8192, 256, fb);
+                    else
+                        tma_load_3d(sd, &smap, 0, 64, b0, fb);
+                    tma_load_3d(dst + 8192, &map, 0, 0, b1, fb);
+                    if (method == 5)
+                        bulk_load_g2s(sd + 256, kv + (int64_t)b1 * 8448 + 8192, 256, fb);
+                    else
+                        tma_load_3d(sd + 256, &smap, 0, 64, b1, fb);
+                } else if (method == 2) {
+                    mbar_arrive_expect_tx(fb, 16384);
+                    bulk_load_g2s(dst, kv + (int64_t)b0 * 8448, 8192, fb);
+                    bulk_load_g2s(dst + 8192, kv + (int64_t)b1 * 8448, 8192, fb);
+                } else {
+                    mbar_arrive_expect_tx(fb, 8192);
+                    tma_load_3d(dst, &map, 0, 0, b0, fb);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (cp_side && warp < nw) {
+        const int first = method == 3 ? 1 : 0;
+        for (int u = 0; u < ntile; ++u) {
+            const int st = u % kBStages;
+            if (u >= kBStages &&
+                !mbar_wait(smem_u32(&g.empty[st]), ((u / kBStages) - 1) & 1, &g.abort_flag)) {
+                atomicExch(err, 1);
+                break;
+            }
+            const uint32_t dst = smem_u32(g.ring[st]);
+            for (int i = first * 512 + warp * 32 + lane; i < 1024; i += 32 * nw) {
+                const int j = i >> 9, r = (i >> 3) & 63, c = i & 7;
+                cp_async_16_zfill_nc(dst + j * 8192 + sw128_offset(r, c),
+                                     kv + (int64_t)g.idx[2 * u + j] * 8448 + r * 128 + c * 16, true);
+            }
+            cp_async_mbar_arrive_noinc(smem_u32(&g.full[st]));
+        }
+        cp_async_wait_all();
+    } else if (method == 4 && warp < nw) {
+        for (int u = warp; u < ntile; u += nw) {
+            const int st = u % kBStages;
+            if (u >= kBStages &&
+                !mbar_wait(smem_u32(&g.empty[st]), ((u / kBStages) - 1) & 1, &g.abort_flag)) {
+                atomicExch(err, 1);
+                break;
+            }
+            uint4 v[32];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                const int i = q * 32 + lane, j = i >> 9, r = (i >> 3) & 63, c = i & 7;
+                v[q] = __ldg(reinterpret_cast<const uint4*>(kv + (int64_t)g.idx[2 * u + j] * 8448 +
+                                                            r * 128 + c * 16));
+            }
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                const int i = q * 32 + lane, j = i >> 9, r = (i >> 3) & 63, c = i & 7;
+                *reinterpret_cast<uint4*>(g.ring[st] + j * 8192 + sw128_offset(r, c)) = v[q];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&g.full[st]));
+        }
+    } else if (warp == 15 && lane == 0) {
+        for (int u = 0; u < ntile; ++u) {
+            const int st = u % kBStages;
+            if (!mbar_wait(smem_u32(&g.full[st]), (u / kBStages) & 1, &g.abort_flag)) {
+                atomicExch(err, 1);
+                break;
+            }
+            mbar_arrive(smem_u32(&g.empty[st]));
+        }
+        cycles[blockIdx.x] = clock64() - t0;
+    }
+    __syncthreads();
+}
+
+}  // namespace
+
+extern "C" __attribute__((visibility("default"))) int mlav_block_rate(
+    const void* kv, long long nblk, const int32_t* blocks, int nctas, int ntile, int method, int nw,
+    long long* cycles, int* err) {
+    CUtensorMap map, smap;
+    if (!mlav::make_fp8_block_map(&map, kv, nblk) || !mlav::make_fp8_scale_map(&smap, kv, nblk))
+        return -2;
+    if (method < 0 || method > 6 || ntile < 1 || 2 * ntile > kBMaxIdx || nctas < 1) return -1;
+    if ((method == 1 || method == 3 || method == 4) && (nw < 1 || nw > 12)) return -1;
+    const int smem = (int)sizeof(BlockSmem) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(block_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return (int)e;
+    block_rate_kernel<<<nctas, 512, smem>>>(map, smap, static_cast<const unsigned char*>(kv), blocks, ntile,
+                                            method, nw, cycles, err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return (int)e;
+    return (int)cudaDeviceSynchronize();
+}

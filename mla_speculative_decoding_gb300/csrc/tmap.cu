@@ -54,6 +54,22 @@ bool make_fp8_block_map(CUtensorMap* map, const void* kv_blocks, int64_t nblocks
     return r == CUDA_SUCCESS;
 }
 
+bool make_fp8_scale_map(CUtensorMap* map, const void* kv_blocks, int64_t nblocks) {
+    std::call_once(g_once, load_entry);
+    if (g_encode == nullptr || nblocks > 0x7fffffffLL) return false;
+    // The same blocks viewed as [block][66 rows][128 bytes]: rows 64-65 hold
+    // the 64 fp32 scales; a box is those two rows, unswizzled (256 bytes).
+    const cuuint64_t dims[3] = {128, 66, (cuuint64_t)(nblocks > 0 ? nblocks : 1)};
+    const cuuint64_t strides[2] = {128, 8448};
+    const cuuint32_t box[3] = {128, 2, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(kv_blocks),
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool make_fp8_query_map(CUtensorMap* map, const void* q, int batch, int num_heads) {
     std::call_once(g_once, load_entry);
     if (g_encode == nullptr || batch < 1 || num_heads < 1 || num_heads > 256) return false;

@@ -16,6 +16,10 @@ bool make_kv_gather_map(CUtensorMap* map, const void* kv_pool, int64_t pool_slot
 // 128-byte swizzle. The 256 scale bytes of each block are not covered.
 bool make_fp8_block_map(CUtensorMap* map, const void* kv_blocks, int64_t nblocks);
 
+// The same cache viewed as [block][66 rows][128 bytes]: a box is rows 64-65,
+// the block's 64 fp32 scales (256 bytes), unswizzled.
+bool make_fp8_scale_map(CUtensorMap* map, const void* kv_blocks, int64_t nblocks);
+
 // 3-D map over fp8 queries [batch][num_heads][128] bytes: a box is one
 // request's num_heads rows, 128-byte swizzle.
 bool make_fp8_query_map(CUtensorMap* map, const void* q, int batch, int num_heads);
