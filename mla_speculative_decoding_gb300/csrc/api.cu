@@ -135,6 +135,7 @@ PartialArgs make_partial_args(const void* q, const void* kv_pool, const int32_t*
     a.nsplit = nsplit;
     a.pool_slots = pool_slots;
     a.scale_log2 = softmax_scale * kLog2e;
+    a.wave_full = 0x7fffffff;  // no wave shaping unless a launcher sets it
     return a;
 }
 

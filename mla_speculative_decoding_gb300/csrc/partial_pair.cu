@@ -135,7 +135,8 @@ partial_pair_kernel(const PartialArgs a) {
     int Lb, K;
     int bad = request_keys(a, b, Lb, K);
     int kb, ke;
-    split_range_tiles(K, a.nsplit, s, kNT, kb, ke);
+    const int nrb_req = (a.T * a.H + kM - 1) / kM;
+    split_range_waves(K, a.nsplit, s, kNT, b * a.nsplit * nrb_req + rb, nrb_req, a.wave_full, kb, ke);
     const int ntiles = (ke - kb + kNT - 1) / kNT;
     const int64_t kbase = a.kv_indptr[b];
 
@@ -666,16 +667,39 @@ partial_pair_kernel(const PartialArgs a) {
 
 }  // namespace
 
+// Resident 2-CTA clusters per device, for the wave shaping of the partitions.
+int g_pair_clusters[64];
+
 cudaError_t setup_partial_pair() {
-    return cudaFuncSetAttribute(partial_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(partial_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    int dev = -1;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, partial_pair_kernel, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();  // unknown: plain even partitions
+        n = 0;
+    }
+    g_pair_clusters[dev] = n;
+    return cudaSuccess;
 }
 
 cudaError_t launch_partial_pair(const PartialArgs& a, cudaStream_t stream) {
     const int rows_req = a.T * a.H;
     const int nrb = (rows_req + kM - 1) / kM;
     dim3 grid(2 * nrb, a.nsplit, a.batch);
-    partial_pair_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a);
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+    PartialArgs w = a;
+    w.wave_full = wave_full_items((long long)a.batch * a.nsplit * nrb,
+                                  dev >= 0 && dev < 64 ? g_pair_clusters[dev] : 0);
+    partial_pair_kernel<<<grid, kThreads, kSmemBytes, stream>>>(w);
     return cudaGetLastError();
 }
 

@@ -830,8 +830,15 @@ namespace {
 //   5: as 0, plus each block's 256 scale bytes by a 1-D bulk copy
 //   6: as 0, plus each block's 256 scale bytes by a TMA box of an
 //      unswizzled map (rows 64-65 of the block viewed as 66 rows of 128 bytes)
+//   7: latent-cache rows instead of blocks: each stage holds 14 whole rows
+//      of 1152 bytes from random slots of a [row_pool][1152-byte] pool,
+//      cp.async by `nw` warps (16128 bytes per stage)
+//   8: as 7 but one 128-byte segment (segment u mod 9) from each of 126
+//      random rows per stage (the same bytes per stage)
+// Methods 7 and 8 read their slots (126 per stage, 14 used by method 7) from
+// `blocks` [CTA][stage][126], staged in shared memory like the block indices.
 constexpr int kBStages = 8;
-constexpr int kBMaxIdx = 2048;
+constexpr int kBMaxIdx = 16384;
 struct __align__(1024) BlockSmem {
     unsigned char ring[kBStages][16384];
     unsigned char scale[kBStages][512];
@@ -843,16 +850,16 @@ struct __align__(1024) BlockSmem {
 __global__ void __launch_bounds__(512, 1)
 block_rate_kernel(const __grid_constant__ CUtensorMap map, const __grid_constant__ CUtensorMap smap,
                   const unsigned char* kv,
-                  const int32_t* blocks, int ntile, int method, int nw, long long* cycles,
-                  int* err) {
+                  const int32_t* blocks, int ntile, int method, int nw, long long row_pool,
+                  long long* cycles, int* err) {
     extern __shared__ __align__(1024) unsigned char raw[];
     unsigned char* base = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
     BlockSmem& g = *reinterpret_cast<BlockSmem*>(base);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool cp_side = method == 1 || method == 3;
+    const bool cp_side = method == 1 || method == 3 || method == 7 || method == 8;
     if (tid == 0) {
-        const uint32_t cnt = method == 0 || method == 2 || method >= 5 ? 1u
-                             : method == 1          ? 32u * nw
+        const uint32_t cnt = method == 0 || method == 2 || method == 5 || method == 6 ? 1u
+                             : method == 1 || method >= 7 ? 32u * nw
                              : method == 3          ? 1u + 32u * nw
                                                     : 1u;
         for (int i = 0; i < kBStages; ++i) {
@@ -862,10 +869,13 @@ block_rate_kernel(const __grid_constant__ CUtensorMap map, const __grid_constant
         g.abort_flag = 0;
         fence_mbar_init();
     }
-    for (int i = tid; i < 2 * ntile; i += 512) g.idx[i] = blocks[(size_t)blockIdx.x * ntile * 2 + i];
+    const int nidx = (method >= 7 ? 126 : 2) * ntile;
+    for (int i = tid; i < nidx; i += 512) g.idx[i] = blocks[(size_t)blockIdx.x * nidx + i];
     __syncthreads();
     const long long t0 = clock64();
-    if (warp == 14 && (method == 0 || method == 2 || method == 3 || method >= 5)) {
+    // TMA / bulk issuer: methods 0, 2, 3, 5, 6 only (7 and 8 are cp.async alone;
+    // an issuer arrival there would exceed the barrier's expected count)
+    if (warp == 14 && (method == 0 || method == 2 || method == 3 || method == 5 || method == 6)) {
         if (lane == 0) {
             for (int u = 0; u < ntile; ++u) {
                 const int st = u % kBStages;
@@ -914,6 +924,18 @@ block_rate_kernel(const __grid_constant__ CUtensorMap map, const __grid_constant
                 break;
             }
             const uint32_t dst = smem_u32(g.ring[st]);
+            if (method >= 7) {
+                // 1008 pieces of 16 bytes: 14 rows x 72 (method 7) or 126 rows x 8 (method 8)
+                const int per = method == 7 ? 72 : 8;
+                for (int i = warp * 32 + lane; i < 1008; i += 32 * nw) {
+                    const int r = i / per, c = i - r * per;
+                    const int64_t slot = g.idx[u * 126 + r];
+                    const int seg = method == 7 ? c : (u % 9) * 8 + c;
+                    cp_async_16_zfill_nc(dst + i * 16, kv + slot * 1152 + seg * 16, true);
+                }
+                cp_async_mbar_arrive_noinc(smem_u32(&g.full[st]));
+                continue;
+            }
             for (int i = first * 512 + warp * 32 + lane; i < 1024; i += 32 * nw) {
                 const int j = i >> 9, r = (i >> 3) & 63, c = i & 7;
                 cp_async_16_zfill_nc(dst + j * 8192 + sw128_offset(r, c),
@@ -963,17 +985,21 @@ block_rate_kernel(const __grid_constant__ CUtensorMap map, const __grid_constant
 
 extern "C" __attribute__((visibility("default"))) int mlav_block_rate(
     const void* kv, long long nblk, const int32_t* blocks, int nctas, int ntile, int method, int nw,
-    long long* cycles, int* err) {
+    long long row_pool, long long* cycles, int* err) {
     CUtensorMap map, smap;
     if (!mlav::make_fp8_block_map(&map, kv, nblk) || !mlav::make_fp8_scale_map(&smap, kv, nblk))
         return -2;
-    if (method < 0 || method > 6 || ntile < 1 || 2 * ntile > kBMaxIdx || nctas < 1) return -1;
-    if ((method == 1 || method == 3 || method == 4) && (nw < 1 || nw > 12)) return -1;
+    if (method < 0 || method > 8 || ntile < 1 || (method >= 7 ? 126 : 2) * ntile > kBMaxIdx ||
+        nctas < 1)
+        return -1;
+    if ((method == 1 || method == 3 || method == 4 || method >= 7) && (nw < 1 || nw > 12)) return -1;
+    if (method >= 7 && (row_pool < 1 || row_pool * 1152 > nblk * 8448 || row_pool > 0xffffffffLL))
+        return -1;
     const int smem = (int)sizeof(BlockSmem) + 1024;
     cudaError_t e = cudaFuncSetAttribute(block_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return (int)e;
     block_rate_kernel<<<nctas, 512, smem>>>(map, smap, static_cast<const unsigned char*>(kv), blocks, ntile,
-                                            method, nw, cycles, err);
+                                            method, nw, row_pool, cycles, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;
     return (int)cudaDeviceSynchronize();
