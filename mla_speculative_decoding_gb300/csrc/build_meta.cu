@@ -54,6 +54,7 @@ build_meta_kernel(const int32_t* __restrict__ req_to_token, int64_t stride, int6
     __shared__ int32_t s_L;
     __shared__ int64_t s_warp[kThreads / 32];
     __shared__ uint64_t s_anc[MLA_MAX_TREE];
+    __shared__ int s_ptr[MLA_MAX_TREE];
     // Offset of this request's list: sum over earlier requests of (L_c + T),
     // with the same clamping those requests' own blocks apply (their errors
     // are reported by those blocks). Integer sum: exact in any order.
@@ -79,10 +80,6 @@ build_meta_kernel(const int32_t* __restrict__ req_to_token, int64_t stride, int6
             if (end > capacity) bad |= MLA_STATUS_CAPACITY;
             kv_indptr[b + 1] = (int32_t)min(end, capacity);
             if (b == 0) kv_indptr[0] = 0;
-            if (anc != nullptr) {
-                bad |= build_anc_serial(tree_parent + (int64_t)b * T, T, s_anc);
-                for (int t = 0; t < T; ++t) anc[(int64_t)b * T + t] = s_anc[t];
-            }
             status_or(status, bad);
         }
     }
@@ -97,6 +94,13 @@ build_meta_kernel(const int32_t* __restrict__ req_to_token, int64_t stride, int6
         const int64_t dst = base + j;
         if (dst >= capacity) break;
         kv_indices[dst] = (j < L) ? row[j] : tree_slots[j - L];
+    }
+    // The tree's ancestor-or-self sets, by the first warp of the request's
+    // first block once its share of the list is written.
+    if (anc != nullptr && blockIdx.y == 0 && threadIdx.x < 32) {
+        const int bad = build_anc_warp(tree_parent + (int64_t)b * T, T, s_anc, s_ptr);
+        for (int t = threadIdx.x; t < T; t += 32) anc[(int64_t)b * T + t] = s_anc[t];
+        if (threadIdx.x == 0) status_or(status, bad);
     }
 }
 

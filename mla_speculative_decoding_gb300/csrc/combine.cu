@@ -7,7 +7,7 @@
 // splits with lse_s = -inf weighing 0. Four warps per query row, one per
 // 128 output dims: lanes hold the split lse values (max and sum by warp
 // shuffles), then each lane streams its 4 dims of every split with 16-byte
-// loads (coalesced 512 bytes per warp and split, several splits in flight),
+// loads (coalesced 512 bytes per warp and split, sixteen splits in flight),
 // summing splits in index order (deterministic), and rounds to bf16
 // (nearest even).
 #include "common.cuh"
@@ -18,7 +18,7 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kParts = 4;                          // warps per row
 constexpr int kMaxPerLane = MLA_MAX_NSPLIT / 32;   // split lse values held per lane
-constexpr int kUnroll = 8;
+constexpr int kUnroll = 16;                        // splits in flight per lane
 
 __global__ void __launch_bounds__(kWarps * 32)
 combine_kernel(const float* __restrict__ lse_part, const float* __restrict__ o_part, int rows,

@@ -117,6 +117,54 @@ __device__ inline int build_anc_serial(const int32_t* par, int T, uint64_t* anc)
     return bad;
 }
 
+// The same sets built by one full warp by pointer jumping: each node t
+// starts from {t} and its parent as pointer; round r ORs in the set of the
+// node its pointer names and doubles the pointer's stride, so after six
+// rounds every set spans the whole root path (depth <= 63). An invalid parent
+// ends the path at the node itself, as in build_anc_serial. `ptr` is warp-
+// private shared scratch of MLA_MAX_TREE entries. Returns the status bits
+// (on every lane).
+__device__ inline int build_anc_warp(const int32_t* par, int T, uint64_t* anc, int* ptr) {
+    const int lane = threadIdx.x & 31;
+    int bad = 0;
+    for (int t = lane; t < MLA_MAX_TREE; t += 32) {
+        int p = -1;
+        if (t < T) {
+            p = par[t];
+            const bool ok = (t == 0) ? (p == -1) : (p >= 0 && p < t);
+            if (!ok) {
+                bad = MLA_STATUS_BAD_PARENT;
+                p = -1;
+            }
+        }
+        ptr[t] = p;
+        anc[t] = t < T ? (1ull << t) : 0ull;
+    }
+    __syncwarp();
+#pragma unroll 1
+    for (int r = 0; r < 6; ++r) {
+        uint64_t add[2] = {0ull, 0ull};
+        int nxt[2] = {-1, -1};
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int t = lane + 32 * u, q = ptr[t];
+            if (q >= 0) {
+                add[u] = anc[q];
+                nxt[u] = ptr[q];
+            }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int t = lane + 32 * u;
+            anc[t] |= add[u];
+            ptr[t] = nxt[u];
+        }
+        __syncwarp();
+    }
+    return __reduce_or_sync(0xffffffffu, bad);
+}
+
 struct PartialArgs;
 
 // Internal launchers (defined in the kernel translation units).
