@@ -420,12 +420,18 @@ partial_pair_kernel(const PartialArgs a) {
                         if (u >= 0 && !(u < T && ((anc_t >> u) & 1ull))) vw[c >> 5] &= ~(1u << (c & 31));
                     }
                 }
+                // Max over the raw scores (the scale is positive, so scaling
+                // the max is exact); masked keys become -inf only where this
+                // row's half-tile has any.
                 float mx = -INFINITY;
+                if ((vw[0] & vw[1] & vw[2] & vw[3]) != 0xffffffffu) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    sc[c] = ((vw[c >> 5] >> (c & 31)) & 1u) ? sc[c] * a.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, sc[c]);
+                    for (int c = 0; c < 128; ++c)
+                        if (!((vw[c >> 5] >> (c & 31)) & 1u)) sc[c] = -INFINITY;
                 }
+#pragma unroll
+                for (int c = 0; c < 128; ++c) mx = fmaxf(mx, sc[c]);
+                mx *= a.scale_log2;
                 S.mx[i & 1][half][r] = mx;
                 mbar_arrive(ba(S.mx_bar[i & 1]));
                 if (!warp_wait(S.mx_bar[i & 1], (i >> 1) & 1, abort_p)) {
@@ -448,7 +454,13 @@ partial_pair_kernel(const PartialArgs a) {
                     break;
                 }
                 // P (bf16) -> the O-CTA's A-operand tile, 8 keys (16 bytes) at a time.
+                // p = 2^(s * scale_log2 - m_ref) in one FMA per key; masked
+                // keys (-inf) give 2^-inf = 0; a row with no visible key yet
+                // (m_ref = -inf) writes zeros.
                 float psum = 0.f;
+                const float sl = a.scale_log2;
+                const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
+                const bool any = m_ref != -INFINITY;
 #pragma unroll
                 for (int blk = 0; blk < 2; ++blk) {
                     const uint32_t pb = p_peer + (2 * half + blk) * kPBlock;
@@ -458,8 +470,8 @@ partial_pair_kernel(const PartialArgs a) {
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
                             const int k = blk * 64 + c * 8 + 2 * u;
-                            const float p0 = sc[k] > -INFINITY ? ex2_approx(sc[k] - m_ref) : 0.f;
-                            const float p1 = sc[k + 1] > -INFINITY ? ex2_approx(sc[k + 1] - m_ref) : 0.f;
+                            const float p0 = any ? ex2_approx(fmaf(sc[k], sl, nm)) : 0.f;
+                            const float p1 = any ? ex2_approx(fmaf(sc[k + 1], sl, nm)) : 0.f;
                             psum += p0 + p1;
                             w[u] = pack_bf16x2(p0, p1);
                         }
