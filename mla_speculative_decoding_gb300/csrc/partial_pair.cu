@@ -429,8 +429,15 @@ partial_pair_kernel(const PartialArgs a) {
                     for (int c = 0; c < 128; ++c)
                         if (!((vw[c >> 5] >> (c & 31)) & 1u)) sc[c] = -INFINITY;
                 }
+                {  // eight independent chains, then a tree
+                    float m8[8];
 #pragma unroll
-                for (int c = 0; c < 128; ++c) mx = fmaxf(mx, sc[c]);
+                    for (int j = 0; j < 8; ++j) m8[j] = sc[j];
+#pragma unroll
+                    for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], sc[c]);
+                    mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                }
                 mx *= a.scale_log2;
                 S.mx[i & 1][half][r] = mx;
                 mbar_arrive(ba(S.mx_bar[i & 1]));
@@ -457,7 +464,7 @@ partial_pair_kernel(const PartialArgs a) {
                 // p = 2^(s * scale_log2 - m_ref) in one FMA per key; masked
                 // keys (-inf) give 2^-inf = 0; a row with no visible key yet
                 // (m_ref = -inf) writes zeros.
-                float psum = 0.f;
+                float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // eight chains
                 const float sl = a.scale_log2;
                 const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
                 const bool any = m_ref != -INFINITY;
@@ -472,13 +479,13 @@ partial_pair_kernel(const PartialArgs a) {
                             const int k = blk * 64 + c * 8 + 2 * u;
                             const float p0 = any ? ex2_approx(fmaf(sc[k], sl, nm)) : 0.f;
                             const float p1 = any ? ex2_approx(fmaf(sc[k + 1], sl, nm)) : 0.f;
-                            psum += p0 + p1;
+                            ps8[(c & 3) * 2 + (u & 1)] += p0 + p1;
                             w[u] = pack_bf16x2(p0, p1);
                         }
                         st_cluster_v4(pb + sw128_offset(r, c), w[0], w[1], w[2], w[3]);
                     }
                 }
-                l_part += psum;
+                l_part += ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
                 if (half == 0) st_cluster_f32(alpha_peer, alpha);
                 fence_proxy_async_all();
                 mbar_arrive_cluster(pfull_peer);
