@@ -712,14 +712,16 @@ def _probe_blocks(lib, err):
     f = lib.mlav_block_rate
     f.restype = ctypes.c_int
     f.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p] + [ctypes.c_int] * 4 + \
-        [ctypes.c_void_p] * 2
+        [ctypes.c_longlong] + [ctypes.c_void_p] * 2
     nblk = 120_000                      # ~1 GB pool
+    rows = nblk * 8448 // 1152          # the same bytes as latent-cache rows
     kv = torch.zeros(nblk * 8448, dtype=torch.uint8, device="cuda")
     nsm = torch.cuda.get_device_properties(0).multi_processor_count
     cyc_sm = torch.zeros(nsm, dtype=torch.int64, device="cuda")
     ntile = 512
     rng = np.random.default_rng(1)
     blocks = torch.from_numpy(rng.integers(0, nblk, size=nsm * ntile * 2).astype(np.int32)).cuda()
+    row_slots = torch.from_numpy(rng.integers(0, rows, size=nsm * 128 * 126).astype(np.int32)).cuda()
     print("8 KB blocks: bytes per clock per SM (and GB/s over all SMs), 2 blocks per 16 KB stage, "
           "8-stage ring, all SMs")
     for method, nw, label in ((0, 1, "TMA 3-D boxes"), (2, 1, "1-D bulk copies"),
@@ -728,18 +730,25 @@ def _probe_blocks(lib, err):
                               (3, 8, "TMA + cp.async x8 (half each)"),
                               (4, 4, "ld.global x4 warps"), (4, 8, "ld.global x8 warps"),
                               (5, 1, "TMA boxes + 256 B bulk scales"),
-                              (6, 1, "TMA boxes + 256 B TMA scale boxes")):
+                              (6, 1, "TMA boxes + 256 B TMA scale boxes"),
+                              (7, 8, "whole 1152 B rows, cp.async x8"),
+                              (7, 12, "whole 1152 B rows, cp.async x12"),
+                              (8, 8, "128 B of each row, cp.async x8"),
+                              (8, 12, "128 B of each row, cp.async x12")):
         ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        nt = ntile if method < 7 else 128
+        idx = blocks if method < 7 else row_slots
         for rep in range(2):
             ev[0].record()
-            rc = f(kv.data_ptr(), nblk, blocks.data_ptr(), nsm, ntile, method, nw, cyc_sm.data_ptr(),
-                   err.data_ptr())
+            rc = f(kv.data_ptr(), nblk, idx.data_ptr(), nsm, nt, method, nw, rows,
+                   cyc_sm.data_ptr(), err.data_ptr())
             ev[1].record()
         assert rc == 0 and int(err.item()) == 0
         torch.cuda.synchronize()
         c = cyc_sm.float().mean().item()
-        gbs = nsm * ntile * 16384 / (ev[0].elapsed_time(ev[1]) * 1e-3) / 1e9
-        print(f"  {label:34s} {ntile * 16384 / c:6.1f} B/clk   {gbs:7.0f} GB/s")
+        stage = 16128 if method >= 7 else 16384
+        gbs = nsm * nt * stage / (ev[0].elapsed_time(ev[1]) * 1e-3) / 1e9
+        print(f"  {label:34s} {nt * stage / c:6.1f} B/clk   {gbs:7.0f} GB/s")
     del kv
     torch.cuda.empty_cache()
 
