@@ -620,7 +620,7 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------- building-block probes
-PROBES = ("mma", "gather", "blocks", "mbar")
+PROBES = ("mma", "gather", "blocks", "dsmem", "mbar")
 
 
 def run_probes(which=PROBES):
@@ -644,6 +644,8 @@ def run_probes(which=PROBES):
         _probe_gather(lib, err)
     if "blocks" in which:
         _probe_blocks(lib, err)
+    if "dsmem" in which:
+        _probe_dsmem(lib, err)
     if "mbar" in which:
         _probe_mbar(lib, cyc, err)
 
@@ -751,6 +753,28 @@ def _probe_blocks(lib, err):
         print(f"  {label:34s} {nt * stage / c:6.1f} B/clk   {gbs:7.0f} GB/s")
     del kv
     torch.cuda.empty_cache()
+
+
+def _probe_dsmem(lib, err):
+    import ctypes
+    import torch
+    # Bulk copies from one CTA's shared memory into its cluster peer's, through
+    # a 4-slot ring released by remote arrives (2-CTA clusters).
+    f = lib.mlav_bulk_rate
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p] * 2
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    cyc = torch.zeros(nsm, dtype=torch.int64, device="cuda")
+    print("DSMEM bulk copy CTA -> peer: bytes per clock per sending SM")
+    for ncl in (1, nsm // 2):
+        parts = []
+        for chunk in (4096, 16384, 32768):
+            n = (64 << 20) // chunk // max(1, ncl) + 64
+            rc = f(ncl, chunk, n, cyc.data_ptr(), err.data_ptr())
+            assert rc == 0 and int(err.item()) == 0
+            c = cyc[:ncl].float().mean().item()
+            parts.append(f"{chunk // 1024} KB chunks {n * chunk / c:5.1f}")
+        print(f"  {ncl:3d} cluster(s): " + "; ".join(parts))
 
 
 def _probe_mbar(lib, cyc, err):

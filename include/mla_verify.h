@@ -203,7 +203,8 @@ int mla_verify_attention_anc(const void *q, const void *kv_pool, const int32_t *
  * (o_part). Exactly one of tree_parent / anc_mask must be non-NULL.
  * flags: 0 = default kernel (tensor cores: for requests with more than 128
  * rows T*H, four SMs per 256-row block with 2-SM MMAs; otherwise two SMs per
- * 128-row block); MLA_PARTIAL_PAIR forces the two-SM kernel;
+ * 128-row block); MLA_PARTIAL_PAIR forces the two-SM kernel,
+ * MLA_PARTIAL_QUAD the four-SM one (rows past T*H are padding);
  * MLA_PARTIAL_SIMT the CUDA-core kernel; MLA_PARTIAL_TC_QUARTER the
  * single-SM tensor-core kernel that splits the V dims over four CTAs. All
  * give results within the documented tolerance of each other.
@@ -215,6 +216,7 @@ int mla_verify_attention_anc(const void *q, const void *kv_pool, const int32_t *
 #define MLA_PARTIAL_SIMT 0x1u
 #define MLA_PARTIAL_TC_QUARTER 0x2u
 #define MLA_PARTIAL_PAIR 0x4u
+#define MLA_PARTIAL_QUAD 0x8u
 int mla_verify_partial(const void *q, const void *kv_pool, const int32_t *kv_indices,
                        const int32_t *kv_indptr, const int32_t *prefix_lens,
                        const int32_t *tree_parent, const uint64_t *anc_mask, int T, int nsplit,

@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     MLA_PARTIAL_SIMT,
     MLA_PARTIAL_TC_QUARTER,
     MLA_PARTIAL_PAIR,
+    MLA_PARTIAL_QUAD,
     MLA_STATUS_BAD_INDPTR,
     MLA_STATUS_BAD_PARENT,
     MLA_STATUS_BAD_PREFIX,

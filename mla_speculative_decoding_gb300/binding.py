@@ -35,6 +35,7 @@ MLA_STATUS_TIMEOUT = 0x40
 MLA_PARTIAL_SIMT = 0x1
 MLA_PARTIAL_TC_QUARTER = 0x2
 MLA_PARTIAL_PAIR = 0x4
+MLA_PARTIAL_QUAD = 0x8
 D_QK = 576
 D_V = 512
 

@@ -145,7 +145,7 @@ int run_partial(const PartialArgs& a, unsigned flags, int sm_count, cudaStream_t
         e = launch_partial_simt(a, stream);
     else if ((flags & MLA_PARTIAL_TC_QUARTER) && partial_tc_supported(a))
         e = launch_partial_tc(a, sm_count, stream);
-    else if ((flags & MLA_PARTIAL_PAIR) || a.T * a.H <= 128)
+    else if ((flags & MLA_PARTIAL_PAIR) || (!(flags & MLA_PARTIAL_QUAD) && a.T * a.H <= 128))
         e = launch_partial_pair(a, stream);
     else
         e = launch_partial_quad(a, stream);
@@ -277,7 +277,7 @@ MLAV_API int mla_verify_partial(const void* q, const void* kv_pool, const int32_
                                 anc_mask, T, nsplit, workspace, batch, num_heads, pool_slots,
                                 softmax_scale, workspace_bytes);
     if (rc != MLA_OK) return rc;
-    if (flags & ~(MLA_PARTIAL_SIMT | MLA_PARTIAL_TC_QUARTER | MLA_PARTIAL_PAIR))
+    if (flags & ~(MLA_PARTIAL_SIMT | MLA_PARTIAL_TC_QUARTER | MLA_PARTIAL_PAIR | MLA_PARTIAL_QUAD))
         return MLA_ERR_INVALID_ARG;
     int sms = 0;
     rc = ensure_ready(stream, &sms);

@@ -64,6 +64,7 @@ tree_accept_kernel(const int32_t* __restrict__ par, const int32_t* __restrict__ 
 constexpr int kRelocRowsPerCta = 64;
 constexpr int kRelocWarps = 8;
 constexpr int kRowVec = kDqk * 2 / 16;  // 72 sixteen-byte pieces per 1152-byte row
+constexpr int kRelocInFlight = 4;       // rows per warp whose loads are in flight together
 
 __global__ void __launch_bounds__(kRelocWarps * 32)
 kv_relocate_kernel(uint4* __restrict__ kv, int64_t pool_slots, int32_t* __restrict__ r2t,
@@ -80,26 +81,47 @@ kv_relocate_kernel(uint4* __restrict__ kv, int64_t pool_slots, int32_t* __restri
     int32_t* row = r2t + (int64_t)rpi[b] * stride;
     const int r_end = min(n, (int)(blockIdx.x + 1) * kRelocRowsPerCta);
     int bad = 0;
-    for (int r = blockIdx.x * kRelocRowsPerCta + warp; r < r_end; r += kRelocWarps) {
-        const int j = j0 + r;
-        const int64_t s = row[j], d = (int64_t)dst[b] + j;
-        if (s < 0 || s >= pool_slots || d < 0 || d >= pool_slots) {
-            bad = MLA_STATUS_BAD_SLOT;
-            continue;
+    // Each warp moves kRelocInFlight rows per step: all their loads are in
+    // flight before any of them is stored.
+    for (int r0 = blockIdx.x * kRelocRowsPerCta + warp; r0 < r_end;
+         r0 += kRelocInFlight * kRelocWarps) {
+        int64_t s[kRelocInFlight], d[kRelocInFlight];
+        bool mv[kRelocInFlight];
+#pragma unroll
+        for (int e = 0; e < kRelocInFlight; ++e) {
+            const int r = r0 + e * kRelocWarps;
+            mv[e] = false;
+            s[e] = d[e] = -1;
+            if (r < r_end) {
+                const int j = j0 + r;
+                s[e] = row[j];
+                d[e] = (int64_t)dst[b] + j;
+                if (s[e] < 0 || s[e] >= pool_slots || d[e] < 0 || d[e] >= pool_slots)
+                    bad = MLA_STATUS_BAD_SLOT;
+                else
+                    mv[e] = s[e] != d[e];
+            }
         }
-        if (s != d) {
-            const uint4* src = kv + s * kRowVec;
-            uint4* out = kv + d * kRowVec;
-            uint4 v[3];
+        uint4 v[kRelocInFlight][3];
+#pragma unroll
+        for (int e = 0; e < kRelocInFlight; ++e)
 #pragma unroll
             for (int u = 0; u < 3; ++u)
-                if (lane + 32 * u < kRowVec) v[u] = __ldg(src + lane + 32 * u);
+                if (mv[e] && lane + 32 * u < kRowVec) v[e][u] = __ldg(kv + s[e] * kRowVec + lane + 32 * u);
+#pragma unroll
+        for (int e = 0; e < kRelocInFlight; ++e)
 #pragma unroll
             for (int u = 0; u < 3; ++u)
-                if (lane + 32 * u < kRowVec) out[lane + 32 * u] = v[u];
-        }
+                if (mv[e] && lane + 32 * u < kRowVec) kv[d[e] * kRowVec + lane + 32 * u] = v[e][u];
         __syncwarp();
-        if (lane == 0) row[j] = (int32_t)d;
+        if (lane == 0) {
+#pragma unroll
+            for (int e = 0; e < kRelocInFlight; ++e) {
+                const int r = r0 + e * kRelocWarps;
+                if (r < r_end && s[e] >= 0 && s[e] < pool_slots && d[e] >= 0 && d[e] < pool_slots)
+                    row[j0 + r] = (int32_t)d[e];
+            }
+        }
     }
     if (lane == 0) status_or(status, bad);
 }

@@ -16,7 +16,8 @@ from tests.gpu_util import config_cached, compare, host_out, oracle_ref, run_gpu
 from workloads import make_config, make_inputs
 
 pytestmark = pytest.mark.gpu
-PATHS = [0, mv.MLA_PARTIAL_PAIR, mv.MLA_PARTIAL_SIMT, mv.MLA_PARTIAL_TC_QUARTER]
+PATHS = [0, mv.MLA_PARTIAL_PAIR, mv.MLA_PARTIAL_QUAD, mv.MLA_PARTIAL_SIMT,
+         mv.MLA_PARTIAL_TC_QUARTER]
 
 
 @pytest.mark.parametrize("flags", PATHS)
