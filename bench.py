@@ -419,6 +419,13 @@ def run_ours(args):
         per[idx] = {"us": round(value, 3), "roofline_us": round(roof_us, 3),
                     "frac": round(roof_us / value, 4), "bound": bound}
         result["per_config"] = {str(k): per[k] for k in sorted(per)}
+        # the mid workload once more with its keys in contiguous slots (the
+        # defragmented placement), to compare gather cost
+        try:
+            result["per_config"]["3c"] = measure_config(3, mv, dev, flush, peaks, args,
+                                                        placement="contiguous")
+        except Exception as e:
+            result["per_config"]["3c"] = {"error": repr(e)}
         try:
             result["next_rows"] = measure_next_rows(mv, dev, flush, peaks)
         except Exception as e:
@@ -436,9 +443,9 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def measure_config(j, mv, dev, flush, peaks, args, steps=10):
+def measure_config(j, mv, dev, flush, peaks, args, steps=10, placement="scattered"):
     import torch
-    inp = make_config(j)
+    inp = make_config(j, placement=placement)
     fig = workload_figures(inp)
     d = mv.to_device(inp, device=dev)
     stream = torch.cuda.current_stream()
