@@ -42,7 +42,8 @@ def _sources():
 
 
 def _deps():
-    return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [
+    return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + \
+        sorted(glob.glob(os.path.join(CSRC, "*.h"))) + [
         *sorted(glob.glob(os.path.join(INCLUDE, "*.h"))), os.path.abspath(__file__)]
 
 

@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "mla_verify.h"
+#include "partition.h"
 
 #define MLAV_API extern "C" __attribute__((visibility("default")))
 
@@ -36,68 +37,6 @@ __host__ __device__ inline WsLayout ws_layout(int batch, int T, int H, int nspli
     return w;
 }
 
-// Key range of split s of a request with K keys: contiguous ranges of
-// ceil(K / nsplit) keys; trailing splits may be empty.
-__host__ __device__ inline void split_range(int K, int nsplit, int s, int& beg, int& end) {
-    const int chunk = (K + nsplit - 1) / nsplit;
-    beg = min(K, s * chunk);
-    end = min(K, beg + chunk);
-}
-
-// Tile-aligned variant for kernels that walk the keys in tiles of `tile`:
-// the ceil(K / tile) tiles are spread as evenly as possible (the first
-// tiles % nsplit splits take one more), so no split carries a mostly empty
-// last tile and the longer work items come first in launch order.
-__host__ __device__ inline void split_range_tiles(int K, int nsplit, int s, int tile, int& beg,
-                                                  int& end) {
-    const int tiles = (K + tile - 1) / tile;
-    const int base = tiles / nsplit, rem = tiles % nsplit;
-    const int t0 = s * base + min(s, rem);
-    const int nt = base + (s < rem ? 1 : 0);
-    beg = min(K, t0 * tile);
-    end = min(K, (t0 + nt) * tile);
-}
-
-// Wave-shaped variant for launches whose work items run in waves of resident
-// clusters. Items are dispatched in the order (request, partition, row
-// block), row block fastest: the item of partition s is item0 + s * nrb.
-// Items at or past index `full` (the items of the last, partial wave) get one
-// tile each, and the partitions before them share the remaining tiles evenly
-// as in split_range_tiles, so that the full waves end together and the
-// partial wave is as short as possible. Every partition keeps at least one
-// tile. Falls back to split_range_tiles when nothing is in the partial wave,
-// when the whole row block is, or when there are fewer than 2 * nsplit tiles.
-__host__ __device__ inline void split_range_waves(int K, int nsplit, int s, int tile, int item0,
-                                                  int nrb, int full, int& beg, int& end) {
-    const int tiles = (K + tile - 1) / tile;
-    const int last = item0 + (nsplit - 1) * nrb;  // item of the last partition
-    const int s_tail = last < full ? nsplit : (full <= item0 ? 0 : (full - item0 + nrb - 1) / nrb);
-    const int n_tail = nsplit - s_tail;
-    if (n_tail == 0 || s_tail == 0 || tiles < 2 * nsplit) {
-        split_range_tiles(K, nsplit, s, tile, beg, end);
-        return;
-    }
-    const int head = tiles - n_tail;  // tiles of partitions [0, s_tail)
-    int t0, nt;
-    if (s < s_tail) {
-        const int base = head / s_tail, rem = head % s_tail;
-        t0 = s * base + min(s, rem);
-        nt = base + (s < rem ? 1 : 0);
-    } else {
-        t0 = head + (s - s_tail);
-        nt = 1;
-    }
-    beg = min(K, t0 * tile);
-    end = min(K, (t0 + nt) * tile);
-}
-
-// Index of the first item of the last, partial wave when `items` work items
-// run on `resident` clusters at a time (items when every wave is full or
-// when there is no more than one wave, or the resident count is unknown).
-__host__ inline int wave_full_items(long long items, int resident) {
-    if (resident <= 0 || items <= resident) return (int)items;
-    return (int)((items / resident) * resident);
-}
 
 __device__ __forceinline__ void status_or(int32_t* st, int bits) {
     if (st != nullptr && bits != 0) atomicOr(st, bits);
