@@ -60,7 +60,6 @@ constexpr int kVStages = 4;
 constexpr uint32_t kVBlock = kVKeys * 128;     // 32 keys x 64 dims
 constexpr uint32_t kVStage = 8 * kVBlock;      // 32 keys x 512 dims
 constexpr uint32_t kPBlock = kM * 128;         // 128 rows x 64 keys (bf16)
-constexpr uint32_t kQStageStride = 1040;       // padded staging row of 512 bf16
 constexpr uint32_t kColQ = 0, kColS = 256;     // S-CTA TMEM map
 constexpr float kRescaleLog2 = 8.0f;
 
@@ -106,7 +105,6 @@ struct __align__(1024) SmemPair {
 
 constexpr size_t kSmemBytes = sizeof(SmemPair) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kM * kQStageStride <= kKStages * kKBlock, "Q staging must fit in the K ring");
 
 __device__ __forceinline__ uint32_t ba(const uint64_t& b) { return smem_u32(&b); }
 
@@ -218,7 +216,7 @@ partial_pair_kernel(const PartialArgs a) {
             // for the softmax); warps 0-3 and 5-7 split the 16-byte copies,
             // eight lanes per 128-byte row segment.
             const int pw = warp < kWarpMMA ? warp : warp - 1;  // 0..6
-            bool ok = warp_wait(S.q_ready, 0, abort_p);  // the ring doubles as Q staging
+            bool ok = true;
             for (int i = 0; ok && i < ntiles; ++i) {
                 const int rb2 = i & 1;
                 if (pw == 0) {
@@ -336,18 +334,17 @@ partial_pair_kernel(const PartialArgs a) {
             const uint32_t lb = (uint32_t)(32 * quarter) << 16;
             const int stid = tid - 256;            // 0..255
 
-            // Q staging: latent dims into the K ring (padded rows), RoPE dims
-            // straight into their swizzled A-operand tile.
+            // Q staging: RoPE dims into their swizzled A-operand tile by
+            // cp.async; latent dims straight from global memory into TMEM (each
+            // thread its row's 256 dims of this half), so the K ring is never
+            // used for Q and the copy warps start on the keys at once.
             {
-                const uint32_t stage0 = smem_u32(S.kring[0]);
                 const __nv_bfloat16* q0 = a.q + ((int64_t)b * rows_req + rb * kM) * kDqk;
-                for (int f = stid; f < kM * (kDqk / 8); f += 256) {
-                    const int rr = f / (kDqk / 8), c = f % (kDqk / 8);
+                for (int f = stid; f < kM * 8; f += 256) {
+                    const int rr = f >> 3, c = f & 7;
                     const bool v = rb * kM + rr < rows_req;
-                    const __nv_bfloat16* src = v ? q0 + (int64_t)rr * kDqk + c * 8 : a.q;
-                    const uint32_t dst = c < 64 ? stage0 + rr * kQStageStride + c * 16
-                                                : smem_u32(S.q_rope) + sw128_offset(rr, c - 64);
-                    cp_async_16_zfill(dst, src, v);
+                    const __nv_bfloat16* src = v ? q0 + (int64_t)rr * kDqk + 512 + c * 8 : a.q;
+                    cp_async_16_zfill(smem_u32(S.q_rope) + sw128_offset(rr, c), src, v);
                 }
                 if (stid < T) {
                     if (a.anc_mask != nullptr)
@@ -355,26 +352,26 @@ partial_pair_kernel(const PartialArgs a) {
                     else
                         S.par[stid] = a.tree_parent[(int64_t)b * T + stid];
                 }
-                cp_async_wait_all();
-                asm volatile("bar.sync 1, 256;" ::: "memory");
-                if (stid == 0 && a.anc_mask == nullptr) bad |= build_anc_serial(S.par, T, S.anc);
-                if (half == 0) {
-                    const unsigned char* row = S.kring[0] + r * kQStageStride;
+                {
+                    const uint4* src = reinterpret_cast<const uint4*>(q0 + (int64_t)r * kDqk + half * 256);
 #pragma unroll 1
-                    for (int c = 0; c < 8; ++c) {
+                    for (int c = 0; c < 4; ++c) {  // 64 dims (eight 16-byte loads) at a time
                         uint32_t w[32];
 #pragma unroll
                         for (int u = 0; u < 8; ++u) {
-                            const uint4 v = *reinterpret_cast<const uint4*>(row + c * 128 + u * 16);
-                            w[4 * u] = v.x;
-                            w[4 * u + 1] = v.y;
-                            w[4 * u + 2] = v.z;
-                            w[4 * u + 3] = v.w;
+                            const uint4 x = row_ok ? __ldg(src + 8 * c + u) : make_uint4(0, 0, 0, 0);
+                            w[4 * u] = x.x;
+                            w[4 * u + 1] = x.y;
+                            w[4 * u + 2] = x.z;
+                            w[4 * u + 3] = x.w;
                         }
-                        tmem_st32(tbase + lb + kColQ + c * 32, w);
+                        tmem_st32(tbase + lb + kColQ + half * 128 + c * 32, w);
                     }
                     tmem_wait_st();
                 }
+                cp_async_wait_all();
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                if (stid == 0 && a.anc_mask == nullptr) bad |= build_anc_serial(S.par, T, S.anc);
                 fence_proxy_async_smem();
                 tc_fence_before();
                 asm volatile("bar.sync 1, 256;" ::: "memory");
