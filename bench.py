@@ -90,7 +90,7 @@ def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_speculative_decoding_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.startswith("partial") or name in ("tc_ptx.cuh", "common.cuh", "partition.h"):
+        if name in ("partial_quad.cu", "partial_tc.cuh", "tc_ptx.cuh", "common.cuh", "partition.h"):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(f.read())
     return h.hexdigest()[:16]
