@@ -59,6 +59,8 @@ constexpr int kVKeys = 32;
 constexpr int kVStages = 4;
 constexpr uint32_t kVBlock = kVKeys * 128;     // 32 keys x 64 dims
 constexpr uint32_t kVStage = 8 * kVBlock;      // 32 keys x 512 dims
+constexpr int kOTileStride = 36;               // floats per row of the epilogue's write tile
+static_assert(4 * 32 * kOTileStride * 4 <= kVStages * kVStage, "epilogue tiles fit in the V ring");
 constexpr uint32_t kPBlock = kM * 128;         // 128 rows x 64 keys (bf16)
 constexpr uint32_t kColQ = 0, kColS = 256;     // S-CTA TMEM map
 constexpr float kRescaleLog2 = 8.0f;
@@ -650,19 +652,33 @@ partial_pair_kernel(const PartialArgs a) {
                 const float l = O.fin_l[0][r] + O.fin_l[1][r];
                 const float inv = l > 0.f ? 1.f / l : 0.f;
                 const int64_t pid = ((int64_t)b * rows_req + (row_ok ? grow : 0)) * a.nsplit + s;
-                float4* dst = reinterpret_cast<float4*>(a.o_part + pid * kDv);
+                // Coalesced partial write: each 32-row x 32-column chunk goes
+                // through a padded tile in the (now idle) V ring and out again
+                // with eight lanes per row, so every store instruction writes
+                // four whole 128-byte lines instead of 32 lines in part.
+                float* tile = reinterpret_cast<float*>(O.vring[0]) + quarter * (32 * kOTileStride);
+                const int jr = lane >> 3, jc = 4 * (lane & 7);  // row in a group of 4, column
+                const int rj0 = rb * kM + 32 * quarter + jr;       // this lane's row of group 0
+                float* const o0 = a.o_part + (((int64_t)b * rows_req + rj0) * a.nsplit + s) * kDv + jc;
+                const int64_t gstep = (int64_t)4 * a.nsplit * kDv;   // four rows on
 #pragma unroll 1
                 for (int c0 = 0; c0 < 512; c0 += 32) {
                     uint32_t o[32];
                     tmem_ld32(tbase + lb + c0, o);
                     tmem_wait_ld();
-                    if (row_ok) {
 #pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            dst[c0 / 4 + u] = make_float4(
-                                __uint_as_float(o[4 * u]) * inv, __uint_as_float(o[4 * u + 1]) * inv,
-                                __uint_as_float(o[4 * u + 2]) * inv, __uint_as_float(o[4 * u + 3]) * inv);
+                    for (int u = 0; u < 8; ++u)
+                        *reinterpret_cast<float4*>(tile + lane * kOTileStride + 4 * u) = make_float4(
+                            __uint_as_float(o[4 * u]) * inv, __uint_as_float(o[4 * u + 1]) * inv,
+                            __uint_as_float(o[4 * u + 2]) * inv, __uint_as_float(o[4 * u + 3]) * inv);
+                    __syncwarp();
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        const float4 v = *reinterpret_cast<const float4*>(tile + (4 * g + jr) * kOTileStride + jc);
+                        if (rj0 + 4 * g < rows_req)
+                            *reinterpret_cast<float4*>(o0 + g * gstep + c0) = v;
                     }
+                    __syncwarp();
                 }
                 if (row_ok)
                     a.lse_part[pid] = l > 0.f ? (O.fin_m[r] + log2f(l)) * kLn2 : -INFINITY;
