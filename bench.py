@@ -743,7 +743,8 @@ def _probe_blocks(lib, err):
                               (7, 8, "whole 1152 B rows, cp.async x8"),
                               (7, 12, "whole 1152 B rows, cp.async x12"),
                               (8, 8, "128 B of each row, cp.async x8"),
-                              (8, 12, "128 B of each row, cp.async x12")):
+                              (8, 12, "128 B of each row, cp.async x12"),
+                              (9, 1, "whole 1152 B rows, 1-D bulk copies")):
         ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
         nt = ntile if method < 7 else 128
         idx = blocks if method < 7 else row_slots

@@ -835,7 +835,9 @@ namespace {
 //      cp.async by `nw` warps (16128 bytes per stage)
 //   8: as 7 but one 128-byte segment (segment u mod 9) from each of 126
 //      random rows per stage (the same bytes per stage)
-// Methods 7 and 8 read their slots (126 per stage, 14 used by method 7) from
+//   9: as 7 but each row by one 1-D bulk copy of 1152 bytes (lanes 0-13 of
+//      one warp issue a stage's 14 copies)
+// Methods 7, 8 and 9 read their slots (126 per stage, 14 used by method 7) from
 // `blocks` [CTA][stage][126], staged in shared memory like the block indices.
 constexpr int kBStages = 8;
 constexpr int kBMaxIdx = 16384;
@@ -858,7 +860,7 @@ block_rate_kernel(const __grid_constant__ CUtensorMap map, const __grid_constant
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool cp_side = method == 1 || method == 3 || method == 7 || method == 8;
     if (tid == 0) {
-        const uint32_t cnt = method == 0 || method == 2 || method == 5 || method == 6 ? 1u
+        const uint32_t cnt = method == 0 || method == 2 || method == 5 || method == 6 || method == 9 ? 1u
                              : method == 1 || method >= 7 ? 32u * nw
                              : method == 3          ? 1u + 32u * nw
                                                     : 1u;
@@ -914,6 +916,22 @@ block_rate_kernel(const __grid_constant__ CUtensorMap map, const __grid_constant
             }
         }
         __syncwarp();
+    } else if (method == 9 && warp == 14) {
+        for (int u = 0; u < ntile; ++u) {
+            const int st = u % kBStages;
+            if (u >= kBStages &&
+                !mbar_wait(smem_u32(&g.empty[st]), ((u / kBStages) - 1) & 1, &g.abort_flag)) {
+                if (lane == 0) atomicExch(err, 1);
+                break;
+            }
+            const uint32_t fb = smem_u32(&g.full[st]);
+            if (lane == 0) mbar_arrive_expect_tx(fb, 14 * 1152);
+            __syncwarp();
+            if (lane < 14)
+                bulk_load_g2s(smem_u32(g.ring[st]) + lane * 1152, kv + (int64_t)g.idx[u * 126 + lane] * 1152,
+                              1152, fb);
+            __syncwarp();
+        }
     } else if (cp_side && warp < nw) {
         const int first = method == 3 ? 1 : 0;
         for (int u = 0; u < ntile; ++u) {
@@ -989,7 +1007,7 @@ extern "C" __attribute__((visibility("default"))) int mlav_block_rate(
     CUtensorMap map, smap;
     if (!mlav::make_fp8_block_map(&map, kv, nblk) || !mlav::make_fp8_scale_map(&smap, kv, nblk))
         return -2;
-    if (method < 0 || method > 8 || ntile < 1 || (method >= 7 ? 126 : 2) * ntile > kBMaxIdx ||
+    if (method < 0 || method > 9 || ntile < 1 || (method >= 7 ? 126 : 2) * ntile > kBMaxIdx ||
         nctas < 1)
         return -1;
     if ((method == 1 || method == 3 || method == 4 || method >= 7) && (nw < 1 || nw > 12)) return -1;
