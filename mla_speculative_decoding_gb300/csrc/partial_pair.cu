@@ -129,14 +129,15 @@ partial_pair_kernel(const PartialArgs a) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();
     const int rb = blockIdx.x >> 1;
-    const int s = blockIdx.y, b = blockIdx.z;
+    // partition-major dispatch: every request's first partitions launch first
+    const int b = blockIdx.y, s = blockIdx.z;
     const int T = a.T, H = a.H, rows_req = T * H;
 
     int Lb, K;
     int bad = request_keys(a, b, Lb, K);
     int kb, ke;
     const int nrb_req = (a.T * a.H + kM - 1) / kM;
-    split_range_waves(K, a.nsplit, s, kNT, b * a.nsplit * nrb_req + rb, nrb_req, a.wave_full, kb, ke);
+    split_range_waves(K, a.nsplit, s, kNT, b * nrb_req + rb, a.batch * nrb_req, a.wave_full, kb, ke);
     const int ntiles = (ke - kb + kNT - 1) / kNT;
     const int64_t kbase = a.kv_indptr[b];
 
@@ -725,7 +726,7 @@ cudaError_t setup_partial_pair() {
 cudaError_t launch_partial_pair(const PartialArgs& a, cudaStream_t stream) {
     const int rows_req = a.T * a.H;
     const int nrb = (rows_req + kM - 1) / kM;
-    dim3 grid(2 * nrb, a.nsplit, a.batch);
+    dim3 grid(2 * nrb, a.batch, a.nsplit);
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
     PartialArgs w = a;

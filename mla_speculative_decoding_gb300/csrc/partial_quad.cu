@@ -185,7 +185,8 @@ partial_quad_kernel(const PartialArgs a) {
     const bool sside = rank < 2;
     const uint32_t hr = rank & 1u;            // row half (and B-operand half) of this CTA
     const int rb = blockIdx.x >> 2;
-    const int s = blockIdx.y, b = blockIdx.z;
+    // partition-major dispatch: every request's first partitions launch first
+    const int b = blockIdx.y, s = blockIdx.z;
     const int T = a.T, H = a.H, rows_req = T * H;
     const int row0 = rb * kRowsBlk + (int)hr * kMh;  // first request row of this CTA
 
@@ -193,7 +194,7 @@ partial_quad_kernel(const PartialArgs a) {
     int bad = request_keys(a, b, Lb, K);
     int kb, ke;
     const int nrb_req = (a.T * a.H + kRowsBlk - 1) / kRowsBlk;
-    split_range_waves(K, a.nsplit, s, kNT, b * a.nsplit * nrb_req + rb, nrb_req, a.wave_full, kb, ke);
+    split_range_waves(K, a.nsplit, s, kNT, b * nrb_req + rb, a.batch * nrb_req, a.wave_full, kb, ke);
     const int ntiles = (ke - kb + kNT - 1) / kNT;
     const int64_t kbase = a.kv_indptr[b];
 
@@ -865,7 +866,7 @@ cudaError_t setup_partial_quad() {
 cudaError_t launch_partial_quad(const PartialArgs& a, cudaStream_t stream) {
     const int rows_req = a.T * a.H;
     const int nrb = (rows_req + kRowsBlk - 1) / kRowsBlk;
-    dim3 grid(4 * nrb, a.nsplit, a.batch);
+    dim3 grid(4 * nrb, a.batch, a.nsplit);
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
     PartialArgs w = a;

@@ -35,19 +35,19 @@ MLAV_HD inline void split_range_tiles(int K, int nsplit, int s, int tile, int& b
 }
 
 // Wave-shaped variant for launches whose work items run in waves of resident
-// clusters. Items are dispatched in the order (request, partition, row
-// block), row block fastest: the item of partition s is item0 + s * nrb.
-// Items at or past index `full` (the items of the last, partial wave) get one
-// tile each, and the partitions before them share the remaining tiles evenly
-// as in split_range_tiles, so that the full waves end together and the
-// partial wave is as short as possible. Every partition keeps at least one
-// tile. Falls back to split_range_tiles when nothing is in the partial wave,
-// when the whole row block is, or when there are fewer than 2 * nsplit tiles.
-MLAV_HD inline void split_range_waves(int K, int nsplit, int s, int tile, int item0, int nrb,
+// clusters, dispatched in index order: the item of partition s is item0 +
+// s * stride. Items at or past index `full` (the items of the last, partial
+// wave) get one tile each, and the partitions before them share the
+// remaining tiles evenly as in split_range_tiles, so that the full waves end
+// together and the partial wave is as short as possible. Every partition
+// keeps at least one tile. Falls back to split_range_tiles when nothing is
+// in the partial wave, when the whole range is, or when there are fewer than
+// 2 * nsplit tiles.
+MLAV_HD inline void split_range_waves(int K, int nsplit, int s, int tile, int item0, int stride,
                                       int full, int& beg, int& end) {
     const int tiles = (K + tile - 1) / tile;
-    const int last = item0 + (nsplit - 1) * nrb;  // item of the last partition
-    const int s_tail = last < full ? nsplit : (full <= item0 ? 0 : (full - item0 + nrb - 1) / nrb);
+    const int last = item0 + (nsplit - 1) * stride;  // item of the last partition
+    const int s_tail = last < full ? nsplit : (full <= item0 ? 0 : (full - item0 + stride - 1) / stride);
     const int n_tail = nsplit - s_tail;
     if (n_tail == 0 || s_tail == 0 || tiles < 2 * nsplit) {
         split_range_tiles(K, nsplit, s, tile, beg, end);

@@ -32,10 +32,10 @@ int main() {
         const int full = wave_full_items(items, res);
         printf("W %lld %d %d\n", items, res, full);
         for (int b = 0; b < B; ++b) for (int rb = 0; rb < nrb; ++rb) {
-            const int item0 = b * ns * nrb + rb;
+            const int item0 = b * nrb + rb;  // partition-major dispatch
             for (int s = 0; s < ns; ++s) {
                 int beg, end;
-                split_range_waves(K, ns, s, tile, item0, nrb, full, beg, end);
+                split_range_waves(K, ns, s, tile, item0, B * nrb, full, beg, end);
                 printf("P %d %d %d %d %d %d %d %d %d %d\n", K, ns, nrb, B, res, b, rb, s, beg, end);
             }
         }
@@ -106,7 +106,7 @@ def test_wave_shaped_split(table):
         _check_cover(K, ranges)
         tiles = -(-K // 256)
         full = full_of[(B * ns * nrb, res)]
-        item = [(b * ns + s) * nrb + rb for s, _, _ in ranges]
+        item = [(s * B + b) * nrb + rb for s, _, _ in ranges]
         tail = [i >= full for i in item]
         sizes = [-(-(e - beg) // 256) for _, beg, e in ranges]
         if tiles >= 2 * ns:
