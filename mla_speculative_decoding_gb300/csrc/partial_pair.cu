@@ -287,7 +287,9 @@ partial_pair_kernel(const PartialArgs a) {
                 fence_proxy_async_smem();
                 tc_fence_after();
                 const uint32_t dS = tbase + kColS;
-                const uint32_t qr = smem_u32(S.q_rope);
+                // descriptors precomputed; the loop only adds offsets
+                const uint64_t kdesc0 = make_sdesc(smem_u32(S.kring[0]), 16, 1024, kSwizzle128B);
+                const uint64_t qrdesc = make_sdesc(smem_u32(S.q_rope), 16, 1024, kSwizzle128B);
                 for (int i = 0; ok && i < ntiles; ++i) {
                     if (i >= 1 && !mbar_wait(ba(S.s_free), (i - 1) & 1, abort_p)) {
                         ok = false;
@@ -303,16 +305,18 @@ partial_pair_kernel(const PartialArgs a) {
                         }
                         fence_proxy_async_smem();
                         tc_fence_after();
-                        const uint32_t kt = smem_u32(S.kring[st]);
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            const uint64_t bd = make_sdesc(kt + ks * 32, 16, 1024, kSwizzle128B);
-                            const uint32_t acc = (kbk | ks) ? 1u : 0u;
-                            if (kbk < 8)
-                                mma_ts(dS, tbase + kColQ + kbk * 32 + ks * 8, bd, idesc, acc);
-                            else
-                                mma_ss(dS, make_sdesc(qr + ks * 32, 16, 1024, kSwizzle128B), bd,
-                                       idesc, acc);
+                        const uint64_t bd = kdesc0 + (uint64_t)st * (kKBlock >> 4);
+                        if (kbk < 8) {
+                            const uint32_t aa = tbase + kColQ + kbk * 32;
+                            mma_ts(dS, aa, bd, idesc, kbk > 0 ? 1u : 0u);
+                            mma_ts(dS, aa + 8, bd + 2, idesc, 1u);
+                            mma_ts(dS, aa + 16, bd + 4, idesc, 1u);
+                            mma_ts(dS, aa + 24, bd + 6, idesc, 1u);
+                        } else {
+                            mma_ss(dS, qrdesc, bd, idesc, 1u);
+                            mma_ss(dS, qrdesc + 2, bd + 2, idesc, 1u);
+                            mma_ss(dS, qrdesc + 4, bd + 4, idesc, 1u);
+                            mma_ss(dS, qrdesc + 6, bd + 6, idesc, 1u);
                         }
                         mma_commit(ba(S.k_empty[st]));
                     }
@@ -561,7 +565,12 @@ partial_pair_kernel(const PartialArgs a) {
             if (lane == 0) {
                 const uint32_t idesc = make_idesc_bf16(kM, 256, false, true);
                 const uint32_t pfree_peer = mapa_shared(ba(sm.h.p_free), peer);
-                const uint32_t p0 = smem_u32(O.p);
+                // descriptors precomputed: only the low word (start address) moves
+                const uint64_t pdesc0 = make_sdesc(smem_u32(O.p), 16, 1024, kSwizzle128B);
+                const uint64_t vdesc0 = make_sdesc(smem_u32(O.vring[0]), kVBlock, 1024, kSwizzle128B);
+                const uint32_t plo = (uint32_t)pdesc0, phi = (uint32_t)(pdesc0 >> 32);
+                const uint32_t vlo = (uint32_t)vdesc0, vhi = (uint32_t)(vdesc0 >> 32);
+                auto dsc = [](uint32_t lo, uint32_t hi) { return ((uint64_t)hi << 32) | lo; };
                 bool ok = true;
                 for (int i = 0; ok && i < ntiles; ++i) {
                     if (!mbar_wait_cluster(ba(sm.h.p_full), i & 1, abort_p) ||
@@ -580,20 +589,14 @@ partial_pair_kernel(const PartialArgs a) {
                         }
                         fence_proxy_async_smem();
                         tc_fence_after();
-                        const uint32_t vs = smem_u32(O.vring[st]);
-#pragma unroll
-                        for (int kk = 0; kk < 2; ++kk) {
-                            const int kg = q * 32 + kk * 16;  // key within the tile
-                            const uint64_t ad = make_sdesc(p0 + (kg >> 6) * kPBlock + ((kg & 63) >> 4) * 32,
-                                                           16, 1024, kSwizzle128B);
-#pragma unroll
-                            for (int hv = 0; hv < 2; ++hv) {
-                                const uint64_t bd = make_sdesc(vs + hv * 4 * kVBlock + kk * 2048,
-                                                               kVBlock, 1024, kSwizzle128B);
-                                mma_ss(tbase + hv * 256, ad, bd, idesc,
-                                       (i > 0 || q > 0 || kk > 0) ? 1u : 0u);
-                            }
-                        }
+                        const uint32_t vd = vlo + (uint32_t)st * (kVStage >> 4);
+                        // keys q*32 .. q*32+31 of the tile: P block q / 2, 16-key steps
+                        const uint32_t pd = plo + (uint32_t)((q >> 1) * kPBlock + (q & 1) * 64) / 16;
+                        const uint32_t acc0 = (i > 0 || q > 0) ? 1u : 0u;
+                        mma_ss(tbase, dsc(pd, phi), dsc(vd, vhi), idesc, acc0);
+                        mma_ss(tbase + 256, dsc(pd, phi), dsc(vd + (4 * kVBlock) / 16, vhi), idesc, acc0);
+                        mma_ss(tbase, dsc(pd + 2, phi), dsc(vd + 2048 / 16, vhi), idesc, 1u);
+                        mma_ss(tbase + 256, dsc(pd + 2, phi), dsc(vd + (4 * kVBlock + 2048) / 16, vhi), idesc, 1u);
                         mma_commit(ba(O.v_empty[st]));
                     }
                     if (!ok) break;
