@@ -50,6 +50,16 @@ def log(*a):
 
 
 # ----------------------------------------------------------------- workload arithmetic
+def workload_name(idx):
+    """What a verify workload is, with its sizes (e.g. "long verify: 1 x
+    prefix 184728, T=64, H=8, nsplit 64")."""
+    c = CONFIGS[idx]
+    kind, _, rest = c["prefix"].partition(":")
+    prefix = rest if kind == "fixed" else "U[" + rest.replace(":", ", ") + "]"
+    return (f"{c['name']} verify: {c['batch']} x prefix {prefix}, T={c['T']}, "
+            f"H={c['num_heads']}, nsplit {c['nsplit']}")
+
+
 def workload_figures(inp):
     """Algorithmic bytes and flops of one verify call (each KV row read once;
     flops count only visible (row, key) pairs)."""
@@ -383,7 +393,7 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_step_max / 1e3, 6),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 q and latent KV; random trees; scattered slots)",
-        "config": {"workload": f"config{idx}:{CONFIGS[idx]['name']}", "batch": inp.batch,
+        "config": {"workload": workload_name(idx), "batch": inp.batch,
                    "heads": inp.num_heads, "prefix_lens": [int(x) for x in inp.prefix_lens][:8],
                    "T": inp.T, "nsplit": inp.nsplit, "pool_slots": inp.pool_slots,
                    "l2": L2Flush.DESCRIPTION,
@@ -616,7 +626,7 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(value / 1e3, 3), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"config{idx}:{CONFIGS[idx]['name']}", "batch": inp.batch,
+        "config": {"workload": workload_name(idx), "batch": inp.batch,
                    "heads": inp.num_heads, "T": inp.T, "nsplit": inp.nsplit},
         "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": threads,
                          "kind": "oracle", "sample": sample},
