@@ -40,6 +40,14 @@
 // into another CTA's shared memory (the final row maxima and sums) uses
 // cluster scope.
 //
+// Persistent clusters: the launch holds one cluster per resident slot, and
+// cluster c takes the work items of rounds k = 0, 1, ... at position
+// (c + k) mod C of each round of C items (C = the launch's clusters), so that
+// over the rounds every cluster meets every request and row block. Every
+// ring, slot and barrier phase counts over the cluster's whole tile
+// sequence, so one item's drain (last softmax, P hand-over, last P V and the
+// partial write) overlaps the next item's Q staging and first key stages.
+//
 // Every wait is bounded; on a timeout a CTA drains its MMAs, reaches the
 // final cluster barrier, frees TMEM and flags MLA_STATUS_TIMEOUT.
 #include "partial_tc.cuh"
@@ -78,12 +86,10 @@ constexpr int kVStages = 4;
 constexpr uint32_t kVSub = kVKeys * 128;       // 32 keys x 64 dims = 4 KB
 constexpr uint32_t kVStage = 4 * kVSub;        // [chain][segment][32 keys][64 dims]
 constexpr int kOTileStride = 36;               // floats per row of the epilogue's write tile
-static_assert(4 * 32 * kOTileStride * 4 <= kVStages * kVStage, "epilogue tiles fit in the V ring");
 constexpr uint32_t kPBlock = kMh * 128;        // 128 rows x 64 keys (bf16)
 constexpr uint32_t kPBytes = 4 * kPBlock;      // 128 rows x 256 keys
 constexpr uint32_t kPXfer = kPBytes + kMh * 4; // P + per-row rescale factors
 constexpr uint32_t kPSlot = 67584;             // 1024-aligned P slot
-constexpr uint32_t kQStageStride = 1040;       // padded staging row of 512 bf16
 constexpr uint32_t kColQ = 0, kColS = 256;     // S-CTA TMEM map
 constexpr float kRescaleLog2 = 8.0f;
 
@@ -98,18 +104,20 @@ struct SmemS {
     int32_t par[MLA_MAX_TREE];
     uint64_t k_full[kKStages], k_empty[kKStages];
     uint64_t meta_full[kMetaRing], meta_free[kMetaRing];
-    uint64_t s_full, s_free, q_ready, q_peer, mx_bar[2], pw_bar[2], pstage_free;
+    uint64_t s_full, s_free, q_landed, q_ready, q_peer, mx_bar[2], pw_bar[2], pstage_free;
     uint64_t rows_full[kRowsRing];
     uint64_t p_free[2];
+    uint64_t fin_free[2];                       // the O partner has read fin[slot]
 };
 struct SmemO {
     unsigned char pbuf[2][kPSlot];              // P + alpha, one slot per tile parity
     unsigned char vring[kVStages][kVStage];
     int32_t rows[kRowsRing][kNT];
-    float fin_m[kMh];
-    float fin_l[2][kMh];
+    float otile[4][32 * kOTileStride];          // the epilogue's write tiles, one per warp
+    float fin_m[2][kMh];                        // per item parity: row maxima
+    float fin_l[2][2][kMh];                     //   and the two key halves' sums
     uint64_t v_full[kVStages], v_empty[kVStages];
-    uint64_t p_full[2], o_gate[2], o_done[2], fin;
+    uint64_t p_full[2], o_gate[2], o_done[2], fin[2];
     uint64_t rows_full[kRowsRing], rows_free[kRowsRing];
 };
 struct Header {
@@ -128,8 +136,7 @@ struct __align__(1024) SmemQuad {
 
 constexpr size_t kSmemBytes = sizeof(SmemQuad) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kMh * kQStageStride <= kKStages * kKBlock + kPXfer,
-              "Q staging must fit in the K ring and the P staging tile");
+static_assert(kKStages * kKBlock == kMh * 1024, "Q's latent dims are staged in the K ring");
 static_assert(kPXfer <= kPSlot && kPSlot % 1024 == 0, "P slot");
 
 __device__ __forceinline__ uint32_t ba(const uint64_t& b) { return smem_u32(&b); }
@@ -175,6 +182,56 @@ __device__ __forceinline__ int stage_rows(const PartialArgs& a, int64_t kbase, i
     return bad;
 }
 
+// One work item of a cluster's sequence: request b, partition s and row
+// block rb, with its key range [kb, ke) in ntiles tiles.
+struct QuadItem {
+    int b, s, rb, kb, ke, ntiles, Lb, bad;
+};
+
+// Item k of cluster `cid` of `C`: round k, position (cid + k) mod C; false
+// past the last item. Items are numbered partition-major, ((s * batch + b) *
+// nrb + rb), so every request's first partitions come first.
+__device__ __forceinline__ bool quad_item(const PartialArgs& a, int nrb, int n_items, int C, int cid,
+                                          int k, QuadItem& it) {
+    const long long j = (long long)k * C + (cid + k) % C;
+    if (j >= n_items) return false;
+    const int jj = (int)j;
+    it.rb = jj % nrb;
+    const int t = jj / nrb;
+    it.b = t % a.batch;
+    it.s = t / a.batch;
+    int K;
+    it.bad = request_keys(a, it.b, it.Lb, K);
+    split_range_waves(K, a.nsplit, it.s, kNT, it.b * nrb + it.rb, a.batch * nrb, a.wave_full, it.kb, it.ke);
+    it.ntiles = (it.ke - it.kb + kNT - 1) / kNT;
+    return true;
+}
+
+// The cluster's tiles in order over its non-empty items.
+struct TileCursor {
+    QuadItem it;
+    int k, i, bad;
+};
+__device__ __forceinline__ void cursor_init(TileCursor& c) {
+    c.k = 0;
+    c.i = 0;
+    c.it.ntiles = 0;
+    c.bad = 0;
+}
+// Moves to the next tile; false past the last one.
+__device__ __forceinline__ bool cursor_next(TileCursor& c, const PartialArgs& a, int nrb, int n_items,
+                                            int C, int cid) {
+    if (++c.i < c.it.ntiles) return true;
+    for (;;) {
+        if (!quad_item(a, nrb, n_items, C, cid, c.k++, c.it)) return false;
+        c.bad |= c.it.bad;
+        if (c.it.ntiles > 0) {
+            c.i = 0;
+            return true;
+        }
+    }
+}
+
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 partial_quad_kernel(const PartialArgs a) {
     extern __shared__ __align__(1024) unsigned char raw[];
@@ -184,34 +241,11 @@ partial_quad_kernel(const PartialArgs a) {
     const uint32_t rank = cluster_ctarank();
     const bool sside = rank < 2;
     const uint32_t hr = rank & 1u;            // row half (and B-operand half) of this CTA
-    const int rb = blockIdx.x >> 2;
-    // partition-major dispatch: every request's first partitions launch first
-    const int b = blockIdx.y, s = blockIdx.z;
+    const int cid = blockIdx.x >> 2, C = gridDim.x >> 2;
     const int T = a.T, H = a.H, rows_req = T * H;
-    const int row0 = rb * kRowsBlk + (int)hr * kMh;  // first request row of this CTA
-
-    int Lb, K;
-    int bad = request_keys(a, b, Lb, K);
-    int kb, ke;
-    const int nrb_req = (a.T * a.H + kRowsBlk - 1) / kRowsBlk;
-    split_range_waves(K, a.nsplit, s, kNT, b * nrb_req + rb, a.batch * nrb_req, a.wave_full, kb, ke);
-    const int ntiles = (ke - kb + kNT - 1) / kNT;
-    const int64_t kbase = a.kv_indptr[b];
-
-    if (ntiles <= 0) {  // empty split (fixed grid, early exit): lse = -inf, o = 0
-        if (!sside && warp >= 8 && warp < 12) {
-            const int grow = row0 + 32 * (warp & 3) + lane;
-            if (grow < rows_req) {
-                const int64_t pid = ((int64_t)b * rows_req + grow) * a.nsplit + s;
-                float4* o = reinterpret_cast<float4*>(a.o_part + pid * kDv);
-                for (int c = 0; c < kDv / 4; ++c) o[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-                a.lse_part[pid] = -INFINITY;
-            }
-        }
-        if (rank == 0 && tid == 0) status_or(a.status, bad);
-        return;
-    }
-    if (rank != 0) bad &= ~MLA_STATUS_BAD_INDPTR;  // reported once
+    const int nrb = (rows_req + kRowsBlk - 1) / kRowsBlk;
+    const int n_items = a.batch * a.nsplit * nrb;
+    int bad = 0;
 
     if (warp == kWarpMMA) {  // both CTAs of each pair allocate together
         tmem_alloc_pair(smem_u32(&sm.h.tmem_base), 512);
@@ -232,12 +266,14 @@ partial_quad_kernel(const PartialArgs a) {
             mbar_init(ba(S.s_full), 1);
             mbar_init(ba(S.s_free), 16);  // rank 0's: the softmax warps of both S CTAs
             mbar_init(ba(S.pstage_free), 1);
+            mbar_init(ba(S.q_landed), 256);
             mbar_init(ba(S.q_ready), 256);
             mbar_init(ba(S.q_peer), 1);
             for (int i = 0; i < 2; ++i) {
                 mbar_init(ba(S.mx_bar[i]), 8);
                 mbar_init(ba(S.pw_bar[i]), 8);
                 mbar_init(ba(S.p_free[i]), 1);
+                mbar_init(ba(S.fin_free[i]), 4);  // the O partner's four correction warps
             }
             for (int i = 0; i < kRowsRing; ++i) {
                 mbar_init(ba(S.rows_full[i]), 1);
@@ -252,12 +288,12 @@ partial_quad_kernel(const PartialArgs a) {
                 mbar_init(ba(O.p_full[i]), 1);
                 mbar_init(ba(O.o_gate[i]), 8);
                 mbar_init(ba(O.o_done[i]), 1);
+                mbar_init(ba(O.fin[i]), 256);
             }
             for (int i = 0; i < kRowsRing; ++i) {
                 mbar_init(ba(O.rows_full[i]), 1);
                 mbar_init(ba(O.rows_free[i]), kOProd);
             }
-            mbar_init(ba(O.fin), 256);
         }
         sm.h.abort_flag = 0;
         sm.h.no_abort = 0;
@@ -276,71 +312,100 @@ partial_quad_kernel(const PartialArgs a) {
         SmemS& S = sm.u.s;
         if (warp != kWarpMMA && warp != kWarpCtl) {
             // ------------------------------------------------ S producers: K blocks
-            // The ten producer warps form five groups of two; stage g (this
-            // CTA's 128 keys x 64 dims of one tile) is copied by group g mod 5,
-            // eight lanes per 128-byte row segment, so that stages complete
-            // independently of one another.
+            // The ten producer warps form five groups of two; fill g of the
+            // cluster's sequence (this CTA's 128 keys x 64 dims of one tile)
+            // is copied by group g mod 5, eight lanes per 128-byte row
+            // segment, so that stages complete independently of one another.
             const int pw = warp < kWarpMMA ? warp : (warp < 8 ? warp - 1 : warp - 10);  // 0..9
             const int grp = pw / kSGroup, gw = pw % kSGroup;
             constexpr int kNGroups = kSProd / kSGroup;
-            bool ok = warp_wait(S.q_ready, 0, abort_p);  // the ring doubles as Q staging
-            const int nfill = ntiles * (kDqk / 64);
-            int seen = -1;  // last tile whose pool rows this warp has waited for
-            for (int g = grp; ok && g < nfill; g += kNGroups) {
-                const int i = g / (kDqk / 64), kbk = g % (kDqk / 64);
-                const int rs = i % kRowsRing;
-                const int st = g % kKStages;
-                if (i != seen) {
-                    if (!warp_wait(S.rows_full[rs], (i / kRowsRing) & 1, abort_p)) break;
-                    seen = i;
+            constexpr int kFills = kDqk / 64;  // per tile
+            bool ok = true;
+            int g0 = 0, j0 = 0, ne = 0;  // fills, tiles and non-empty items so far
+            QuadItem it;
+            for (int k = 0; ok && quad_item(a, nrb, n_items, C, cid, k, it); ++k) {
+                if (it.ntiles <= 0) continue;
+                ok = warp_wait(S.q_ready, ne & 1, abort_p);  // the ring doubles as Q staging
+                const int nfill = it.ntiles * kFills;
+                int seen = -1;  // last tile whose pool rows this warp has waited for
+                for (int g = g0 + (grp - g0 % kNGroups + kNGroups) % kNGroups; ok && g < g0 + nfill;
+                     g += kNGroups) {
+                    const int jt = j0 + (g - g0) / kFills, kbk = (g - g0) % kFills;
+                    const int rs = jt % kRowsRing;
+                    const int st = g % kKStages;
+                    if (jt != seen) {
+                        if (!warp_wait(S.rows_full[rs], (jt / kRowsRing) & 1, abort_p)) {
+                            ok = false;
+                            break;
+                        }
+                        seen = jt;
+                    }
+                    if (g >= kKStages && !warp_wait(S.k_empty[st], ((g / kKStages) - 1) & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    const int32_t* my_rows = S.rows[rs] + hr * kNh;
+                    const uint32_t dst0 = smem_u32(S.kring[st]);
+                    for (int r = gw; r < kNh / 4; r += kSGroup) {
+                        const int key = r * 4 + (lane >> 3), c = lane & 7;
+                        const int32_t slot = my_rows[key];
+                        const __nv_bfloat16* src =
+                            a.kv + (slot >= 0 ? (int64_t)slot * kDqk : 0) + kbk * 64 + c * 8;
+                        cp_async_16_zfill_nc(dst0 + sw128_offset(key, c), src, slot >= 0);
+                    }
+                    cp_async_mbar_arrive_noinc(ba(S.k_full[st]));
                 }
-                if (g >= kKStages && !warp_wait(S.k_empty[st], ((g / kKStages) - 1) & 1, abort_p)) break;
-                const int32_t* my_rows = S.rows[rs] + hr * kNh;
-                const uint32_t dst0 = smem_u32(S.kring[st]);
-                for (int it = gw; it < kNh / 4; it += kSGroup) {
-                    const int key = it * 4 + (lane >> 3), c = lane & 7;
-                    const int32_t slot = my_rows[key];
-                    const __nv_bfloat16* src =
-                        a.kv + (slot >= 0 ? (int64_t)slot * kDqk : 0) + kbk * 64 + c * 8;
-                    cp_async_16_zfill_nc(dst0 + sw128_offset(key, c), src, slot >= 0);
-                }
-                cp_async_mbar_arrive_noinc(ba(S.k_full[st]));
+                g0 += nfill;
+                j0 += it.ntiles;
+                ++ne;
             }
             cp_async_wait_all();
         } else if (warp == kWarpCtl) {
             // ------------------------------------------------ tile metadata + P sender
             // The warp stages each tile's pool rows (all 256, with validity
-            // bits for the softmax) two tiles ahead of the copies; lane 0 sends
-            // each tile's P (and rescale factors) from the staging tile to the
-            // O partner's slot once that slot is free, then hands the staging
-            // tile back to the softmax.
+            // bits for the softmax) two tiles ahead of the copies, across
+            // item boundaries; lane 0 sends each tile's P (and rescale
+            // factors) from the staging tile to the O partner's slot once that
+            // slot is free, then hands the staging tile back to the softmax.
             // Slot j % 4 last held tile j - 4; the softmax has released that
             // tile's validity bits only after its S tile was complete, i.e.
             // after every producer had issued every stage of it, so the pool
             // rows are free as well.
             static_assert(kRowsRing == kMetaRing, "rows and metadata share the release");
-            auto stage = [&](int j) -> bool {
+            TileCursor cur;
+            cursor_init(cur);
+            int staged = 0;
+            auto stage_next = [&]() -> int {  // 1: staged, 0: no tile left, -1: timed out
+                if (!cursor_next(cur, a, nrb, n_items, C, cid)) return 0;
+                const int j = staged;
                 const int rs = j % kRowsRing, mi = j % kMetaRing;
                 if (j >= kMetaRing && !warp_wait(S.meta_free[mi], ((j / kMetaRing) - 1) & 1, abort_p))
-                    return false;
-                bad |= stage_rows(a, kbase, kb + j * kNT, ke, lane, S.rows[rs], S.valid[mi]);
+                    return -1;
+                bad |= stage_rows(a, a.kv_indptr[cur.it.b], cur.it.kb + cur.i * kNT, cur.it.ke, lane,
+                                  S.rows[rs], S.valid[mi]);
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(ba(S.meta_full[mi]));
                     mbar_arrive(ba(S.rows_full[rs]));
                 }
-                return true;
+                ++staged;
+                return 1;
             };
             const uint32_t p_local = smem_u32(S.pstage);
             const uint32_t orank = 2u + hr;
-            bool ok = stage(0) && (ntiles < 2 || stage(1));
-            for (int i = 0; ok && i < ntiles; ++i) {
-                if (i + 2 < ntiles && !stage(i + 2)) break;
+            int more = stage_next();
+            if (more > 0) more = stage_next();
+            bool ok = more >= 0;
+            for (int j = 0; ok && j < staged; ++j) {
+                if (more > 0) {
+                    more = stage_next();
+                    if (more < 0) break;
+                }
                 int sent = 1;
                 if (lane == 0) {
-                    const int slot = i & 1;
-                    sent = mbar_wait_spin(ba(S.pw_bar[slot]), (i >> 1) & 1, abort_p);
-                    if (sent && i >= 2) sent = mbar_wait_spin(ba(S.p_free[slot]), ((i - 2) >> 1) & 1, abort_p);
+                    const int slot = j & 1;
+                    sent = mbar_wait_spin(ba(S.pw_bar[slot]), (j >> 1) & 1, abort_p);
+                    if (sent && j >= 2) sent = mbar_wait_spin(ba(S.p_free[slot]), ((j - 2) >> 1) & 1, abort_p);
                     if (sent) {
                         const uint32_t dst = mapa_shared(smem_u32(sm.u.o.pbuf[slot]), orank);
                         const uint32_t bar = mapa_shared(ba(sm.u.o.p_full[slot]), orank);
@@ -357,6 +422,7 @@ partial_quad_kernel(const PartialArgs a) {
                 ok = __shfl_sync(0xffffffffu, sent, 0) != 0;
             }
             if (lane == 0) bulk_wait_all();
+            bad |= cur.bad;
         } else if (rank == 0) {
             // ------------------------------------------------ S MMA issuer (pair)
             // The issue loop is kept free of per-MMA descriptor construction
@@ -364,50 +430,56 @@ partial_quad_kernel(const PartialArgs a) {
             // issuing thread does between MMAs is lost tensor time.
             if (lane == 0) {
                 const uint32_t idesc = make_idesc_bf16(kRowsBlk, kNT, false, false);
-                bool ok = mbar_wait_spin(ba(S.q_ready), 0, abort_p) &&
-                          mbar_wait_spin(ba(S.q_peer), 0, abort_p);
-                fence_proxy_async_smem();
-                tc_fence_after();
                 const uint32_t dS = tbase + kColS;
                 const uint64_t kdesc0 = make_sdesc(smem_u32(S.kring[0]), 16, 1024, kSwizzle128B);
                 const uint64_t qrdesc = make_sdesc(smem_u32(S.q_rope), 16, 1024, kSwizzle128B);
                 const uint32_t kfull0 = ba(S.k_full[0]), kempty0 = ba(S.k_empty[0]);
-                int st = 0;
+                int st = 0, jt = 0, ne = 0;  // ring stage, tiles and non-empty items so far
                 uint32_t ph = 0;
-                for (int i = 0; ok && i < ntiles; ++i) {
-                    if (i >= 1 && !mbar_wait_spin(ba(S.s_free), (i - 1) & 1, abort_p)) {
-                        ok = false;
-                        break;
-                    }
+                bool ok = true;
+                QuadItem it;
+                for (int k = 0; ok && quad_item(a, nrb, n_items, C, cid, k, it); ++k) {
+                    if (it.ntiles <= 0) continue;
+                    ok = mbar_wait_spin(ba(S.q_ready), ne & 1, abort_p) &&
+                         mbar_wait_spin(ba(S.q_peer), ne & 1, abort_p);
+                    fence_proxy_async_smem();
                     tc_fence_after();
-#pragma unroll 1
-                    for (int kbk = 0; kbk < kDqk / 64; ++kbk) {
-                        if (!mbar_wait_spin(kfull0 + 8 * st, ph, abort_p)) {
+                    for (int i = 0; ok && i < it.ntiles; ++i, ++jt) {
+                        if (jt >= 1 && !mbar_wait_spin(ba(S.s_free), (jt - 1) & 1, abort_p)) {
                             ok = false;
                             break;
                         }
-                        fence_proxy_async_smem();
                         tc_fence_after();
-                        const uint64_t bd = kdesc0 + (uint64_t)(st * (kKBlock >> 4));
-                        if (kbk < 8) {  // latent dims: A = Q from TMEM
-                            const uint32_t aa = tbase + kColQ + kbk * 32;
-                            mma_ts_pair(dS, aa, bd, idesc, kbk > 0 ? 1u : 0u);
-                            mma_ts_pair(dS, aa + 8, bd + 2, idesc, 1u);
-                            mma_ts_pair(dS, aa + 16, bd + 4, idesc, 1u);
-                            mma_ts_pair(dS, aa + 24, bd + 6, idesc, 1u);
-                        } else {        // RoPE dims: A = Q's RoPE tile in shared memory
-                            mma_ss_pair(dS, qrdesc, bd, idesc, 1u);
-                            mma_ss_pair(dS, qrdesc + 2, bd + 2, idesc, 1u);
-                            mma_ss_pair(dS, qrdesc + 4, bd + 4, idesc, 1u);
-                            mma_ss_pair(dS, qrdesc + 6, bd + 6, idesc, 1u);
+#pragma unroll 1
+                        for (int kbk = 0; kbk < kDqk / 64; ++kbk) {
+                            if (!mbar_wait_spin(kfull0 + 8 * st, ph, abort_p)) {
+                                ok = false;
+                                break;
+                            }
+                            fence_proxy_async_smem();
+                            tc_fence_after();
+                            const uint64_t bd = kdesc0 + (uint64_t)(st * (kKBlock >> 4));
+                            if (kbk < 8) {  // latent dims: A = Q from TMEM
+                                const uint32_t aa = tbase + kColQ + kbk * 32;
+                                mma_ts_pair(dS, aa, bd, idesc, kbk > 0 ? 1u : 0u);
+                                mma_ts_pair(dS, aa + 8, bd + 2, idesc, 1u);
+                                mma_ts_pair(dS, aa + 16, bd + 4, idesc, 1u);
+                                mma_ts_pair(dS, aa + 24, bd + 6, idesc, 1u);
+                            } else {        // RoPE dims: A = Q's RoPE tile in shared memory
+                                mma_ss_pair(dS, qrdesc, bd, idesc, 1u);
+                                mma_ss_pair(dS, qrdesc + 2, bd + 2, idesc, 1u);
+                                mma_ss_pair(dS, qrdesc + 4, bd + 4, idesc, 1u);
+                                mma_ss_pair(dS, qrdesc + 6, bd + 6, idesc, 1u);
+                            }
+                            mma_commit_pair_mc(kempty0 + 8 * st, 0x3);
+                            if (++st == kKStages) {
+                                st = 0;
+                                ph ^= 1u;
+                            }
                         }
-                        mma_commit_pair_mc(kempty0 + 8 * st, 0x3);
-                        if (++st == kKStages) {
-                            st = 0;
-                            ph ^= 1u;
-                        }
+                        if (ok) mma_commit_pair_mc(ba(S.s_full), 0x3);
                     }
-                    if (ok) mma_commit_pair_mc(ba(S.s_full), 0x3);
+                    ++ne;
                 }
                 mma_commit_pair_mc(ba(sm.h.drain), 0x1);
                 mbar_wait(ba(sm.h.drain), 0, &sm.h.no_abort);
@@ -415,18 +487,29 @@ partial_quad_kernel(const PartialArgs a) {
         } else {
             // ------------------------------------------------ rank 1: forward readiness to rank 0
             // Copies complete on this CTA's own barriers; rank 0's MMA issuer
-            // learns of each filled K stage through this thread.
+            // learns of each filled K stage (and of this CTA's Q) through
+            // this thread.
             if (lane == 0) {
-                bool ok = mbar_wait_spin(ba(S.q_ready), 0, abort_p);
-                tc_fence_after();
-                tc_fence_before();
-                if (ok) mbar_arrive_remote(mapa_shared(ba(S.q_peer), 0));
-                const int nfill = ntiles * (kDqk / 64);
-                for (int g = 0; ok && g < nfill; ++g) {
-                    const int st = g % kKStages;
-                    if (!mbar_wait_spin(ba(S.k_full[st]), (g / kKStages) & 1, abort_p)) break;
-                    fence_proxy_async_smem();
-                    mbar_arrive_remote(mapa_shared(ba(S.k_full[st]), 0));
+                int g = 0, ne = 0;
+                bool ok = true;
+                QuadItem it;
+                for (int k = 0; ok && quad_item(a, nrb, n_items, C, cid, k, it); ++k) {
+                    if (it.ntiles <= 0) continue;
+                    ok = mbar_wait_spin(ba(S.q_ready), ne & 1, abort_p);
+                    tc_fence_after();
+                    tc_fence_before();
+                    if (ok) mbar_arrive_remote(mapa_shared(ba(S.q_peer), 0));
+                    const int gend = g + it.ntiles * (kDqk / 64);
+                    for (; ok && g < gend; ++g) {
+                        const int st = g % kKStages;
+                        if (!mbar_wait_spin(ba(S.k_full[st]), (g / kKStages) & 1, abort_p)) {
+                            ok = false;
+                            break;
+                        }
+                        fence_proxy_async_smem();
+                        mbar_arrive_remote(mapa_shared(ba(S.k_full[st]), 0));
+                    }
+                    ++ne;
                 }
             }
         }
@@ -439,184 +522,210 @@ partial_quad_kernel(const PartialArgs a) {
             const int quarter = warp & 3;
             const int half = (warp - 8) >> 2;     // 128-key half of the tile
             const int r = 32 * quarter + lane;     // row = TMEM lane
-            const int grow = row0 + r;
-            const bool row_ok = grow < rows_req;
-            const int t = row_ok ? grow / H : 0;
             const uint32_t lb = (uint32_t)(32 * quarter) << 16;
             const int stid = tid - 256;            // 0..255
             const uint32_t orank = 2u + hr;        // O partner holding the same rows
-
-            // Q staging: latent dims into the K ring (padded rows), RoPE dims
-            // straight into their swizzled A-operand tile.
-            {
-                const uint32_t stage0 = smem_u32(S.kring[0]);
-                const __nv_bfloat16* q0 = a.q + ((int64_t)b * rows_req + row0) * kDqk;
-                for (int f = stid; f < kMh * (kDqk / 8); f += 256) {
-                    const int rr = f / (kDqk / 8), c = f % (kDqk / 8);
-                    const bool v = row0 + rr < rows_req;
-                    const __nv_bfloat16* src = v ? q0 + (int64_t)rr * kDqk + c * 8 : a.q;
-                    const uint32_t dst = c < 64 ? stage0 + rr * kQStageStride + c * 16
-                                                : smem_u32(S.q_rope) + sw128_offset(rr, c - 64);
-                    cp_async_16_zfill(dst, src, v);
-                }
-                if (stid < T) {
-                    if (a.anc_mask != nullptr)
-                        S.anc[stid] = a.anc_mask[(int64_t)b * T + stid];
-                    else
-                        S.par[stid] = a.tree_parent[(int64_t)b * T + stid];
-                }
-                cp_async_wait_all();
-                asm volatile("bar.sync 1, 256;" ::: "memory");
-                if (stid == 0 && a.anc_mask == nullptr) bad |= build_anc_serial(S.par, T, S.anc);
-                if (half == 0) {
-                    const unsigned char* row = S.kring[0] + r * kQStageStride;
-#pragma unroll 1
-                    for (int c = 0; c < 8; ++c) {
-                        uint32_t w[32];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const uint4 v = *reinterpret_cast<const uint4*>(row + c * 128 + u * 16);
-                            w[4 * u] = v.x;
-                            w[4 * u + 1] = v.y;
-                            w[4 * u + 2] = v.z;
-                            w[4 * u + 3] = v.w;
-                        }
-                        tmem_st32(tbase + lb + kColQ + c * 32, w);
-                    }
-                    tmem_wait_st();
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                asm volatile("bar.sync 1, 256;" ::: "memory");
-                mbar_arrive(ba(S.q_ready));
-            }
-            const uint64_t anc_t = S.anc[t];
             const uint32_t sfree0 = mapa_shared(ba(S.s_free), 0);
             const uint32_t p_local = smem_u32(S.pstage);
             float* alpha_local = reinterpret_cast<float*>(S.pstage + kPBytes);
-            float m_ref = -INFINITY, l_part = 0.f;
+            const float sl = a.scale_log2;
             bool ok = true;
-            for (int i = 0; i < ntiles; ++i) {
-                if (!warp_wait(S.s_full, i & 1, abort_p)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                float sc[128];
+            int jt = 0, ne = 0;  // tiles and non-empty items so far
+            QuadItem it;
+            for (int k = 0; ok && quad_item(a, nrb, n_items, C, cid, k, it); ++k) {
+                if (it.ntiles <= 0) continue;
+                const int b = it.b;
+                const int row0 = it.rb * kRowsBlk + (int)hr * kMh;  // first request row of this CTA
+                const int grow = row0 + r;
+                const bool row_ok = grow < rows_req;
+                const int t = row_ok ? grow / H : 0;
+                // Q staging: latent dims into the K ring as eight 128-row x
+                // 64-dim swizzled blocks, RoPE dims straight into their
+                // swizzled A-operand tile. The previous item's MMAs are
+                // complete (its last S tile was waited for), so neither the
+                // ring nor TMEM's Q columns are still being read.
                 {
-                    uint32_t w[4][32];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) tmem_ld32(tbase + lb + kColS + half * 128 + c * 32, w[c]);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-#pragma unroll
-                        for (int u = 0; u < 32; ++u) sc[c * 32 + u] = __uint_as_float(w[c][u]);
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_remote(sfree0);
-                const int mi = i % kMetaRing;
-                if (!warp_wait(S.meta_full[mi], (i / kMetaRing) & 1, abort_p)) {
-                    ok = false;
-                    break;
-                }
-                uint32_t vw[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) vw[q] = row_ok ? S.valid[mi][4 * half + q] : 0u;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(ba(S.meta_free[mi]));
-                const int k0 = kb + i * kNT + 128 * half;
-                if (k0 + 128 > Lb) {  // this half reaches the tree keys
-#pragma unroll
-                    for (int c = 0; c < 128; ++c) {
-                        const int u = k0 + c - Lb;
-                        if (u >= 0 && !(u < T && ((anc_t >> u) & 1ull))) vw[c >> 5] &= ~(1u << (c & 31));
+                    const __nv_bfloat16* q0 = a.q + ((int64_t)b * rows_req + row0) * kDqk;
+                    for (int f = stid; f < kMh * (kDqk / 8); f += 256) {
+                        const int rr = f / (kDqk / 8), c = f % (kDqk / 8);
+                        const bool v = row0 + rr < rows_req;
+                        const __nv_bfloat16* src = v ? q0 + (int64_t)rr * kDqk + c * 8 : a.q;
+                        const uint32_t dst = c < 64 ? smem_u32(S.kring[c >> 3]) + sw128_offset(rr, c & 7)
+                                                    : smem_u32(S.q_rope) + sw128_offset(rr, c - 64);
+                        cp_async_16_zfill(dst, src, v);
                     }
-                }
-                // Max over the raw scores (the scale is positive, so scaling
-                // the max is exact); masked keys become -inf only where this
-                // row's half-tile has any.
-                float mx = -INFINITY;
-                if ((vw[0] & vw[1] & vw[2] & vw[3]) != 0xffffffffu) {
-#pragma unroll
-                    for (int c = 0; c < 128; ++c)
-                        if (!((vw[c >> 5] >> (c & 31)) & 1u)) sc[c] = -INFINITY;
-                }
-                {  // eight independent chains, then a tree
-                    float m8[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) m8[j] = sc[j];
-#pragma unroll
-                    for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], sc[c]);
-                    mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-                }
-                mx *= a.scale_log2;
-                S.mx[i & 1][half][r] = mx;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(ba(S.mx_bar[i & 1]));
-                if (!warp_wait(S.mx_bar[i & 1], (i >> 1) & 1, abort_p)) {
-                    ok = false;
-                    break;
-                }
-                const float mt = fmaxf(mx, S.mx[i & 1][half ^ 1][r]);
-                float alpha = 1.f;
-                if (mt > -INFINITY) {
-                    if (m_ref == -INFINITY) {
-                        m_ref = mt;
-                    } else if (mt > m_ref + kRescaleLog2) {
-                        alpha = ex2_approx(m_ref - mt);
-                        m_ref = mt;
-                        l_part *= alpha;
+                    if (stid < T) {
+                        if (a.anc_mask != nullptr)
+                            S.anc[stid] = a.anc_mask[(int64_t)b * T + stid];
+                        else
+                            S.par[stid] = a.tree_parent[(int64_t)b * T + stid];
                     }
-                }
-                // P (bf16) -> local staging tile (the O pair's A-operand layout),
-                // once the previous tile's P has been read out of it.
-                if (i >= 1 && !warp_wait(S.pstage_free, (i - 1) & 1, abort_p)) {
-                    ok = false;
-                    break;
-                }
-                // p = 2^(s * scale_log2 - m_ref) in one FMA per key; masked
-                // keys (-inf) give 2^-inf = 0; a row with no visible key yet
-                // (m_ref = -inf) writes zeros.
-                float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // eight chains
-                const float sl = a.scale_log2;
-                const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
-                const bool any = m_ref != -INFINITY;
+                    // The softmax warps meet on mbarriers (bounded waits), not
+                    // on a named barrier: a warp that gave up on a timed-out
+                    // wait must not leave the others blocked for good.
+                    cp_async_wait_all();
+                    mbar_arrive(ba(S.q_landed));
+                    if (!warp_wait(S.q_landed, ne & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    if (stid == 0 && a.anc_mask == nullptr) bad |= build_anc_serial(S.par, T, S.anc);
+                    if (half == 0) {
+#pragma unroll 1
+                        for (int c = 0; c < 8; ++c) {
+                            const unsigned char* blk = S.kring[c];
+                            uint32_t w[32];
 #pragma unroll
-                for (int blk = 0; blk < 2; ++blk) {
-                    const uint32_t pb = p_local + (2 * half + blk) * kPBlock;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int k = blk * 64 + c * 8 + 2 * u;
-                            const float p0 = any ? ex2_approx(fmaf(sc[k], sl, nm)) : 0.f;
-                            const float p1 = any ? ex2_approx(fmaf(sc[k + 1], sl, nm)) : 0.f;
-                            ps8[(c & 3) * 2 + (u & 1)] += p0 + p1;
-                            w[u] = pack_bf16x2(p0, p1);
+                            for (int u = 0; u < 8; ++u) {
+                                const uint4 v = *reinterpret_cast<const uint4*>(blk + sw128_offset(r, u));
+                                w[4 * u] = v.x;
+                                w[4 * u + 1] = v.y;
+                                w[4 * u + 2] = v.z;
+                                w[4 * u + 3] = v.w;
+                            }
+                            tmem_st32(tbase + lb + kColQ + c * 32, w);
                         }
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + sw128_offset(r, c)),
-                                     "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
-                                     : "memory");
+                        tmem_wait_st();
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    mbar_arrive(ba(S.q_ready));  // also orders the masks built above
+                    if (!warp_wait(S.q_ready, ne & 1, abort_p)) {
+                        ok = false;
+                        break;
                     }
                 }
-                l_part += ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
-                if (half == 0) alpha_local[r] = alpha;
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(ba(S.pw_bar[i & 1]));
-            }
-            if (ok) {
-                if (half == 0) {
-                    st_cluster_f32(mapa_shared(smem_u32(&sm.u.o.fin_m[r]), orank), m_ref);
-                    st_cluster_f32(mapa_shared(smem_u32(&sm.u.o.fin_l[0][r]), orank), l_part);
-                } else {
-                    st_cluster_f32(mapa_shared(smem_u32(&sm.u.o.fin_l[1][r]), orank), l_part);
+                const uint64_t anc_t = S.anc[t];
+                float m_ref = -INFINITY, l_part = 0.f;
+                for (int i = 0; i < it.ntiles; ++i, ++jt) {
+                    if (!warp_wait(S.s_full, jt & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    float sc[128];
+                    {
+                        uint32_t w[4][32];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) tmem_ld32(tbase + lb + kColS + half * 128 + c * 32, w[c]);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+#pragma unroll
+                            for (int u = 0; u < 32; ++u) sc[c * 32 + u] = __uint_as_float(w[c][u]);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_remote(sfree0);
+                    const int mi = jt % kMetaRing;
+                    if (!warp_wait(S.meta_full[mi], (jt / kMetaRing) & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    uint32_t vw[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) vw[q] = row_ok ? S.valid[mi][4 * half + q] : 0u;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(ba(S.meta_free[mi]));
+                    const int k0 = it.kb + i * kNT + 128 * half;
+                    if (k0 + 128 > it.Lb) {  // this half reaches the tree keys
+#pragma unroll
+                        for (int c = 0; c < 128; ++c) {
+                            const int u = k0 + c - it.Lb;
+                            if (u >= 0 && !(u < T && ((anc_t >> u) & 1ull))) vw[c >> 5] &= ~(1u << (c & 31));
+                        }
+                    }
+                    // Max over the raw scores (the scale is positive, so scaling
+                    // the max is exact); masked keys become -inf only where this
+                    // row's half-tile has any.
+                    float mx = -INFINITY;
+                    if ((vw[0] & vw[1] & vw[2] & vw[3]) != 0xffffffffu) {
+#pragma unroll
+                        for (int c = 0; c < 128; ++c)
+                            if (!((vw[c >> 5] >> (c & 31)) & 1u)) sc[c] = -INFINITY;
+                    }
+                    {  // eight independent chains, then a tree
+                        float m8[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) m8[j] = sc[j];
+#pragma unroll
+                        for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], sc[c]);
+                        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                    }
+                    mx *= sl;
+                    S.mx[jt & 1][half][r] = mx;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(ba(S.mx_bar[jt & 1]));
+                    if (!warp_wait(S.mx_bar[jt & 1], (jt >> 1) & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    const float mt = fmaxf(mx, S.mx[jt & 1][half ^ 1][r]);
+                    float alpha = 1.f;
+                    if (mt > -INFINITY) {
+                        if (m_ref == -INFINITY) {
+                            m_ref = mt;
+                        } else if (mt > m_ref + kRescaleLog2) {
+                            alpha = ex2_approx(m_ref - mt);
+                            m_ref = mt;
+                            l_part *= alpha;
+                        }
+                    }
+                    // P (bf16) -> local staging tile (the O pair's A-operand
+                    // layout), once the previous tile's P has been read out of it.
+                    if (jt >= 1 && !warp_wait(S.pstage_free, (jt - 1) & 1, abort_p)) {
+                        ok = false;
+                        break;
+                    }
+                    // p = 2^(s * scale_log2 - m_ref) in one FMA per key; masked
+                    // keys (-inf) give 2^-inf = 0; a row with no visible key yet
+                    // (m_ref = -inf) writes zeros.
+                    float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // eight chains
+                    const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
+                    const bool any = m_ref != -INFINITY;
+#pragma unroll
+                    for (int blk = 0; blk < 2; ++blk) {
+                        const uint32_t pb = p_local + (2 * half + blk) * kPBlock;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int kk = blk * 64 + c * 8 + 2 * u;
+                                const float p0 = any ? ex2_approx(fmaf(sc[kk], sl, nm)) : 0.f;
+                                const float p1 = any ? ex2_approx(fmaf(sc[kk + 1], sl, nm)) : 0.f;
+                                ps8[(c & 3) * 2 + (u & 1)] += p0 + p1;
+                                w[u] = pack_bf16x2(p0, p1);
+                            }
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + sw128_offset(r, c)),
+                                         "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                                         : "memory");
+                        }
+                    }
+                    l_part += ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
+                    if (half == 0) alpha_local[r] = alpha;
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(ba(S.pw_bar[jt & 1]));
                 }
-                mbar_arrive_cluster(mapa_shared(ba(sm.u.o.fin), orank));
+                if (!ok) break;
+                // The item's row maxima and sums go to the O partner's slot of
+                // this item's parity, once the partner has read what the item
+                // two before left there.
+                const int fs = ne & 1;
+                if (ne >= 2 && !warp_wait(S.fin_free[fs], ((ne - 2) >> 1) & 1, abort_p)) {
+                    ok = false;
+                    break;
+                }
+                if (half == 0) {
+                    st_cluster_f32(mapa_shared(smem_u32(&sm.u.o.fin_m[fs][r]), orank), m_ref);
+                    st_cluster_f32(mapa_shared(smem_u32(&sm.u.o.fin_l[fs][0][r]), orank), l_part);
+                } else {
+                    st_cluster_f32(mapa_shared(smem_u32(&sm.u.o.fin_l[fs][1][r]), orank), l_part);
+                }
+                mbar_arrive_cluster(mapa_shared(ba(sm.u.o.fin[fs]), orank));
+                ++ne;
             }
         }
     } else if (wg != 2) {
@@ -628,60 +737,77 @@ partial_quad_kernel(const PartialArgs a) {
             // CTA's four 64-dim segments (eight lanes per 128-byte segment).
             const int pw = warp < kWarpMMA ? warp : (warp < 8 ? warp - 1 : warp - 6);  // 0..13
             bool ok = true;
-            for (int i = 0; ok && i < ntiles; ++i) {
-                const int rs = i % kRowsRing;
-                if (!warp_wait(O.rows_full[rs], (i / kRowsRing) & 1, abort_p)) {
-                    ok = false;
-                    break;
-                }
-                for (int q = 0; q < kNT / kVKeys; ++q) {
-                    const int g = i * (kNT / kVKeys) + q;
-                    const int st = g % kVStages;
-                    if (g >= kVStages && !warp_wait(O.v_empty[st], ((g / kVStages) - 1) & 1, abort_p)) {
+            int jt = 0;  // tiles so far
+            QuadItem it;
+            for (int k = 0; ok && quad_item(a, nrb, n_items, C, cid, k, it); ++k) {
+                for (int i = 0; ok && i < it.ntiles; ++i, ++jt) {
+                    const int rs = jt % kRowsRing;
+                    if (!warp_wait(O.rows_full[rs], (jt / kRowsRing) & 1, abort_p)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t dst0 = smem_u32(O.vring[st]);
-                    for (int it = pw; it < kVKeys * 4 * 8 / 32; it += kOProd) {
-                        const int idx = it * 32 + lane;
-                        const int chunk = idx & 7, pair = idx >> 3;
-                        const int kl = pair >> 2, sel = pair & 3;   // key in stage; (chain, segment)
-                        const int seg = 4 * (sel >> 1) + 2 * (int)hr + (sel & 1);
-                        const int32_t slot = O.rows[rs][kVKeys * q + kl];
-                        const __nv_bfloat16* src =
-                            a.kv + (slot >= 0 ? (int64_t)slot * kDqk : 0) + seg * 64 + chunk * 8;
-                        cp_async_16_zfill_nc(dst0 + sel * kVSub + sw128_offset(kl, chunk), src, slot >= 0);
+                    for (int q = 0; q < kNT / kVKeys; ++q) {
+                        const int g = jt * (kNT / kVKeys) + q;
+                        const int st = g % kVStages;
+                        if (g >= kVStages && !warp_wait(O.v_empty[st], ((g / kVStages) - 1) & 1, abort_p)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t dst0 = smem_u32(O.vring[st]);
+                        for (int x = pw; x < kVKeys * 4 * 8 / 32; x += kOProd) {
+                            const int idx = x * 32 + lane;
+                            const int chunk = idx & 7, pair = idx >> 3;
+                            const int kl = pair >> 2, sel = pair & 3;   // key in stage; (chain, segment)
+                            const int seg = 4 * (sel >> 1) + 2 * (int)hr + (sel & 1);
+                            const int32_t slot = O.rows[rs][kVKeys * q + kl];
+                            const __nv_bfloat16* src =
+                                a.kv + (slot >= 0 ? (int64_t)slot * kDqk : 0) + seg * 64 + chunk * 8;
+                            cp_async_16_zfill_nc(dst0 + sel * kVSub + sw128_offset(kl, chunk), src, slot >= 0);
+                        }
+                        cp_async_mbar_arrive_noinc(ba(O.v_full[st]));
                     }
-                    cp_async_mbar_arrive_noinc(ba(O.v_full[st]));
+                    if (!ok) break;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(ba(O.rows_free[rs]));
                 }
-                if (!ok) break;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(ba(O.rows_free[rs]));
             }
             cp_async_wait_all();
         } else if (warp == kWarpCtl) {
             // ------------------------------------------------ tile rows + P slot release
             // The warp stages each tile's pool rows two tiles ahead of the
-            // copies; on rank 2, lane 0 frees P slots: once P V of tile i is
-            // complete, its slot may take tile i + 2.
-            auto stage = [&](int j) -> bool {
+            // copies, across item boundaries; on rank 2, lane 0 frees P
+            // slots: once P V of tile j is complete, its slot may take tile
+            // j + 2.
+            TileCursor cur;
+            cursor_init(cur);
+            int staged = 0;
+            auto stage_next = [&]() -> int {  // 1: staged, 0: no tile left, -1: timed out
+                if (!cursor_next(cur, a, nrb, n_items, C, cid)) return 0;
+                const int j = staged;
                 const int rs = j % kRowsRing;
                 if (j >= kRowsRing && !warp_wait(O.rows_free[rs], ((j / kRowsRing) - 1) & 1, abort_p))
-                    return false;
-                (void)stage_rows(a, kbase, kb + j * kNT, ke, lane, O.rows[rs], nullptr);
+                    return -1;
+                (void)stage_rows(a, a.kv_indptr[cur.it.b], cur.it.kb + cur.i * kNT, cur.it.ke, lane,
+                                 O.rows[rs], nullptr);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ba(O.rows_full[rs]));
-                return true;
+                ++staged;
+                return 1;
             };
-            bool ok = stage(0) && (ntiles < 2 || stage(1));
-            for (int i = 0; ok && i < ntiles; ++i) {
-                if (i + 2 < ntiles && !stage(i + 2)) break;
+            int more = stage_next();
+            if (more > 0) more = stage_next();
+            bool ok = more >= 0;
+            for (int j = 0; ok && j < staged; ++j) {
+                if (more > 0) {
+                    more = stage_next();
+                    if (more < 0) break;
+                }
                 int rel = 1;
-                if (rank == 2 && lane == 0 && i + 2 < ntiles) {
-                    rel = mbar_wait_spin(ba(O.o_done[i & 1]), (i >> 1) & 1, abort_p);
+                if (rank == 2 && lane == 0 && j + 2 < staged) {
+                    rel = mbar_wait_spin(ba(O.o_done[j & 1]), (j >> 1) & 1, abort_p);
                     if (rel) {
-                        mbar_arrive_remote(mapa_shared(ba(sm.u.s.p_free[i & 1]), 0));
-                        mbar_arrive_remote(mapa_shared(ba(sm.u.s.p_free[i & 1]), 1));
+                        mbar_arrive_remote(mapa_shared(ba(sm.u.s.p_free[j & 1]), 0));
+                        mbar_arrive_remote(mapa_shared(ba(sm.u.s.p_free[j & 1]), 1));
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, rel, 0) != 0;
@@ -695,42 +821,45 @@ partial_quad_kernel(const PartialArgs a) {
                 const uint64_t vdesc0 = make_sdesc(smem_u32(O.vring[0]), kVSub, 1024, kSwizzle128B);
                 const uint32_t vfull0 = ba(O.v_full[0]), vempty0 = ba(O.v_empty[0]);
                 const uint32_t d0 = tbase, d1 = tbase + 256;
-                int st = 0;
+                int st = 0, jt = 0;
                 uint32_t ph = 0;
                 bool ok = true;
-                for (int i = 0; ok && i < ntiles; ++i) {
-                    const int slot = i & 1;
-                    if (!mbar_wait_spin(ba(O.o_gate[slot]), (i >> 1) & 1, abort_p)) {
-                        ok = false;
-                        break;
-                    }
-                    fence_proxy_async_smem();
-                    tc_fence_after();
-                    const uint64_t pd = pdesc0 + (uint64_t)(slot * (kPSlot >> 4));
-#pragma unroll 1
-                    for (int q = 0; q < kNT / kVKeys; ++q) {
-                        if (!mbar_wait_spin(vfull0 + 8 * st, ph, abort_p)) {
+                QuadItem it;
+                for (int k = 0; ok && quad_item(a, nrb, n_items, C, cid, k, it); ++k) {
+                    for (int i = 0; ok && i < it.ntiles; ++i, ++jt) {
+                        const int slot = jt & 1;
+                        if (!mbar_wait_spin(ba(O.o_gate[slot]), (jt >> 1) & 1, abort_p)) {
                             ok = false;
                             break;
                         }
                         fence_proxy_async_smem();
                         tc_fence_after();
-                        const uint64_t vd = vdesc0 + (uint64_t)(st * (kVStage >> 4));
-                        // keys q*32 .. q*32+31 of the tile: P block q/2, 32-byte K steps
-                        const uint64_t ad = pd + (uint64_t)((q >> 1) * (kPBlock >> 4) + (q & 1) * 4);
-                        const uint32_t acc0 = (i > 0 || q > 0) ? 1u : 0u;
-                        mma_ss_pair(d0, ad, vd, idesc, acc0);
-                        mma_ss_pair(d1, ad, vd + (2 * kVSub >> 4), idesc, acc0);
-                        mma_ss_pair(d0, ad + 2, vd + (2048 >> 4), idesc, 1u);
-                        mma_ss_pair(d1, ad + 2, vd + ((2 * kVSub + 2048) >> 4), idesc, 1u);
-                        mma_commit_pair_mc(vempty0 + 8 * st, 0xC);
-                        if (++st == kVStages) {
-                            st = 0;
-                            ph ^= 1u;
+                        const uint64_t pd = pdesc0 + (uint64_t)(slot * (kPSlot >> 4));
+#pragma unroll 1
+                        for (int q = 0; q < kNT / kVKeys; ++q) {
+                            if (!mbar_wait_spin(vfull0 + 8 * st, ph, abort_p)) {
+                                ok = false;
+                                break;
+                            }
+                            fence_proxy_async_smem();
+                            tc_fence_after();
+                            const uint64_t vd = vdesc0 + (uint64_t)(st * (kVStage >> 4));
+                            // keys q*32 .. q*32+31 of the tile: P block q/2, 32-byte K steps
+                            const uint64_t ad = pd + (uint64_t)((q >> 1) * (kPBlock >> 4) + (q & 1) * 4);
+                            const uint32_t acc0 = (i > 0 || q > 0) ? 1u : 0u;  // each item starts afresh
+                            mma_ss_pair(d0, ad, vd, idesc, acc0);
+                            mma_ss_pair(d1, ad, vd + (2 * kVSub >> 4), idesc, acc0);
+                            mma_ss_pair(d0, ad + 2, vd + (2048 >> 4), idesc, 1u);
+                            mma_ss_pair(d1, ad + 2, vd + ((2 * kVSub + 2048) >> 4), idesc, 1u);
+                            mma_commit_pair_mc(vempty0 + 8 * st, 0xC);
+                            if (++st == kVStages) {
+                                st = 0;
+                                ph ^= 1u;
+                            }
                         }
+                        if (!ok) break;
+                        mma_commit_pair_mc(ba(O.o_done[slot]), 0xC);
                     }
-                    if (!ok) break;
-                    mma_commit_pair_mc(ba(O.o_done[slot]), 0xC);
                 }
                 mma_commit_pair_mc(ba(sm.h.drain), 0x4);
                 mbar_wait(ba(sm.h.drain), 0, &sm.h.no_abort);
@@ -738,12 +867,20 @@ partial_quad_kernel(const PartialArgs a) {
         } else {
             // ------------------------------------------------ rank 3: forward V readiness to rank 2
             if (lane == 0) {
-                const int nfill = ntiles * (kNT / kVKeys);
-                for (int g = 0; g < nfill; ++g) {
-                    const int st = g % kVStages;
-                    if (!mbar_wait_spin(ba(O.v_full[st]), (g / kVStages) & 1, abort_p)) break;
-                    fence_proxy_async_smem();
-                    mbar_arrive_remote(mapa_shared(ba(O.v_full[st]), 2));
+                int g = 0;
+                bool ok = true;
+                QuadItem it;
+                for (int k = 0; ok && quad_item(a, nrb, n_items, C, cid, k, it); ++k) {
+                    const int gend = g + it.ntiles * (kNT / kVKeys);
+                    for (; g < gend; ++g) {
+                        const int st = g % kVStages;
+                        if (!mbar_wait_spin(ba(O.v_full[st]), (g / kVStages) & 1, abort_p)) {
+                            ok = false;
+                            break;
+                        }
+                        fence_proxy_async_smem();
+                        mbar_arrive_remote(mapa_shared(ba(O.v_full[st]), 2));
+                    }
                 }
             }
         }
@@ -754,54 +891,72 @@ partial_quad_kernel(const PartialArgs a) {
             // ------------------------------------------------ correction + epilogue
             const int quarter = warp & 3;
             const int r = 32 * quarter + lane;
-            const int grow = row0 + r;
-            const bool row_ok = grow < rows_req;
             const uint32_t lb = (uint32_t)(32 * quarter) << 16;
+            const uint32_t srank = hr;  // S partner holding the same rows
+            float* tile = O.otile[quarter];
+            const int jr = lane >> 3, jc = 4 * (lane & 7);  // row in a group of 4, column
+            const int64_t gstep = (int64_t)4 * a.nsplit * kDv;  // four rows on
             bool ok = true;
-            for (int i = 0; i < ntiles; ++i) {
-                const int slot = i & 1;
-                if (!warp_wait(O.p_full[slot], (i >> 1) & 1, abort_p)) {
-                    ok = false;
-                    break;
+            int jt = 0, ne = 0;  // tiles and non-empty items so far
+            QuadItem it;
+            for (int k = 0; ok && quad_item(a, nrb, n_items, C, cid, k, it); ++k) {
+                const int row0 = it.rb * kRowsBlk + (int)hr * kMh;
+                const int grow = row0 + r;
+                const bool row_ok = grow < rows_req;
+                if (it.ntiles <= 0) {  // empty split: lse = -inf, o = 0
+                    if (row_ok) {
+                        const int64_t pid = ((int64_t)it.b * rows_req + grow) * a.nsplit + it.s;
+                        float4* o = reinterpret_cast<float4*>(a.o_part + pid * kDv);
+                        for (int c = 0; c < kDv / 4; ++c) o[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        a.lse_part[pid] = -INFINITY;
+                    }
+                    continue;
                 }
-                const float alpha = reinterpret_cast<const float*>(O.pbuf[slot] + kPBytes)[r];
-                if (__any_sync(0xffffffffu, alpha != 1.f) && i > 0) {
-                    if (!warp_wait(O.o_done[slot ^ 1], ((i - 1) >> 1) & 1, abort_p)) {
+                for (int i = 0; i < it.ntiles; ++i, ++jt) {
+                    const int slot = jt & 1;
+                    if (!warp_wait(O.p_full[slot], (jt >> 1) & 1, abort_p)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
+                    const float alpha = reinterpret_cast<const float*>(O.pbuf[slot] + kPBytes)[r];
+                    if (__any_sync(0xffffffffu, alpha != 1.f) && i > 0) {
+                        if (!warp_wait(O.o_done[slot ^ 1], ((jt - 1) >> 1) & 1, abort_p)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
 #pragma unroll 1
-                    for (int c0 = 0; c0 < 512; c0 += 32) {
-                        uint32_t o[32];
-                        tmem_ld32(tbase + lb + c0, o);
-                        tmem_wait_ld();
+                        for (int c0 = 0; c0 < 512; c0 += 32) {
+                            uint32_t o[32];
+                            tmem_ld32(tbase + lb + c0, o);
+                            tmem_wait_ld();
 #pragma unroll
-                        for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
-                        tmem_st32(tbase + lb + c0, o);
+                            for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
+                            tmem_st32(tbase + lb + c0, o);
+                        }
+                        tmem_wait_st();
                     }
-                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_remote(mapa_shared(ba(O.o_gate[slot]), 2));
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_remote(mapa_shared(ba(O.o_gate[slot]), 2));
-            }
-            if (ok) ok = warp_wait_cluster(O.fin, 0, abort_p);
-            if (ok) ok = warp_wait(O.o_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort_p);
-            tc_fence_after();
-            if (ok) {
-                const float l = O.fin_l[0][r] + O.fin_l[1][r];
+                if (!ok) break;
+                const int fs = ne & 1;
+                ok = warp_wait_cluster(O.fin[fs], (ne >> 1) & 1, abort_p) &&
+                     warp_wait(O.o_done[(jt - 1) & 1], ((jt - 1) >> 1) & 1, abort_p);
+                if (!ok) break;
+                tc_fence_after();
+                const float l = O.fin_l[fs][0][r] + O.fin_l[fs][1][r];
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-                const int64_t pid = ((int64_t)b * rows_req + (row_ok ? grow : 0)) * a.nsplit + s;
+                const float lse = l > 0.f ? (O.fin_m[fs][r] + log2f(l)) * kLn2 : -INFINITY;
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(mapa_shared(ba(sm.u.s.fin_free[fs]), srank));
                 // Coalesced partial write: each 32-row x 32-column chunk goes
-                // through a padded tile in the (now idle) V ring and out again
-                // with eight lanes per row, so every store instruction writes
-                // four whole 128-byte lines instead of 32 lines in part.
-                float* tile = reinterpret_cast<float*>(O.vring[0]) + quarter * (32 * kOTileStride);
-                const int jr = lane >> 3, jc = 4 * (lane & 7);  // row in a group of 4, column
-                const int rj0 = row0 + 32 * quarter + jr;          // this lane's row of group 0
-                float* const o0 = a.o_part + (((int64_t)b * rows_req + rj0) * a.nsplit + s) * kDv + jc;
-                const int64_t gstep = (int64_t)4 * a.nsplit * kDv;   // four rows on
+                // through a padded tile and out again with eight lanes per
+                // row, so every store instruction writes four whole 128-byte
+                // lines instead of 32 lines in part.
+                const int rj0 = row0 + 32 * quarter + jr;  // this lane's row of group 0
+                float* const o0 = a.o_part + (((int64_t)it.b * rows_req + rj0) * a.nsplit + it.s) * kDv + jc;
 #pragma unroll 1
                 for (int c0 = 0; c0 < 512; c0 += 32) {
                     uint32_t o[32];
@@ -821,8 +976,8 @@ partial_quad_kernel(const PartialArgs a) {
                     }
                     __syncwarp();
                 }
-                if (row_ok)
-                    a.lse_part[pid] = l > 0.f ? (O.fin_m[r] + log2f(l)) * kLn2 : -INFINITY;
+                if (row_ok) a.lse_part[((int64_t)it.b * rows_req + grow) * a.nsplit + it.s] = lse;
+                ++ne;
             }
         }
     }
@@ -840,7 +995,7 @@ partial_quad_kernel(const PartialArgs a) {
 
 }  // namespace
 
-// Resident 4-CTA clusters per device, for the wave shaping of the partitions.
+// Resident 4-CTA clusters per device: the persistent launch's cluster count.
 int g_quad_clusters[64];
 
 cudaError_t setup_partial_quad() {
@@ -856,7 +1011,7 @@ cudaError_t setup_partial_quad() {
     cfg.dynamicSmemBytes = kSmemBytes;
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, partial_quad_kernel, &cfg) != cudaSuccess) {
-        (void)cudaGetLastError();  // unknown: plain even partitions
+        (void)cudaGetLastError();  // unknown: one cluster per item
         n = 0;
     }
     g_quad_clusters[dev] = n;
@@ -866,13 +1021,15 @@ cudaError_t setup_partial_quad() {
 cudaError_t launch_partial_quad(const PartialArgs& a, cudaStream_t stream) {
     const int rows_req = a.T * a.H;
     const int nrb = (rows_req + kRowsBlk - 1) / kRowsBlk;
-    dim3 grid(4 * nrb, a.batch, a.nsplit);
+    const long long items = (long long)a.batch * a.nsplit * nrb;
+    if (items <= 0 || items > (1ll << 30)) return cudaErrorInvalidValue;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+    const int resident = dev >= 0 && dev < 64 ? g_quad_clusters[dev] : 0;
+    const int clusters = resident > 0 && resident < items ? resident : (int)items;
     PartialArgs w = a;
-    w.wave_full = wave_full_items((long long)a.batch * a.nsplit * nrb,
-                                  dev >= 0 && dev < 64 ? g_quad_clusters[dev] : 0);
-    partial_quad_kernel<<<grid, kThreads, kSmemBytes, stream>>>(w);
+    w.wave_full = wave_full_items(items, clusters);
+    partial_quad_kernel<<<dim3(4 * clusters, 1, 1), kThreads, kSmemBytes, stream>>>(w);
     return cudaGetLastError();
 }
 

@@ -71,6 +71,10 @@ CASES = [
     (3, 8, [0, 129, 5], 33, "star", 64),    # 264 rows: 8 rows in the last block; empty splits
     (1, 3, [2500], 43, "random", 11),       # 129 rows: one row past the two-SM kernel's range
     (1, 64, [0], 64, "chain", 4),           # 4096 rows, no prefix, maximum tree
+    # more four-SM work items than resident clusters: each persistent cluster
+    # walks several items of different requests, row blocks and lengths
+    (6, 32, [1500, 0, 17, 4000, 260, 2500], 16, "random", 8),
+    (2, 16, [20000, 100], 32, "random", 48),
 ]
 
 
@@ -78,8 +82,8 @@ CASES = [
 @pytest.mark.parametrize("case", CASES, ids=[f"c{i}" for i in range(len(CASES))])
 def test_edge_cases(case, flags):
     B, H, L, T, tree, ns = case
-    inp = make_inputs(batch=B, num_heads=H, prefix=L, T=T, tree=tree, pool_slots=16384,
-                      nsplit=ns, seed=sum(L) + T)
+    inp = make_inputs(batch=B, num_heads=H, prefix=L, T=T, tree=tree,
+                      pool_slots=max(16384, 2 * (sum(L) + B * T)), nsplit=ns, seed=sum(L) + T)
     d = run_gpu(inp, flags=flags)
     assert status(d) == 0
     out, lse = host_out(d)
