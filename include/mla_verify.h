@@ -162,10 +162,12 @@ int mla_build_verify_meta(const int32_t *req_to_token, int64_t req_to_token_stri
  *   tree_parent  int32 [batch][T] (visibility is built in-kernel from it)
  *   T            tree tokens per request, 1..64
  *   nsplit       KV partitions per request, 1..128: request b's L_b + T keys
- *                are cut into nsplit contiguous ranges of ceil((L_b+T)/nsplit)
- *                keys; each range gives one partial result per query row and
- *                empty ranges give lse = -inf ([VK] Part VII: NSPLIT multiplies
- *                the number of partials)
+ *                are cut into at most nsplit contiguous ranges (the pages cut
+ *                ceil((L_b+T)/nsplit)-key chunks; the kernels cut at 256-key
+ *                tiles and balance the ranges over the SMs); each range gives
+ *                one partial result per query row and empty ranges give
+ *                lse = -inf ([VK] Part VII: NSPLIT multiplies the number of
+ *                partials)
  *   workspace    device buffer of >= mla_verify_workspace_bytes(batch, T,
  *                num_heads, nsplit) bytes, 256-byte aligned; holds the status
  *                word and the partials; contents need no initialisation
@@ -198,7 +200,9 @@ int mla_verify_attention_anc(const void *q, const void *kv_pool, const int32_t *
  *   lse_part[n*nsplit + s]          fp32, natural-log partition sum of the
  *                                   split's visible keys (-inf if none)
  *   o_part[(n*nsplit + s)*512 + d]  fp32, that split's softmax-weighted V
- *                                   (normalised within the split; 0 if none)
+ *                                   (normalised within the split); where
+ *                                   lse_part is -inf its contents are
+ *                                   unspecified (not read by the combine)
  * at workspace + 256 (lse_part, padded to 256 bytes) and right after it
  * (o_part). Exactly one of tree_parent / anc_mask must be non-NULL.
  * flags: 0 = default kernel (tensor cores: for requests with more than 128

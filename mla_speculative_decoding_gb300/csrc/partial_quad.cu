@@ -120,11 +120,15 @@ struct SmemO {
     uint64_t p_full[2], o_gate[2], o_done[2], fin[2];
     uint64_t rows_full[kRowsRing], rows_free[kRowsRing];
 };
+constexpr int kPlanMaxReq = 128;  // requests the balanced plan tabulates
 struct Header {
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
     int no_abort;
+    int balanced;                       // 1: balanced tile ranges, 0: rotated rounds
+    int w;                              // balanced: tiles over all (request, row block)
+    int ptile[kPlanMaxReq + 1];         // balanced: first tile of request b (row block 0)
 };
 struct __align__(1024) SmemQuad {
     union {
@@ -188,9 +192,11 @@ struct QuadItem {
     int b, s, rb, kb, ke, ntiles, Lb, bad;
 };
 
-// Item k of cluster `cid` of `C`: round k, position (cid + k) mod C; false
-// past the last item. Items are numbered partition-major, ((s * batch + b) *
-// nrb + rb), so every request's first partitions come first.
+// Rotated rounds (the fallback plan): item k of cluster `cid` of `C` is the
+// item at position (cid + k) mod C of round k; false past the last item.
+// Items are numbered partition-major, ((s * batch + b) * nrb + rb), so every
+// request's first partitions come first, and the partitions are the
+// wave-shaped split of the request's tiles.
 __device__ __forceinline__ bool quad_item(const PartialArgs& a, int nrb, int n_items, int C, int cid,
                                           int k, QuadItem& it) {
     const long long j = (long long)k * C + (cid + k) % C;
@@ -207,25 +213,110 @@ __device__ __forceinline__ bool quad_item(const PartialArgs& a, int nrb, int n_i
     return true;
 }
 
-// The cluster's tiles in order over its non-empty items.
-struct TileCursor {
-    QuadItem it;
-    int k, i, bad;
+// Built by one warp of every CTA (all CTAs reach the same plan): the first
+// tile of each request and the choice of plan. The balanced plan (the key
+// tiles of all (request, row block) pairs cut into one contiguous range per
+// cluster, each cluster's part of a pair one partition of it) needs at most
+// kPlanMaxReq requests and plan_fits; otherwise the rotated rounds run.
+// (Not inlined: its registers stay out of the roles' budgets; it takes the
+// few arguments it reads by value so that the kernel parameters stay in
+// parameter space.)
+__device__ __noinline__ void build_plan(const int32_t* prefix_lens, const int32_t* kv_indptr, int batch,
+                                        int T, int nsplit, int nrb, int C, int lane, Header& h) {
+    PartialArgs a;
+    a.prefix_lens = prefix_lens;
+    a.kv_indptr = kv_indptr;
+    a.batch = batch;
+    a.T = T;
+    a.nsplit = nsplit;
+    if (a.batch > kPlanMaxReq) {
+        if (lane == 0) h.balanced = 0;
+        return;
+    }
+    long long run = 0;
+    int tmax = 0;
+    for (int b0 = 0; b0 < a.batch; b0 += 32) {
+        const int b = b0 + lane;
+        int t = 0;
+        if (b < a.batch) {
+            int Lb, K;
+            (void)request_keys(a, b, Lb, K);
+            t = (K + kNT - 1) / kNT;
+        }
+        tmax = max(tmax, t);
+        int incl = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (b < a.batch) h.ptile[b] = (int)min(run + (long long)(incl - t) * nrb, 1ll << 30);
+        run += (long long)__shfl_sync(0xffffffffu, incl, 31) * nrb;
+    }
+    tmax = __reduce_max_sync(0xffffffffu, tmax);
+    if (lane == 0) {
+        const bool fits = plan_fits(run, tmax, C, a.nsplit);
+        h.ptile[a.batch] = fits ? (int)run : 0;
+        h.w = fits ? (int)run : 0;
+        h.balanced = fits ? 1 : 0;
+    }
+}
+
+// A cluster's walk over its items under either plan.
+struct ItemWalk {
+    int x, xend;        // balanced: the cluster's next tile and the end of its range
+    int b;              // balanced: request holding tile x
+    int k;              // rotated rounds: next round
 };
-__device__ __forceinline__ void cursor_init(TileCursor& c) {
-    c.k = 0;
+__device__ __forceinline__ ItemWalk walk_init(const Header& h, int cid, int C) {
+    ItemWalk w;
+    w.k = 0;
+    w.b = 0;
+    w.x = h.balanced ? plan_begin(cid, C, h.w) : 0;
+    w.xend = h.balanced ? plan_begin(cid + 1, C, h.w) : 0;
+    return w;
+}
+__device__ __forceinline__ bool walk_next(ItemWalk& w, const PartialArgs& a, const Header& h, int nrb,
+                                          int n_items, int C, int cid, QuadItem& it) {
+    if (!h.balanced) return quad_item(a, nrb, n_items, C, cid, w.k++, it);
+    if (w.x >= w.xend) return false;
+    int u0, u1;
+    const int n = plan_step(h.ptile, nrb, C, h.w, cid, w.x, w.xend, w.b, it.rb, u0, u1, it.s);
+    it.b = w.b;
+    int K;
+    it.bad = request_keys(a, it.b, it.Lb, K);
+    it.kb = u0 * kNT;
+    it.ke = min(K, u1 * kNT);
+    it.ntiles = n;
+    w.x += n;
+    return true;
+}
+
+// The cluster's tiles in order over its non-empty items (what the row
+// staging needs of each: request, key range, tile count).
+struct TileCursor {
+    ItemWalk w;
+    int b, kb, ke, ntiles, i, bad;
+};
+__device__ __forceinline__ void cursor_init(TileCursor& c, const Header& h, int cid, int C) {
+    c.w = walk_init(h, cid, C);
     c.i = 0;
-    c.it.ntiles = 0;
+    c.ntiles = 0;
     c.bad = 0;
 }
 // Moves to the next tile; false past the last one.
-__device__ __forceinline__ bool cursor_next(TileCursor& c, const PartialArgs& a, int nrb, int n_items,
-                                            int C, int cid) {
-    if (++c.i < c.it.ntiles) return true;
+__device__ __forceinline__ bool cursor_next(TileCursor& c, const PartialArgs& a, const Header& h, int nrb,
+                                            int n_items, int C, int cid) {
+    if (++c.i < c.ntiles) return true;
     for (;;) {
-        if (!quad_item(a, nrb, n_items, C, cid, c.k++, c.it)) return false;
-        c.bad |= c.it.bad;
-        if (c.it.ntiles > 0) {
+        QuadItem it;
+        if (!walk_next(c.w, a, h, nrb, n_items, C, cid, it)) return false;
+        c.bad |= it.bad;
+        if (it.ntiles > 0) {
+            c.b = it.b;
+            c.kb = it.kb;
+            c.ke = it.ke;
+            c.ntiles = it.ntiles;
             c.i = 0;
             return true;
         }
@@ -251,6 +342,7 @@ partial_quad_kernel(const PartialArgs a) {
         tmem_alloc_pair(smem_u32(&sm.h.tmem_base), 512);
         tmem_relinquish_pair();
     }
+    if (warp == 1) build_plan(a.prefix_lens, a.kv_indptr, a.batch, T, a.nsplit, nrb, C, lane, sm.h);
     if (tid == 0) {
         mbar_init(ba(sm.h.drain), 1);
         if (sside) {
@@ -323,7 +415,7 @@ partial_quad_kernel(const PartialArgs a) {
             bool ok = true;
             int g0 = 0, j0 = 0, ne = 0;  // fills, tiles and non-empty items so far
             QuadItem it;
-            for (int k = 0; ok && quad_item(a, nrb, n_items, C, cid, k, it); ++k) {
+            for (ItemWalk wk = walk_init(sm.h, cid, C); ok && walk_next(wk, a, sm.h, nrb, n_items, C, cid, it);) {
                 if (it.ntiles <= 0) continue;
                 ok = warp_wait(S.q_ready, ne & 1, abort_p);  // the ring doubles as Q staging
                 const int nfill = it.ntiles * kFills;
@@ -373,15 +465,15 @@ partial_quad_kernel(const PartialArgs a) {
             // rows are free as well.
             static_assert(kRowsRing == kMetaRing, "rows and metadata share the release");
             TileCursor cur;
-            cursor_init(cur);
+            cursor_init(cur, sm.h, cid, C);
             int staged = 0;
             auto stage_next = [&]() -> int {  // 1: staged, 0: no tile left, -1: timed out
-                if (!cursor_next(cur, a, nrb, n_items, C, cid)) return 0;
+                if (!cursor_next(cur, a, sm.h, nrb, n_items, C, cid)) return 0;
                 const int j = staged;
                 const int rs = j % kRowsRing, mi = j % kMetaRing;
                 if (j >= kMetaRing && !warp_wait(S.meta_free[mi], ((j / kMetaRing) - 1) & 1, abort_p))
                     return -1;
-                bad |= stage_rows(a, a.kv_indptr[cur.it.b], cur.it.kb + cur.i * kNT, cur.it.ke, lane,
+                bad |= stage_rows(a, a.kv_indptr[cur.b], cur.kb + cur.i * kNT, cur.ke, lane,
                                   S.rows[rs], S.valid[mi]);
                 __syncwarp();
                 if (lane == 0) {
@@ -438,7 +530,7 @@ partial_quad_kernel(const PartialArgs a) {
                 uint32_t ph = 0;
                 bool ok = true;
                 QuadItem it;
-                for (int k = 0; ok && quad_item(a, nrb, n_items, C, cid, k, it); ++k) {
+                for (ItemWalk wk = walk_init(sm.h, cid, C); ok && walk_next(wk, a, sm.h, nrb, n_items, C, cid, it);) {
                     if (it.ntiles <= 0) continue;
                     ok = mbar_wait_spin(ba(S.q_ready), ne & 1, abort_p) &&
                          mbar_wait_spin(ba(S.q_peer), ne & 1, abort_p);
@@ -493,7 +585,7 @@ partial_quad_kernel(const PartialArgs a) {
                 int g = 0, ne = 0;
                 bool ok = true;
                 QuadItem it;
-                for (int k = 0; ok && quad_item(a, nrb, n_items, C, cid, k, it); ++k) {
+                for (ItemWalk wk = walk_init(sm.h, cid, C); ok && walk_next(wk, a, sm.h, nrb, n_items, C, cid, it);) {
                     if (it.ntiles <= 0) continue;
                     ok = mbar_wait_spin(ba(S.q_ready), ne & 1, abort_p);
                     tc_fence_after();
@@ -532,7 +624,7 @@ partial_quad_kernel(const PartialArgs a) {
             bool ok = true;
             int jt = 0, ne = 0;  // tiles and non-empty items so far
             QuadItem it;
-            for (int k = 0; ok && quad_item(a, nrb, n_items, C, cid, k, it); ++k) {
+            for (ItemWalk wk = walk_init(sm.h, cid, C); ok && walk_next(wk, a, sm.h, nrb, n_items, C, cid, it);) {
                 if (it.ntiles <= 0) continue;
                 const int b = it.b;
                 const int row0 = it.rb * kRowsBlk + (int)hr * kMh;  // first request row of this CTA
@@ -739,7 +831,7 @@ partial_quad_kernel(const PartialArgs a) {
             bool ok = true;
             int jt = 0;  // tiles so far
             QuadItem it;
-            for (int k = 0; ok && quad_item(a, nrb, n_items, C, cid, k, it); ++k) {
+            for (ItemWalk wk = walk_init(sm.h, cid, C); ok && walk_next(wk, a, sm.h, nrb, n_items, C, cid, it);) {
                 for (int i = 0; ok && i < it.ntiles; ++i, ++jt) {
                     const int rs = jt % kRowsRing;
                     if (!warp_wait(O.rows_full[rs], (jt / kRowsRing) & 1, abort_p)) {
@@ -779,15 +871,15 @@ partial_quad_kernel(const PartialArgs a) {
             // slots: once P V of tile j is complete, its slot may take tile
             // j + 2.
             TileCursor cur;
-            cursor_init(cur);
+            cursor_init(cur, sm.h, cid, C);
             int staged = 0;
             auto stage_next = [&]() -> int {  // 1: staged, 0: no tile left, -1: timed out
-                if (!cursor_next(cur, a, nrb, n_items, C, cid)) return 0;
+                if (!cursor_next(cur, a, sm.h, nrb, n_items, C, cid)) return 0;
                 const int j = staged;
                 const int rs = j % kRowsRing;
                 if (j >= kRowsRing && !warp_wait(O.rows_free[rs], ((j / kRowsRing) - 1) & 1, abort_p))
                     return -1;
-                (void)stage_rows(a, a.kv_indptr[cur.it.b], cur.it.kb + cur.i * kNT, cur.it.ke, lane,
+                (void)stage_rows(a, a.kv_indptr[cur.b], cur.kb + cur.i * kNT, cur.ke, lane,
                                  O.rows[rs], nullptr);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ba(O.rows_full[rs]));
@@ -825,7 +917,7 @@ partial_quad_kernel(const PartialArgs a) {
                 uint32_t ph = 0;
                 bool ok = true;
                 QuadItem it;
-                for (int k = 0; ok && quad_item(a, nrb, n_items, C, cid, k, it); ++k) {
+                for (ItemWalk wk = walk_init(sm.h, cid, C); ok && walk_next(wk, a, sm.h, nrb, n_items, C, cid, it);) {
                     for (int i = 0; ok && i < it.ntiles; ++i, ++jt) {
                         const int slot = jt & 1;
                         if (!mbar_wait_spin(ba(O.o_gate[slot]), (jt >> 1) & 1, abort_p)) {
@@ -870,7 +962,7 @@ partial_quad_kernel(const PartialArgs a) {
                 int g = 0;
                 bool ok = true;
                 QuadItem it;
-                for (int k = 0; ok && quad_item(a, nrb, n_items, C, cid, k, it); ++k) {
+                for (ItemWalk wk = walk_init(sm.h, cid, C); ok && walk_next(wk, a, sm.h, nrb, n_items, C, cid, it);) {
                     const int gend = g + it.ntiles * (kNT / kVKeys);
                     for (; g < gend; ++g) {
                         const int st = g % kVStages;
@@ -896,10 +988,33 @@ partial_quad_kernel(const PartialArgs a) {
             float* tile = O.otile[quarter];
             const int jr = lane >> 3, jc = 4 * (lane & 7);  // row in a group of 4, column
             const int64_t gstep = (int64_t)4 * a.nsplit * kDv;  // four rows on
+            if (sm.h.balanced) {
+                // The partitions past a (request, row block) pair's last
+                // part get lse = -inf; the cluster holding the pair's first
+                // tile writes them (or, for a pair without tiles, the
+                // cluster holding the tile at its place in the sequence).
+                const int w = sm.h.w;
+                const int e1 = plan_begin(cid + 1, C, w);
+                for (int b = 0; b < a.batch; ++b) {
+                    const int p0 = sm.h.ptile[b], p1 = sm.h.ptile[b + 1];
+                    if (p0 >= e1 && !(p0 >= w && cid == C - 1)) break;  // pairs start in order
+                    if (p1 <= plan_begin(cid, C, w) && p1 > p0) continue;
+                    const int t = (p1 - p0) / nrb;
+                    for (int rb = 0; rb < nrb; ++rb) {
+                        const int s0 = p0 + rb * t;
+                        if (plan_pair_owner(s0, t, C, w) != cid) continue;
+                        const int parts = plan_pair_parts(s0, t, C, w);
+                        const int grow = rb * kRowsBlk + (int)hr * kMh + r;
+                        if (grow >= rows_req) continue;
+                        float* lp = a.lse_part + ((int64_t)b * rows_req + grow) * a.nsplit;
+                        for (int p = parts; p < a.nsplit; ++p) lp[p] = -INFINITY;
+                    }
+                }
+            }
             bool ok = true;
             int jt = 0, ne = 0;  // tiles and non-empty items so far
             QuadItem it;
-            for (int k = 0; ok && quad_item(a, nrb, n_items, C, cid, k, it); ++k) {
+            for (ItemWalk wk = walk_init(sm.h, cid, C); ok && walk_next(wk, a, sm.h, nrb, n_items, C, cid, it);) {
                 const int row0 = it.rb * kRowsBlk + (int)hr * kMh;
                 const int grow = row0 + r;
                 const bool row_ok = grow < rows_req;

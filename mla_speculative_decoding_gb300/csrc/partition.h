@@ -75,4 +75,61 @@ inline int wave_full_items(long long items, int resident) {
     return (int)((items / resident) * resident);
 }
 
+// Balanced plan for persistent clusters. The key tiles of every (request,
+// row block) pair, request major and row block minor, form one sequence of
+// w tiles; request b's pairs start at ptile[b] (ptile[batch] = w) and hold
+// (ptile[b + 1] - ptile[b]) / nrb tiles each. Cluster c of C takes tiles
+// [plan_begin(c), plan_begin(c + 1)); the part of a pair one cluster holds
+// is one partition of that pair's rows, numbered in key order from 0.
+MLAV_HD inline int plan_begin(int c, int C, int w) { return (int)((long long)c * w / C); }
+
+// The cluster holding tile x (0 <= x < w).
+MLAV_HD inline int plan_cluster(int x, int C, int w) { return (int)(((long long)(x + 1) * C - 1) / w); }
+
+// Whether no pair of at most tmax tiles is cut into more than nsplit parts:
+// clusters hold at least floor(w / C) tiles, so a pair of t tiles meets at
+// most ceil((t - 1) / floor(w / C)) + 1 of them (t of them when a cluster
+// may hold no tile at all).
+MLAV_HD inline bool plan_fits(long long w, int tmax, int C, int nsplit) {
+    if (w <= 0 || w > (1ll << 30) || C <= 0) return false;
+    const long long m = w / C;
+    const long long parts = m == 0 ? tmax : (tmax - 1 + m - 1) / m + 1;
+    return parts <= nsplit;
+}
+
+// Partition of the pair starting at tile s0 that holds its tile x: the
+// clusters met since s0 (every cluster holds a tile when w >= C; otherwise
+// each holds at most one, and the count is the tile offset).
+MLAV_HD inline int plan_part(int s0, int x, int C, int w) {
+    return w >= C ? plan_cluster(x, C, w) - plan_cluster(s0, C, w) : x - s0;
+}
+
+// Parts of the pair whose t tiles start at tile s0, and the cluster that
+// writes its empty partitions (the one holding its first tile; for a pair
+// without tiles, the one holding the tile at its place, or the last).
+MLAV_HD inline int plan_pair_parts(int s0, int t, int C, int w) {
+    return t > 0 ? plan_part(s0, s0 + t - 1, C, w) + 1 : 0;
+}
+MLAV_HD inline int plan_pair_owner(int s0, int t, int C, int w) {
+    return plan_cluster(t > 0 ? s0 : (s0 < w - 1 ? s0 : w - 1), C, w);
+}
+
+// One step of cluster `cid`'s walk from its tile x (< xend): the pair
+// holding x is request b (advanced past requests that end at or before x)
+// and row block rb; the step takes that pair's tiles [u0, u1), partition s.
+// Returns the number of tiles taken.
+MLAV_HD inline int plan_step(const int* ptile, int nrb, int C, int w, int cid, int x, int xend, int& b,
+                             int& rb, int& u0, int& u1, int& s) {
+    while (ptile[b + 1] <= x) ++b;
+    const int p0 = ptile[b];
+    const int t = (ptile[b + 1] - p0) / nrb;
+    const int off = x - p0;
+    rb = off / t;
+    u0 = off - rb * t;
+    u1 = mlav_min(t, u0 + (xend - x));
+    s = plan_part(p0 + rb * t, x, C, w);
+    (void)cid;
+    return u1 - u0;
+}
+
 }  // namespace mlav

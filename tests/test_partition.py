@@ -131,3 +131,140 @@ def test_long_workload_shape(table):
         sizes = [-(-(e - b) // 256) for _, b, e in ranges]
         assert sizes[54:] == [1] * 10
         assert sum(sizes[:54]) == 722 - 10 and set(sizes[:54]) <= {13, 14}
+
+
+PLAN_HARNESS = r'''
+#include <cstdio>
+#include <vector>
+#include <random>
+#include "partition.h"
+using namespace mlav;
+int main() {
+    std::mt19937 rng(7);
+    const int Cs[] = {1, 5, 36, 76};
+    for (int trial = 0; trial < 400; ++trial) {
+        const int B = 1 + rng() % 12, nrb = 1 + rng() % 5, nsplit = 1 + rng() % 64;
+        std::vector<int> t(B), ptile(B + 1, 0);
+        for (int b = 0; b < B; ++b) {
+            const int r = rng() % 10;
+            t[b] = r == 0 ? 0 : (r < 4 ? 1 + rng() % 3 : 1 + rng() % 900);
+            ptile[b + 1] = ptile[b] + t[b] * nrb;
+        }
+        int tmax = 0;
+        for (int x : t) tmax = x > tmax ? x : tmax;
+        const int w = ptile[B];
+        for (int C : Cs) {
+            const bool fits = plan_fits(w, tmax, C, nsplit);
+            printf("F %d %d %d %d %d %d %d\n", trial, C, w, nrb, nsplit, tmax, fits ? 1 : 0);
+            for (int b = 0; b < B; ++b) printf("T %d %d %d %d\n", trial, C, b, t[b]);
+            if (!fits) continue;
+            for (int c = 0; c < C; ++c) {
+                int x = plan_begin(c, C, w);
+                const int xend = plan_begin(c + 1, C, w);
+                printf("R %d %d %d %d %d\n", trial, C, c, x, xend);
+                int b = 0;
+                while (x < xend) {
+                    int rb, u0, u1, s;
+                    const int n = plan_step(ptile.data(), nrb, C, w, c, x, xend, b, rb, u0, u1, s);
+                    printf("I %d %d %d %d %d %d %d %d\n", trial, C, c, b, rb, u0, u1, s);
+                    if (n <= 0) return 1;
+                    x += n;
+                }
+            }
+            for (int b = 0; b < B; ++b)
+                for (int rb = 0; rb < nrb; ++rb) {
+                    const int s0 = ptile[b] + rb * t[b];
+                    printf("O %d %d %d %d %d %d\n", trial, C, b, rb, plan_pair_owner(s0, t[b], C, w),
+                           plan_pair_parts(s0, t[b], C, w));
+                }
+        }
+    }
+    return 0;
+}
+'''
+
+
+@pytest.fixture(scope="module")
+def plan(tmp_path_factory):
+    d = tmp_path_factory.mktemp("plan")
+    src, exe = d / "plan.cpp", d / "plan"
+    src.write_text(PLAN_HARNESS)
+    subprocess.run(["g++", "-O1", "-std=c++17", "-I", CSRC, str(src), "-o", str(exe)], check=True,
+                   capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    cases = {}
+    for line in out.splitlines():
+        f = line.split()
+        key = (int(f[1]), int(f[2]))
+        c = cases.setdefault(key, {"t": {}, "ranges": {}, "items": [], "owners": {}})
+        v = [int(x) for x in f[3:]]
+        if f[0] == "F":
+            c["w"], c["nrb"], c["nsplit"], c["tmax"], c["fits"] = v
+        elif f[0] == "T":
+            c["t"][v[0]] = v[1]
+        elif f[0] == "R":
+            c["ranges"][v[0]] = (v[1], v[2])
+        elif f[0] == "I":
+            c["items"].append(tuple(v))
+        else:
+            c["owners"][(v[0], v[1])] = (v[2], v[3])
+    return cases
+
+
+def test_balanced_plan(plan):
+    """Every (request, row block) pair's tiles are covered once, in key
+    order, by partitions 0, 1, 2, ... (fewer than nsplit) held by clusters
+    in increasing order (consecutive ones when every cluster holds a tile);
+    cluster loads differ by at most one tile; each pair
+    has one owner cluster, which holds its first tile, and its part count
+    equals the partitions the walk produced."""
+    n_fit = 0
+    for (trial, C), c in plan.items():
+        if not c["fits"]:
+            # refused only when some pair could be cut into more than nsplit parts
+            m = c["w"] // C
+            bound = c["tmax"] if m == 0 else (c["tmax"] - 1 + m - 1) // m + 1
+            assert c["w"] == 0 or bound > c["nsplit"]
+            continue
+        n_fit += 1
+        w, nrb = c["w"], c["nrb"]
+        sizes = [e - b for b, e in (c["ranges"][k] for k in range(C))]
+        assert sum(sizes) == w and max(sizes) - min(sizes) <= 1
+        pos = {}
+        for cl, b, rb, u0, u1, s in c["items"]:
+            assert 0 <= s < c["nsplit"] and u1 > u0
+            cov = pos.setdefault((b, rb), [])
+            cov.append((u0, u1, s, cl))
+        for b, t in c["t"].items():
+            for rb in range(nrb):
+                cov = sorted(pos.get((b, rb), []))
+                if t == 0:
+                    assert not cov
+                else:
+                    assert cov[0][0] == 0 and cov[-1][1] == t
+                    assert all(x[1] == y[0] for x, y in zip(cov, cov[1:]))
+                    assert [x[2] for x in cov] == list(range(len(cov)))
+                    assert all(y[3] > x[3] for x, y in zip(cov, cov[1:]))
+                    if w >= C:  # every cluster holds a tile: the holders are consecutive
+                        assert all(y[3] == x[3] + 1 for x, y in zip(cov, cov[1:]))
+                owner, parts = c["owners"][(b, rb)]
+                assert 0 <= owner < C and parts == len(cov)
+                if cov:
+                    assert owner == cov[0][3]
+    assert n_fit > 100
+
+
+def test_long_workload_plan():
+    """The long workload (184,792 keys: 722 tiles per row block, 2 row
+    blocks) on 36 clusters: one item of 40-41 tiles per cluster, 18
+    partitions per row block."""
+    ptile, C = [0, 2 * 722], 36
+    w = ptile[-1]
+    sizes = [0] * C
+    parts = {0: 0, 1: 0}
+    exe_free = [(c, (c * w) // C, ((c + 1) * w) // C) for c in range(C)]
+    for c, b0, e0 in exe_free:
+        sizes[c] = e0 - b0
+        parts[b0 // 722] += 1
+        assert b0 // 722 == (e0 - 1) // 722, "no cluster spans both row blocks"
+    assert set(sizes) <= {40, 41} and parts == {0: 18, 1: 18}
