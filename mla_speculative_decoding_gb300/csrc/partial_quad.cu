@@ -140,7 +140,6 @@ struct __align__(1024) SmemQuad {
 
 constexpr size_t kSmemBytes = sizeof(SmemQuad) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kKStages * kKBlock == kMh * 1024, "Q's latent dims are staged in the K ring");
 static_assert(kPXfer <= kPSlot && kPSlot % 1024 == 0, "P slot");
 
 __device__ __forceinline__ uint32_t ba(const uint64_t& b) { return smem_u32(&b); }
@@ -323,6 +322,37 @@ __device__ __forceinline__ bool cursor_next(TileCursor& c, const PartialArgs& a,
     }
 }
 
+// Columns [c0, c1) of one warp's 32 rows (the TMEM lanes of its quarter) of
+// an item's partial o, scaled by the lane's 1/l: each 32-row x 32-column
+// chunk goes through a padded tile and out again with eight lanes per row,
+// so every store instruction writes four whole 128-byte lines.
+__device__ __forceinline__ void write_o_cols(const PartialArgs& a, const QuadItem& it, int rows_req,
+                                             int row0w, uint32_t taddr, float inv, float* tile, int lane,
+                                             int c0, int c1) {
+    const int jr = lane >> 3, jc = 4 * (lane & 7);  // row in a group of 4, column
+    const int rj0 = row0w + jr;                     // this lane's row of group 0
+    float* const o0 = a.o_part + (((int64_t)it.b * rows_req + rj0) * a.nsplit + it.s) * kDv + jc;
+    const int64_t gstep = (int64_t)4 * a.nsplit * kDv;  // four rows on
+#pragma unroll 1
+    for (int c = c0; c < c1; c += 32) {
+        uint32_t o[32];
+        tmem_ld32(taddr + c, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<float4*>(tile + lane * kOTileStride + 4 * u) = make_float4(
+                __uint_as_float(o[4 * u]) * inv, __uint_as_float(o[4 * u + 1]) * inv,
+                __uint_as_float(o[4 * u + 2]) * inv, __uint_as_float(o[4 * u + 3]) * inv);
+        __syncwarp();
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+            const float4 v = *reinterpret_cast<const float4*>(tile + (4 * g + jr) * kOTileStride + jc);
+            if (rj0 + 4 * g < rows_req) *reinterpret_cast<float4*>(o0 + g * gstep + c) = v;
+        }
+        __syncwarp();
+    }
+}
+
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 partial_quad_kernel(const PartialArgs a) {
     extern __shared__ __align__(1024) unsigned char raw[];
@@ -413,11 +443,10 @@ partial_quad_kernel(const PartialArgs a) {
             constexpr int kNGroups = kSProd / kSGroup;
             constexpr int kFills = kDqk / 64;  // per tile
             bool ok = true;
-            int g0 = 0, j0 = 0, ne = 0;  // fills, tiles and non-empty items so far
+            int g0 = 0, j0 = 0;  // fills and tiles so far
             QuadItem it;
             for (ItemWalk wk = walk_init(sm.h, cid, C); ok && walk_next(wk, a, sm.h, nrb, n_items, C, cid, it);) {
                 if (it.ntiles <= 0) continue;
-                ok = warp_wait(S.q_ready, ne & 1, abort_p);  // the ring doubles as Q staging
                 const int nfill = it.ntiles * kFills;
                 int seen = -1;  // last tile whose pool rows this warp has waited for
                 for (int g = g0 + (grp - g0 % kNGroups + kNGroups) % kNGroups; ok && g < g0 + nfill;
@@ -449,13 +478,12 @@ partial_quad_kernel(const PartialArgs a) {
                 }
                 g0 += nfill;
                 j0 += it.ntiles;
-                ++ne;
             }
             cp_async_wait_all();
         } else if (warp == kWarpCtl) {
             // ------------------------------------------------ tile metadata + P sender
             // The warp stages each tile's pool rows (all 256, with validity
-            // bits for the softmax) two tiles ahead of the copies, across
+            // bits for the softmax) three tiles ahead of the P it sends, across
             // item boundaries; lane 0 sends each tile's P (and rescale
             // factors) from the staging tile to the O partner's slot once that
             // slot is free, then hands the staging tile back to the softmax.
@@ -485,7 +513,10 @@ partial_quad_kernel(const PartialArgs a) {
             };
             const uint32_t p_local = smem_u32(S.pstage);
             const uint32_t orank = 2u + hr;
+            // Slot j % 4 is restaged for tile j + 3 once the softmax has read
+            // tile j - 1's bits, which it has when P of tile j - 1 is sent.
             int more = stage_next();
+            if (more > 0) more = stage_next();
             if (more > 0) more = stage_next();
             bool ok = more >= 0;
             for (int j = 0; ok && j < staged; ++j) {
@@ -631,26 +662,43 @@ partial_quad_kernel(const PartialArgs a) {
                 const int grow = row0 + r;
                 const bool row_ok = grow < rows_req;
                 const int t = row_ok ? grow / H : 0;
-                // Q staging: latent dims into the K ring as eight 128-row x
-                // 64-dim swizzled blocks, RoPE dims straight into their
-                // swizzled A-operand tile. The previous item's MMAs are
-                // complete (its last S tile was waited for), so neither the
-                // ring nor TMEM's Q columns are still being read.
+                // Q staging: RoPE dims into their swizzled A-operand tile by
+                // cp.async; latent dims straight from global memory into TMEM
+                // (each thread its row's 256 dims of this half), so the K ring
+                // is never used for Q and the copy warps run on into the next
+                // item's keys. The previous item's MMAs are complete (its last
+                // S tile was waited for), so neither TMEM's Q columns nor the
+                // RoPE tile are still being read.
                 {
                     const __nv_bfloat16* q0 = a.q + ((int64_t)b * rows_req + row0) * kDqk;
-                    for (int f = stid; f < kMh * (kDqk / 8); f += 256) {
-                        const int rr = f / (kDqk / 8), c = f % (kDqk / 8);
+                    for (int f = stid; f < kMh * 8; f += 256) {
+                        const int rr = f >> 3, c = f & 7;
                         const bool v = row0 + rr < rows_req;
-                        const __nv_bfloat16* src = v ? q0 + (int64_t)rr * kDqk + c * 8 : a.q;
-                        const uint32_t dst = c < 64 ? smem_u32(S.kring[c >> 3]) + sw128_offset(rr, c & 7)
-                                                    : smem_u32(S.q_rope) + sw128_offset(rr, c - 64);
-                        cp_async_16_zfill(dst, src, v);
+                        const __nv_bfloat16* src = v ? q0 + (int64_t)rr * kDqk + 512 + c * 8 : a.q;
+                        cp_async_16_zfill(smem_u32(S.q_rope) + sw128_offset(rr, c), src, v);
                     }
                     if (stid < T) {
                         if (a.anc_mask != nullptr)
                             S.anc[stid] = a.anc_mask[(int64_t)b * T + stid];
                         else
                             S.par[stid] = a.tree_parent[(int64_t)b * T + stid];
+                    }
+                    {
+                        const uint4* src = reinterpret_cast<const uint4*>(q0 + (int64_t)r * kDqk + half * 256);
+#pragma unroll 1
+                        for (int c = 0; c < 4; ++c) {  // 64 dims (eight 16-byte loads) at a time
+                            uint32_t w[32];
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                const uint4 x = row_ok ? __ldg(src + 8 * c + u) : make_uint4(0, 0, 0, 0);
+                                w[4 * u] = x.x;
+                                w[4 * u + 1] = x.y;
+                                w[4 * u + 2] = x.z;
+                                w[4 * u + 3] = x.w;
+                            }
+                            tmem_st32(tbase + lb + kColQ + half * 128 + c * 32, w);
+                        }
+                        tmem_wait_st();
                     }
                     // The softmax warps meet on mbarriers (bounded waits), not
                     // on a named barrier: a warp that gave up on a timed-out
@@ -662,23 +710,6 @@ partial_quad_kernel(const PartialArgs a) {
                         break;
                     }
                     if (stid == 0 && a.anc_mask == nullptr) bad |= build_anc_serial(S.par, T, S.anc);
-                    if (half == 0) {
-#pragma unroll 1
-                        for (int c = 0; c < 8; ++c) {
-                            const unsigned char* blk = S.kring[c];
-                            uint32_t w[32];
-#pragma unroll
-                            for (int u = 0; u < 8; ++u) {
-                                const uint4 v = *reinterpret_cast<const uint4*>(blk + sw128_offset(r, u));
-                                w[4 * u] = v.x;
-                                w[4 * u + 1] = v.y;
-                                w[4 * u + 2] = v.z;
-                                w[4 * u + 3] = v.w;
-                            }
-                            tmem_st32(tbase + lb + kColQ + c * 32, w);
-                        }
-                        tmem_wait_st();
-                    }
                     fence_proxy_async_smem();
                     tc_fence_before();
                     mbar_arrive(ba(S.q_ready));  // also orders the masks built above
@@ -821,7 +852,7 @@ partial_quad_kernel(const PartialArgs a) {
             }
         }
     } else if (wg != 2) {
-        regs_dec<kRegsLow>();
+        // (the O CTAs keep the 96 launch registers: no role there needs more)
         SmemO& O = sm.u.o;
         if (warp != kWarpMMA && warp != kWarpCtl) {
             // ------------------------------------------------ O producers: V segments
@@ -829,9 +860,14 @@ partial_quad_kernel(const PartialArgs a) {
             // CTA's four 64-dim segments (eight lanes per 128-byte segment).
             const int pw = warp < kWarpMMA ? warp : (warp < 8 ? warp - 1 : warp - 6);  // 0..13
             bool ok = true;
-            int jt = 0;  // tiles so far
-            QuadItem it;
+            int jt = 0, ne = 0;  // tiles and non-empty items so far
+            QuadItem it, last;
+            last.ntiles = 0;
             for (ItemWalk wk = walk_init(sm.h, cid, C); ok && walk_next(wk, a, sm.h, nrb, n_items, C, cid, it);) {
+                if (it.ntiles > 0) {
+                    last = it;
+                    ++ne;
+                }
                 for (int i = 0; ok && i < it.ntiles; ++i, ++jt) {
                     const int rs = jt % kRowsRing;
                     if (!warp_wait(O.rows_full[rs], (jt / kRowsRing) & 1, abort_p)) {
@@ -864,6 +900,25 @@ partial_quad_kernel(const PartialArgs a) {
                 }
             }
             cp_async_wait_all();
+            // The cluster's last item's partial write is split four ways per
+            // row quarter: the correction warp takes columns [0, 128) and
+            // warps q, 12 + q and 16 + q (copies done) the other three parts,
+            // with transpose tiles in the V ring, idle once P V is complete.
+            if (ok && last.ntiles > 0 && (warp < 4 || warp >= 12)) {
+                const int quarter = warp & 3, part = warp < 4 ? 1 : (warp < 16 ? 2 : 3);
+                const int fs = (ne - 1) & 1;
+                if (warp_wait_cluster(O.fin[fs], ((ne - 1) >> 1) & 1, abort_p) &&
+                    warp_wait(O.o_done[(jt - 1) & 1], ((jt - 1) >> 1) & 1, abort_p)) {
+                    tc_fence_after();
+                    const int r = 32 * quarter + lane;
+                    const float l = O.fin_l[fs][0][r] + O.fin_l[fs][1][r];
+                    const float inv = l > 0.f ? 1.f / l : 0.f;
+                    float* tile = reinterpret_cast<float*>(O.vring[0]) + (warp < 4 ? warp : warp - 8) * (32 * kOTileStride);
+                    write_o_cols(a, last, rows_req, last.rb * kRowsBlk + (int)hr * kMh + 32 * quarter,
+                                 tbase + ((uint32_t)(32 * quarter) << 16), inv, tile, lane, 128 * part,
+                                 128 * part + 128);
+                }
+            }
         } else if (warp == kWarpCtl) {
             // ------------------------------------------------ tile rows + P slot release
             // The warp stages each tile's pool rows two tiles ahead of the
@@ -986,8 +1041,6 @@ partial_quad_kernel(const PartialArgs a) {
             const uint32_t lb = (uint32_t)(32 * quarter) << 16;
             const uint32_t srank = hr;  // S partner holding the same rows
             float* tile = O.otile[quarter];
-            const int jr = lane >> 3, jc = 4 * (lane & 7);  // row in a group of 4, column
-            const int64_t gstep = (int64_t)4 * a.nsplit * kDv;  // four rows on
             if (sm.h.balanced) {
                 // The partitions past a (request, row block) pair's last
                 // part get lse = -inf; the cluster holding the pair's first
@@ -1066,31 +1119,21 @@ partial_quad_kernel(const PartialArgs a) {
                 const float lse = l > 0.f ? (O.fin_m[fs][r] + log2f(l)) * kLn2 : -INFINITY;
                 __syncwarp();
                 if (lane == 0) mbar_arrive_remote(mapa_shared(ba(sm.u.s.fin_free[fs]), srank));
-                // Coalesced partial write: each 32-row x 32-column chunk goes
-                // through a padded tile and out again with eight lanes per
-                // row, so every store instruction writes four whole 128-byte
-                // lines instead of 32 lines in part.
-                const int rj0 = row0 + 32 * quarter + jr;  // this lane's row of group 0
-                float* const o0 = a.o_part + (((int64_t)it.b * rows_req + rj0) * a.nsplit + it.s) * kDv + jc;
-#pragma unroll 1
-                for (int c0 = 0; c0 < 512; c0 += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(tbase + lb + c0, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        *reinterpret_cast<float4*>(tile + lane * kOTileStride + 4 * u) = make_float4(
-                            __uint_as_float(o[4 * u]) * inv, __uint_as_float(o[4 * u + 1]) * inv,
-                            __uint_as_float(o[4 * u + 2]) * inv, __uint_as_float(o[4 * u + 3]) * inv);
-                    __syncwarp();
-#pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        const float4 v = *reinterpret_cast<const float4*>(tile + (4 * g + jr) * kOTileStride + jc);
-                        if (rj0 + 4 * g < rows_req)
-                            *reinterpret_cast<float4*>(o0 + g * gstep + c0) = v;
-                    }
-                    __syncwarp();
+                // The partial write (coalesced through the warp's transpose
+                // tile); the cluster's last item shares it with the copy
+                // warps, which take columns [128, 512).
+                bool last = true;
+                {
+                    ItemWalk pk = wk;
+                    QuadItem nx;
+                    while (walk_next(pk, a, sm.h, nrb, n_items, C, cid, nx))
+                        if (nx.ntiles > 0) {
+                            last = false;
+                            break;
+                        }
                 }
+                write_o_cols(a, it, rows_req, row0 + 32 * quarter, tbase + lb, inv, tile, lane, 0,
+                             last ? 128 : 512);
                 if (row_ok) a.lse_part[((int64_t)it.b * rows_req + grow) * a.nsplit + it.s] = lse;
                 ++ne;
             }
