@@ -860,14 +860,9 @@ partial_quad_kernel(const PartialArgs a) {
             // CTA's four 64-dim segments (eight lanes per 128-byte segment).
             const int pw = warp < kWarpMMA ? warp : (warp < 8 ? warp - 1 : warp - 6);  // 0..13
             bool ok = true;
-            int jt = 0, ne = 0;  // tiles and non-empty items so far
-            QuadItem it, last;
-            last.ntiles = 0;
+            int jt = 0;  // tiles so far
+            QuadItem it;
             for (ItemWalk wk = walk_init(sm.h, cid, C); ok && walk_next(wk, a, sm.h, nrb, n_items, C, cid, it);) {
-                if (it.ntiles > 0) {
-                    last = it;
-                    ++ne;
-                }
                 for (int i = 0; ok && i < it.ntiles; ++i, ++jt) {
                     const int rs = jt % kRowsRing;
                     if (!warp_wait(O.rows_full[rs], (jt / kRowsRing) & 1, abort_p)) {
@@ -900,25 +895,6 @@ partial_quad_kernel(const PartialArgs a) {
                 }
             }
             cp_async_wait_all();
-            // The cluster's last item's partial write is split four ways per
-            // row quarter: the correction warp takes columns [0, 128) and
-            // warps q, 12 + q and 16 + q (copies done) the other three parts,
-            // with transpose tiles in the V ring, idle once P V is complete.
-            if (ok && last.ntiles > 0 && (warp < 4 || warp >= 12)) {
-                const int quarter = warp & 3, part = warp < 4 ? 1 : (warp < 16 ? 2 : 3);
-                const int fs = (ne - 1) & 1;
-                if (warp_wait_cluster(O.fin[fs], ((ne - 1) >> 1) & 1, abort_p) &&
-                    warp_wait(O.o_done[(jt - 1) & 1], ((jt - 1) >> 1) & 1, abort_p)) {
-                    tc_fence_after();
-                    const int r = 32 * quarter + lane;
-                    const float l = O.fin_l[fs][0][r] + O.fin_l[fs][1][r];
-                    const float inv = l > 0.f ? 1.f / l : 0.f;
-                    float* tile = reinterpret_cast<float*>(O.vring[0]) + (warp < 4 ? warp : warp - 8) * (32 * kOTileStride);
-                    write_o_cols(a, last, rows_req, last.rb * kRowsBlk + (int)hr * kMh + 32 * quarter,
-                                 tbase + ((uint32_t)(32 * quarter) << 16), inv, tile, lane, 128 * part,
-                                 128 * part + 128);
-                }
-            }
         } else if (warp == kWarpCtl) {
             // ------------------------------------------------ tile rows + P slot release
             // The warp stages each tile's pool rows two tiles ahead of the
@@ -1119,21 +1095,11 @@ partial_quad_kernel(const PartialArgs a) {
                 const float lse = l > 0.f ? (O.fin_m[fs][r] + log2f(l)) * kLn2 : -INFINITY;
                 __syncwarp();
                 if (lane == 0) mbar_arrive_remote(mapa_shared(ba(sm.u.s.fin_free[fs]), srank));
-                // The partial write (coalesced through the warp's transpose
-                // tile); the cluster's last item shares it with the copy
-                // warps, which take columns [128, 512).
-                bool last = true;
-                {
-                    ItemWalk pk = wk;
-                    QuadItem nx;
-                    while (walk_next(pk, a, sm.h, nrb, n_items, C, cid, nx))
-                        if (nx.ntiles > 0) {
-                            last = false;
-                            break;
-                        }
-                }
-                write_o_cols(a, it, rows_req, row0 + 32 * quarter, tbase + lb, inv, tile, lane, 0,
-                             last ? 128 : 512);
+                // The partial write, coalesced through the warp's transpose
+                // tile. (Spreading the last item's write over the idle copy
+                // warps as well was measured slower: the write is bound by
+                // the SM's store throughput, not by the issuing warps.)
+                write_o_cols(a, it, rows_req, row0 + 32 * quarter, tbase + lb, inv, tile, lane, 0, 512);
                 if (row_ok) a.lse_part[((int64_t)it.b * rows_req + grow) * a.nsplit + it.s] = lse;
                 ++ne;
             }
