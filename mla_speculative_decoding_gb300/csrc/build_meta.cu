@@ -49,6 +49,8 @@ build_meta_kernel(const int32_t* __restrict__ req_to_token, int64_t stride, int6
                   const int32_t* __restrict__ tree_parent, int batch, int T, int64_t capacity,
                   int32_t* __restrict__ kv_indptr, int32_t* __restrict__ kv_indices,
                   uint64_t* __restrict__ anc, int32_t* status) {
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
     const int b = blockIdx.x;
     __shared__ int64_t s_base;
     __shared__ int32_t s_L;
@@ -118,11 +120,9 @@ cudaError_t launch_build_meta(const int32_t* req_to_token, int64_t stride, int64
     const int64_t want = (per_req + 2 * kThreads - 1) / (2 * kThreads);
     const int by = (int)(want < 1 ? 1 : (want > kMaxBlocksPerReq ? kMaxBlocksPerReq : want));
     dim3 grid(batch, by);
-    build_meta_kernel<<<grid, kThreads, 0, stream>>>(req_to_token, stride, rows,
-                                                     req_pool_indices, prefix_lens, out_cache_loc,
-                                                     tree_parent, batch, T, capacity, kv_indptr,
-                                                     kv_indices, anc, status);
-    return cudaGetLastError();
+    return launch_pdl(build_meta_kernel, grid, dim3(kThreads), 0, stream, req_to_token, stride, rows,
+                      req_pool_indices, prefix_lens, out_cache_loc, tree_parent, batch, T, capacity,
+                      kv_indptr, kv_indices, anc, status);
 }
 
 }  // namespace mlav

@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(kWarps * 32)
 combine_kernel(const float* __restrict__ lse_part, const float* __restrict__ o_part, int rows,
                int nsplit, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
                int32_t* status) {
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
     const int64_t n = gw / kParts;
@@ -97,9 +99,8 @@ cudaError_t launch_combine(const float* lse_part, const float* o_part, int rows,
                            __nv_bfloat16* out, float* lse, int32_t* status, cudaStream_t stream) {
     const int64_t warps = (int64_t)rows * kParts;
     const int blocks = (int)((warps + kWarps - 1) / kWarps);
-    combine_kernel<<<blocks, kWarps * 32, 0, stream>>>(lse_part, o_part, rows, nsplit, out, lse,
-                                                      status);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3(blocks), dim3(kWarps * 32), 0, stream, lse_part, o_part, rows,
+                      nsplit, out, lse, status);
 }
 
 }  // namespace mlav

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "mla_verify.h"
 #include "partition.h"
 
@@ -37,6 +39,36 @@ __host__ __device__ inline WsLayout ws_layout(int batch, int T, int H, int nspli
     return w;
 }
 
+
+// Programmatic dependent launch. The verify path's kernels are launched
+// with the programmatic stream-serialization attribute, so each may start
+// (and set up its shared memory, TMEM and barriers) while the kernel before
+// it on the stream is still running. pdl_wait() blocks until that kernel has
+// completed and its writes are visible: every kernel calls it before its
+// first global memory access, which by induction orders it after all
+// earlier work on the stream. pdl_launch_dependents() lets the next kernel
+// start early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Host: launches `kernel` with the programmatic stream-serialization attribute.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 __device__ __forceinline__ void status_or(int32_t* st, int bits) {
     if (st != nullptr && bits != 0) atomicOr(st, bits);

@@ -123,6 +123,8 @@ __device__ __forceinline__ bool warp_wait_cluster(const uint64_t& bar, uint32_t 
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 partial_pair_kernel(const PartialArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
     extern __shared__ __align__(1024) unsigned char raw[];
     unsigned char* base = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
     SmemPair& sm = *reinterpret_cast<SmemPair*>(base);
@@ -735,8 +737,7 @@ cudaError_t launch_partial_pair(const PartialArgs& a, cudaStream_t stream) {
     PartialArgs w = a;
     w.wave_full = wave_full_items((long long)a.batch * a.nsplit * nrb,
                                   dev >= 0 && dev < 64 ? g_pair_clusters[dev] : 0);
-    partial_pair_kernel<<<grid, kThreads, kSmemBytes, stream>>>(w);
-    return cudaGetLastError();
+    return launch_pdl(partial_pair_kernel, grid, dim3(kThreads), kSmemBytes, stream, w);
 }
 
 }  // namespace mlav

@@ -355,6 +355,7 @@ __device__ __forceinline__ void write_o_cols(const PartialArgs& a, const QuadIte
 
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 partial_quad_kernel(const PartialArgs a) {
+    pdl_launch_dependents();
     extern __shared__ __align__(1024) unsigned char raw[];
     unsigned char* base = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
     SmemQuad& sm = *reinterpret_cast<SmemQuad*>(base);
@@ -372,7 +373,6 @@ partial_quad_kernel(const PartialArgs a) {
         tmem_alloc_pair(smem_u32(&sm.h.tmem_base), 512);
         tmem_relinquish_pair();
     }
-    if (warp == 1) build_plan(a.prefix_lens, a.kv_indptr, a.batch, T, a.nsplit, nrb, C, lane, sm.h);
     if (tid == 0) {
         mbar_init(ba(sm.h.drain), 1);
         if (sside) {
@@ -421,6 +421,8 @@ partial_quad_kernel(const PartialArgs a) {
         sm.h.no_abort = 0;
         fence_mbar_init();
     }
+    pdl_wait();  // the set-up above touches no global memory
+    if (warp == 1) build_plan(a.prefix_lens, a.kv_indptr, a.batch, T, a.nsplit, nrb, C, lane, sm.h);
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();  // every CTA's barriers exist before any remote arrive
@@ -1153,8 +1155,7 @@ cudaError_t launch_partial_quad(const PartialArgs& a, cudaStream_t stream) {
     const int clusters = resident > 0 && resident < items ? resident : (int)items;
     PartialArgs w = a;
     w.wave_full = wave_full_items(items, clusters);
-    partial_quad_kernel<<<dim3(4 * clusters, 1, 1), kThreads, kSmemBytes, stream>>>(w);
-    return cudaGetLastError();
+    return launch_pdl(partial_quad_kernel, dim3(4 * clusters, 1, 1), dim3(kThreads), kSmemBytes, stream, w);
 }
 
 }  // namespace mlav

@@ -56,6 +56,8 @@ __device__ __forceinline__ float dot8(const uint4& a, const uint4& b, float acc)
 }
 
 __global__ void __launch_bounds__(kThreads) partial_simt_kernel(const PartialArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SmemSimt& sm = *reinterpret_cast<SmemSimt*>(smem_raw);
     const int rb = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
@@ -201,8 +203,7 @@ cudaError_t setup_partial_simt() {
 cudaError_t launch_partial_simt(const PartialArgs& a, cudaStream_t stream) {
     const int rows_req = a.T * a.H;
     dim3 grid((rows_req + kRows - 1) / kRows, a.nsplit, a.batch);
-    partial_simt_kernel<<<grid, kThreads, sizeof(SmemSimt), stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(partial_simt_kernel, grid, dim3(kThreads), sizeof(SmemSimt), stream, a);
 }
 
 }  // namespace mlav

@@ -75,6 +75,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t& bar, uint32_t parity, volati
 }
 
 __global__ void __launch_bounds__(kThreads, 1) partial_tc_kernel(const PartialArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
     extern __shared__ __align__(1024) unsigned char raw[];
     unsigned char* base = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
     SmemTC& sm = *reinterpret_cast<SmemTC*>(base);
@@ -399,8 +401,7 @@ cudaError_t launch_partial_tc(const PartialArgs& a, int /*sm_count*/, cudaStream
     const int rows_req = a.T * a.H;
     const int nrb = (rows_req + kM - 1) / kM;
     dim3 grid(nrb * kParts, a.nsplit, a.batch);
-    partial_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(partial_tc_kernel, grid, dim3(kThreads), kSmemBytes, stream, a);
 }
 
 }  // namespace mlav
