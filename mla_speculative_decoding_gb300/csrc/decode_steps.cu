@@ -16,6 +16,8 @@ tree_accept_kernel(const int32_t* __restrict__ par, const int32_t* __restrict__ 
                    const int32_t* __restrict__ tgt, const int32_t* __restrict__ loc, int T,
                    int32_t* __restrict__ commit, int32_t* __restrict__ an, int32_t* __restrict__ ks,
                    int32_t* __restrict__ nt, int32_t* status) {
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
     const int b = blockIdx.x, lane = threadIdx.x;
     const int64_t base = (int64_t)b * T;
     int p[2], k[2];
@@ -71,6 +73,8 @@ kv_relocate_kernel(uint4* __restrict__ kv, int64_t pool_slots, int32_t* __restri
                    int64_t stride, const int32_t* __restrict__ rpi, const int32_t* __restrict__ L,
                    const int32_t* __restrict__ dst, const int32_t* __restrict__ progress, int budget,
                    int32_t* status) {
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
     const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int32_t len = L[b], j0 = progress[b];
     if (len < 0 || j0 < 0 || j0 > len) {
@@ -128,6 +132,8 @@ kv_relocate_kernel(uint4* __restrict__ kv, int64_t pool_slots, int32_t* __restri
 
 __global__ void kv_relocate_progress_kernel(int32_t* progress, const int32_t* L, int batch,
                                             int budget) {
+    pdl_launch_dependents();
+    pdl_wait();  // after the copies have read the counters
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b < batch) {
         const int32_t len = L[b], j0 = progress[b];
@@ -140,8 +146,8 @@ __global__ void kv_relocate_progress_kernel(int32_t* progress, const int32_t* L,
 cudaError_t launch_tree_accept(const int32_t* par, const int32_t* tok, const int32_t* tgt,
                                const int32_t* loc, int batch, int T, int32_t* commit, int32_t* an,
                                int32_t* ks, int32_t* nt, int32_t* status, cudaStream_t stream) {
-    tree_accept_kernel<<<batch, 32, 0, stream>>>(par, tok, tgt, loc, T, commit, an, ks, nt, status);
-    return cudaGetLastError();
+    return launch_pdl(tree_accept_kernel, dim3(batch), dim3(32), 0, stream, par, tok, tgt, loc, T, commit,
+                      an, ks, nt, status);
 }
 
 cudaError_t launch_kv_relocate(void* kv, int64_t pool_slots, int32_t* r2t, int64_t stride,
@@ -149,12 +155,12 @@ cudaError_t launch_kv_relocate(void* kv, int64_t pool_slots, int32_t* r2t, int64
                                int32_t* progress, int batch, int budget, int32_t* status,
                                cudaStream_t stream) {
     dim3 grid((budget + kRelocRowsPerCta - 1) / kRelocRowsPerCta, batch);
-    kv_relocate_kernel<<<grid, kRelocWarps * 32, 0, stream>>>(
-        static_cast<uint4*>(kv), pool_slots, r2t, stride, rpi, L, dst, progress, budget, status);
-    cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_pdl(kv_relocate_kernel, grid, dim3(kRelocWarps * 32), 0, stream,
+                                     static_cast<uint4*>(kv), pool_slots, r2t, stride, rpi, L, dst,
+                                     static_cast<const int32_t*>(progress), budget, status);
     if (e != cudaSuccess) return e;
-    kv_relocate_progress_kernel<<<(batch + 127) / 128, 128, 0, stream>>>(progress, L, batch, budget);
-    return cudaGetLastError();
+    return launch_pdl(kv_relocate_progress_kernel, dim3((batch + 127) / 128), dim3(128), 0, stream,
+                      progress, L, batch, budget);
 }
 
 }  // namespace mlav

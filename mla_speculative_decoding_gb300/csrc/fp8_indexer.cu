@@ -87,6 +87,8 @@ fp8_indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_con
                       int64_t nblocks, const int32_t* __restrict__ bt,
                       const int32_t* __restrict__ lens, int batch, int H, int P,
                       float* __restrict__ out, int32_t* status) {
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
     constexpr int kCols = 32 * NCH;                       // columns per accumulator
     constexpr uint32_t kAlloc = kCols * kIxAcc <= 128 ? 128 : (kCols * kIxAcc <= 256 ? 256 : 512);
     extern __shared__ uint8_t ix_raw[];
@@ -430,18 +432,19 @@ cudaError_t launch_fp8_indexer(const void* q, const float* w, const void* kv, in
         return cudaErrorInvalidValue;
     const uint8_t* kvb = static_cast<const uint8_t*>(kv);
 #define MLAV_IX_LAUNCH(NCH)                                                                       \
-    fp8_indexer_tc_kernel<NCH><<<grid, kIxThreads, ix_smem<NCH>(), stream>>>(                    \
-        kmap, qmap, kvb, w, nblocks, bt, lens, batch, H, P, out, status)
+    launch_pdl(fp8_indexer_tc_kernel<NCH>, dim3(grid), dim3(kIxThreads), ix_smem<NCH>(), stream, kmap, \
+               qmap, kvb, w, nblocks, bt, lens, batch, H, P, out, status)
+    cudaError_t e;
     if (H <= 32)
-        MLAV_IX_LAUNCH(1);
+        e = MLAV_IX_LAUNCH(1);
     else if (H <= 64)
-        MLAV_IX_LAUNCH(2);
+        e = MLAV_IX_LAUNCH(2);
     else if (H <= 96)
-        MLAV_IX_LAUNCH(3);
+        e = MLAV_IX_LAUNCH(3);
     else
-        MLAV_IX_LAUNCH(4);
+        e = MLAV_IX_LAUNCH(4);
 #undef MLAV_IX_LAUNCH
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace mlav
