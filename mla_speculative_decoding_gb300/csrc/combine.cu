@@ -6,8 +6,9 @@
 //   lse = ln sum_s exp(lse_s),   out = sum_s exp(lse_s - lse) * o_s,
 // splits with lse_s = -inf weighing 0. Four warps per query row, one per
 // 128 output dims: lanes hold the split lse values (max and sum by warp
-// shuffles), then each lane streams its 4 dims of every split with 16-byte
-// loads (coalesced 512 bytes per warp and split, sixteen splits in flight),
+// shuffles), then each lane streams its 4 dims of every split with weight
+// with 16-byte loads (coalesced 512 bytes per warp and split, sixteen
+// splits in flight; sparse groups of splits visit only the weighted ones),
 // summing splits in index order (deterministic), and rounds to bf16
 // (nearest even).
 #include "common.cuh"
@@ -61,28 +62,52 @@ combine_kernel(const float* __restrict__ lse_part, const float* __restrict__ o_p
     const float inv = 1.f / sum;
     if (lane == 0 && part == 0) lse[n] = mx + logf(sum);
 
+    // Splits in index order, sixteen loads in flight. A group of 32 with
+    // more than sixteen weighted splits is streamed whole (zero weights skip
+    // their loads); a sparser one visits only its weighted splits (a ballot),
+    // which is what the balanced four-SM plan leaves (most splits empty).
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     const float4* op = reinterpret_cast<const float4*>(o_part + n * nsplit * (int64_t)kDv) +
                        part * 32 + lane;
+    auto accumulate = [&](const float (&ws)[kUnroll], const float4 (&x)[kUnroll]) {
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            acc.x = fmaf(ws[u], x[u].x, acc.x);
+            acc.y = fmaf(ws[u], x[u].y, acc.y);
+            acc.z = fmaf(ws[u], x[u].z, acc.z);
+            acc.w = fmaf(ws[u], x[u].w, acc.w);
+        }
+    };
 #pragma unroll
     for (int g = 0; g < kMaxPerLane; ++g) {
-        for (int s0 = 0; s0 < 32; s0 += kUnroll) {
-            if (g * 32 + s0 >= nsplit) break;
+        if (g * 32 >= nsplit) break;
+        uint32_t live = __ballot_sync(0xffffffffu, w[g] != 0.f);  // warp-uniform
+        if (__popc(live) > kUnroll) {
+            for (int s0 = 0; s0 < 32; s0 += kUnroll) {
+                if (g * 32 + s0 >= nsplit) break;
+                float4 x[kUnroll];
+                float ws[kUnroll];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int s = g * 32 + s0 + u;
+                    ws[u] = __shfl_sync(0xffffffffu, w[g], s0 + u) * inv;
+                    x[u] = (s < nsplit && ws[u] != 0.f) ? op[s * (kDv / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                accumulate(ws, x);
+            }
+        } else if (live != 0u) {
             float4 x[kUnroll];
             float ws[kUnroll];
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
-                const int s = g * 32 + s0 + u;
-                ws[u] = __shfl_sync(0xffffffffu, w[g], s0 + u) * inv;
-                x[u] = (s < nsplit && ws[u] != 0.f) ? op[s * (kDv / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+                const bool have = live != 0u;
+                const int j = have ? __ffs((int)live) - 1 : 0;
+                const float wj = __shfl_sync(0xffffffffu, w[g], j) * inv;
+                ws[u] = have ? wj : 0.f;
+                x[u] = have ? op[(g * 32 + j) * (kDv / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+                live &= live - 1u;  // next set bit (no change once empty)
             }
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                acc.x = fmaf(ws[u], x[u].x, acc.x);
-                acc.y = fmaf(ws[u], x[u].y, acc.y);
-                acc.z = fmaf(ws[u], x[u].z, acc.z);
-                acc.w = fmaf(ws[u], x[u].w, acc.w);
-            }
+            accumulate(ws, x);
         }
     }
     const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
