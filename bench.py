@@ -355,22 +355,20 @@ def run_ours(args):
     # step's inputs (queries, tree, prefix lengths, table rows, draft slots) from
     # pinned memory, the verify path, D2H of out and lse. The KV pool and the
     # req_to_token table are resident device state.
-    h_in = {k: getattr(d, k).cpu().pin_memory() for k in
-            ("q", "tree_parent", "prefix_lens", "req_pool_indices", "out_cache_loc")}
-    h_out = d.out.cpu().pin_memory()
-    h_lse = d.lse.cpu().pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
-    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+    # The step's inputs live in one device buffer (d.step_in) and its outputs
+    # in another (d.step_out), so each direction is one copy.
+    h_in = d.step_in.cpu().pin_memory()
+    h_out = d.step_out.cpu().pin_memory()
+    h2d = h_in.numel()
+    d2h = h_out.numel()
     e2e_us = []
     for k in range(args.warmup + args.steps):
         flush()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for name, ht in h_in.items():
-            getattr(d, name).copy_(ht, non_blocking=True)
+        d.step_in.copy_(h_in, non_blocking=True)
         d.step()
-        h_out.copy_(d.out, non_blocking=True)
-        h_lse.copy_(d.lse, non_blocking=True)
+        h_out.copy_(d.step_out, non_blocking=True)
         torch.cuda.synchronize()
         if k >= args.warmup:
             e2e_us.append((time.perf_counter() - t0) * 1e6)

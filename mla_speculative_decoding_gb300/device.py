@@ -47,6 +47,14 @@ class DeviceInputs:
     workspace: torch.Tensor = None
     out: torch.Tensor = None
     lse: torch.Tensor = None
+    # One byte buffer each for the per-step inputs (q, tree_parent,
+    # prefix_lens, req_pool_indices, out_cache_loc) and outputs (out, lse);
+    # the named tensors are views into them, so a step's host data moves in
+    # one copy each way.
+    step_in: torch.Tensor = None
+    step_out: torch.Tensor = None
+
+    STEP_INPUTS = ("q", "tree_parent", "prefix_lens", "req_pool_indices", "out_cache_loc")
 
     def allocate(self):
         dev = self.q.device
@@ -55,9 +63,12 @@ class DeviceInputs:
         self.anc_mask = torch.zeros(self.batch * self.T, dtype=torch.int64, device=dev)
         self.workspace = B.alloc_workspace(self.batch, self.T, self.num_heads, self.nsplit, dev)
         self.workspace[:256].zero_()
-        self.out = torch.empty(self.batch * self.T, self.num_heads, B.D_V, dtype=torch.bfloat16,
-                               device=dev)
-        self.lse = torch.empty(self.batch * self.T, self.num_heads, dtype=torch.float32, device=dev)
+        self.step_in = _pack(self, self.STEP_INPUTS, dev)
+        out = torch.empty(self.batch * self.T, self.num_heads, B.D_V, dtype=torch.bfloat16,
+                          device=dev)
+        lse = torch.empty(self.batch * self.T, self.num_heads, dtype=torch.float32, device=dev)
+        self.out, self.lse = out, lse
+        self.step_out = _pack(self, ("out", "lse"), dev)
         return self
 
     @property
@@ -94,6 +105,24 @@ class DeviceInputs:
         """One pass of the whole verify path: build, partial, combine."""
         self.build(stream)
         self.attention(True, stream)
+
+
+def _pack(d: DeviceInputs, names, dev) -> torch.Tensor:
+    """Moves the named tensors of `d` into one byte buffer (each at a 256-byte
+    aligned offset) and rebinds the names to views of it; returns the buffer."""
+    offs, total = [], 0
+    for n in names:
+        t = getattr(d, n)
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    buf = torch.empty(max(total, 256), dtype=torch.uint8, device=dev)
+    for n, off in zip(names, offs):
+        t = getattr(d, n)
+        nb = t.numel() * t.element_size()
+        v = buf[off:off + nb].view(t.dtype).view(t.shape)
+        v.copy_(t)
+        setattr(d, n, v)
+    return buf
 
 
 def to_device(inp, device="cuda", nsplit=None, capacity=None) -> DeviceInputs:
