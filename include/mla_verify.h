@@ -192,6 +192,34 @@ int mla_verify_attention_anc(const void *q, const void *kv_pool, const int32_t *
                              int64_t pool_slots, float softmax_scale, size_t workspace_bytes,
                              cudaStream_t stream);
 
+/* The same verify attention with the index build fused into the gathers:
+ * the partial kernels read each key's pool slot straight from the page
+ * table (mla_build_verify_meta's inputs) instead of from a prebuilt combined
+ * list, and build the tree's visibility in-kernel from tree_parent, so a
+ * call is two launches (partial, combine) with no kv_indptr / kv_indices /
+ * anc_mask buffers ([VK] Part IX: combined indices = prefix slots ++
+ * out_cache_loc; [CR] section 2: the build is memory-trivial).
+ *   req_to_token      int32 [req_to_token_rows][req_to_token_stride], the
+ *                     request-to-slot table; stride in [1, 2^31 - 65]
+ *   req_pool_indices  int32 [batch]  table row of request b
+ *   prefix_lens       int32 [batch]  L_b; keys 0..L_b-1 are the row's first
+ *                     L_b entries, keys L_b..L_b+T-1 are out_cache_loc[b*T..]
+ *   out_cache_loc     int32 [batch*T] pool slots of the draft-tree tokens
+ * Everything else is as in mla_verify_attention (the default kernels, the
+ * same workspace). A row index outside the table or L_b outside [0,
+ * stride] is clamped as the builder clamps it and flagged with
+ * MLA_STATUS_BAD_PREFIX in the workspace status word (that request's
+ * keys are then its draft keys, resp. its whole row). On valid inputs the
+ * results are bit-identical to mla_build_verify_meta +
+ * mla_verify_attention. */
+int mla_verify_attention_paged(const void *q, const void *kv_pool, const int32_t *req_to_token,
+                               int64_t req_to_token_stride, int64_t req_to_token_rows,
+                               const int32_t *req_pool_indices, const int32_t *prefix_lens,
+                               const int32_t *out_cache_loc, const int32_t *tree_parent, int T,
+                               int nsplit, void *workspace, void *out, float *lse, int batch,
+                               int num_heads, int64_t pool_slots, float softmax_scale,
+                               size_t workspace_bytes, cudaStream_t stream);
+
 /*
  * The two halves of mla_verify_attention, for callers that schedule them
  * separately (e.g. to merge partials gathered from elsewhere).

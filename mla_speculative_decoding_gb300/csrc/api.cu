@@ -136,6 +136,10 @@ PartialArgs make_partial_args(const void* q, const void* kv_pool, const int32_t*
     a.pool_slots = pool_slots;
     a.scale_log2 = softmax_scale * kLog2e;
     a.wave_full = 0x7fffffff;  // no wave shaping unless a launcher sets it
+    a.req_to_token = nullptr;  // the combined-list form
+    a.r2t_stride = a.r2t_rows = 0;
+    a.req_pool_indices = nullptr;
+    a.out_cache_loc = nullptr;
     return a;
 }
 
@@ -265,6 +269,42 @@ MLAV_API int mla_verify_attention_anc(const void* q, const void* kv_pool,
     return attention_impl(q, kv_pool, kv_indices, kv_indptr, prefix_lens, nullptr, anc_mask, T,
                           nsplit, workspace, out, lse, batch, num_heads, pool_slots,
                           softmax_scale, workspace_bytes, stream);
+}
+
+MLAV_API int mla_verify_attention_paged(const void* q, const void* kv_pool,
+                                        const int32_t* req_to_token, int64_t req_to_token_stride,
+                                        int64_t req_to_token_rows, const int32_t* req_pool_indices,
+                                        const int32_t* prefix_lens, const int32_t* out_cache_loc,
+                                        const int32_t* tree_parent, int T, int nsplit,
+                                        void* workspace, void* out, float* lse, int batch,
+                                        int num_heads, int64_t pool_slots, float softmax_scale,
+                                        size_t workspace_bytes, cudaStream_t stream) {
+    if (!req_to_token || !req_pool_indices || !out_cache_loc || !tree_parent)
+        return MLA_ERR_INVALID_ARG;
+    if (req_to_token_stride < 1 || req_to_token_stride > (int64_t)INT32_MAX - MLA_MAX_TREE ||
+        req_to_token_rows < 1)
+        return MLA_ERR_INVALID_ARG;
+    // The list-form checks, with the table standing in for the list.
+    int rc = check_partial_args(q, kv_pool, req_to_token, req_pool_indices, prefix_lens, tree_parent,
+                                nullptr, T, nsplit, workspace, batch, num_heads, pool_slots,
+                                softmax_scale, workspace_bytes);
+    if (rc != MLA_OK) return rc;
+    rc = check_combine_args(workspace, batch, T, num_heads, nsplit, out, lse, workspace_bytes);
+    if (rc != MLA_OK) return rc;
+    int sms = 0;
+    rc = ensure_ready(stream, &sms);
+    if (rc != MLA_OK) return rc;
+    PartialArgs a = make_partial_args(q, kv_pool, nullptr, nullptr, prefix_lens, tree_parent, nullptr,
+                                      T, nsplit, workspace, batch, num_heads, pool_slots,
+                                      softmax_scale);
+    a.req_to_token = req_to_token;
+    a.r2t_stride = req_to_token_stride;
+    a.r2t_rows = req_to_token_rows;
+    a.req_pool_indices = req_pool_indices;
+    a.out_cache_loc = out_cache_loc;
+    rc = run_partial(a, 0u, sms, stream);
+    if (rc != MLA_OK) return rc;
+    return run_combine(workspace, batch, T, num_heads, nsplit, out, lse, stream);
 }
 
 MLAV_API int mla_verify_partial(const void* q, const void* kv_pool, const int32_t* kv_indices,

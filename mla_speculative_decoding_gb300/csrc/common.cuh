@@ -154,6 +154,13 @@ struct PartialArgs {
     int64_t pool_slots;
     float scale_log2;  // softmax_scale * log2(e)
     int wave_full;     // first item of the last, partial wave (split_range_waves)
+    // Paged form (kv_indices == nullptr): request b's keys are its table row
+    // req_to_token[req_pool_indices[b]][0, L_b) followed by its T draft slots
+    // out_cache_loc[b*T, b*T + T), read where the combined list would be.
+    const int32_t* req_to_token;
+    int64_t r2t_stride, r2t_rows;
+    const int32_t* req_pool_indices;
+    const int32_t* out_cache_loc;
 };
 
 // Prefix length and key count of request b, made consistent: a negative
@@ -161,6 +168,22 @@ struct PartialArgs {
 // keys are ignored, missing ones are absent). Returns the status bits.
 __device__ inline int request_keys(const PartialArgs& a, int b, int& Lb, int& K) {
     int bad = 0;
+    if (a.kv_indices == nullptr) {  // paged form: the builder's clamping, K = L_b + T
+        Lb = a.prefix_lens[b];
+        const int32_t r = a.req_pool_indices[b];
+        if (r < 0 || r >= a.r2t_rows) {
+            bad |= MLA_STATUS_BAD_PREFIX;
+            Lb = 0;
+        } else if (Lb < 0) {
+            bad |= MLA_STATUS_BAD_PREFIX;
+            Lb = 0;
+        } else if (Lb > a.r2t_stride) {
+            bad |= MLA_STATUS_BAD_PREFIX;
+            Lb = (int)a.r2t_stride;
+        }
+        K = Lb + a.T;
+        return bad;
+    }
     Lb = a.prefix_lens[b];
     if (Lb < 0) {
         Lb = 0;
@@ -170,6 +193,34 @@ __device__ inline int request_keys(const PartialArgs& a, int b, int& Lb, int& K)
     if (K != Lb + a.T) bad |= MLA_STATUS_BAD_INDPTR;
     K = max(0, min(K, Lb + a.T));
     return bad;
+}
+
+// Where request b's keys start: its offset in the combined list, or, in the
+// paged form, its table row's offset (0 for a row out of range, whose prefix
+// request_keys has cut to nothing).
+__device__ __forceinline__ int64_t key_base(const PartialArgs& a, int b) {
+    if (a.kv_indices != nullptr) return a.kv_indptr[b];
+    const int32_t r = a.req_pool_indices[b];
+    return (r >= 0 && r < a.r2t_rows) ? (int64_t)r * a.r2t_stride : 0;
+}
+// Pool slot of key j (0 <= j < K) of request b, given key_base and L_b.
+__device__ __forceinline__ int32_t key_slot(const PartialArgs& a, int b, int64_t base, int Lb, int j) {
+    if (a.kv_indices != nullptr) return __ldg(a.kv_indices + base + j);
+    return j < Lb ? __ldg(a.req_to_token + base + j) : __ldg(a.out_cache_loc + (int64_t)b * a.T + (j - Lb));
+}
+
+// Warms L2 with the slot entries of keys [j0, j1) of request b, one 128-byte
+// line (32 entries) per lane step, so that the row staging of the tiles to
+// come finds them there (the paged form reads the table, which no kernel
+// has just written).
+__device__ __forceinline__ void key_prefetch(const PartialArgs& a, int b, int64_t base, int Lb, int j0,
+                                             int j1, int lane) {
+    for (int j = j0 + 32 * lane; j < j1; j += 32 * 32) {
+        const int32_t* p = a.kv_indices != nullptr ? a.kv_indices + base + j
+                           : j < Lb ? a.req_to_token + base + j
+                                    : a.out_cache_loc + (int64_t)b * a.T + (j - Lb);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+    }
 }
 
 cudaError_t launch_partial_simt(const PartialArgs& a, cudaStream_t stream);

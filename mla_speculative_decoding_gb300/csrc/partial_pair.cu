@@ -141,7 +141,7 @@ partial_pair_kernel(const PartialArgs a) {
     const int nrb_req = (a.T * a.H + kM - 1) / kM;
     split_range_waves(K, a.nsplit, s, kNT, b * nrb_req + rb, a.batch * nrb_req, a.wave_full, kb, ke);
     const int ntiles = (ke - kb + kNT - 1) / kNT;
-    const int64_t kbase = a.kv_indptr[b];
+    const int64_t kbase = key_base(a, b);
 
     if (ntiles <= 0) {  // empty split (fixed grid, early exit): lse = -inf, o = 0
         if (rank == 1 && warp >= 8 && warp < 12) {
@@ -222,6 +222,7 @@ partial_pair_kernel(const PartialArgs a) {
             // eight lanes per 128-byte row segment.
             const int pw = warp < kWarpMMA ? warp : warp - 1;  // 0..6
             bool ok = true;
+            if (pw == 0) key_prefetch(a, b, kbase, Lb, kb + kNT, ke, lane);  // later tiles' slots
             for (int i = 0; ok && i < ntiles; ++i) {
                 const int rb2 = i & 1;
                 if (pw == 0) {
@@ -239,7 +240,7 @@ partial_pair_kernel(const PartialArgs a) {
                         const int j = kb + i * kNT + 32 * q + lane;
                         int32_t v = -1;
                         if (j < ke) {
-                            v = a.kv_indices[kbase + j];
+                            v = key_slot(a, b, kbase, Lb, j);
                             if (v < 0 || (int64_t)v >= a.pool_slots) {
                                 bad |= MLA_STATUS_BAD_SLOT;
                                 v = -1;
@@ -527,7 +528,7 @@ partial_pair_kernel(const PartialArgs a) {
                         const int j = kb + i * kNT + 32 * q + lane;
                         int32_t v = -1;
                         if (j < ke) {
-                            v = a.kv_indices[kbase + j];
+                            v = key_slot(a, b, kbase, Lb, j);
                             if (v < 0 || (int64_t)v >= a.pool_slots) v = -1;
                         }
                         O.rows[rb2][32 * q + lane] = v;

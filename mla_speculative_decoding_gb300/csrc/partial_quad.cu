@@ -160,14 +160,41 @@ __device__ __forceinline__ bool warp_wait_cluster(const uint64_t& bar, uint32_t 
 
 // Pool rows of one 256-key tile (and, for the softmax, their validity bits).
 // Returns MLA_STATUS_BAD_SLOT if a slot was out of range (that key is masked).
-__device__ __forceinline__ int stage_rows(const PartialArgs& a, int64_t kbase, int j0, int ke,
-                                          int lane, int32_t* rows, uint32_t* valid) {
+// The source is chosen once per tile (one base for all eight loads, as for
+// the combined list): the table row while the tile is in the prefix, the
+// draft slots after it; the one tile that straddles L_b takes its draft
+// keys in a second pass.
+__device__ __forceinline__ int stage_rows(const PartialArgs& a, int b, int64_t kbase, int Lb, int j0,
+                                          int ke, int lane, int32_t* rows, uint32_t* valid) {
     int bad = 0;
     int32_t v[8];
+    const bool paged = a.kv_indices == nullptr;
+    const int32_t* src;
+    int lim = ke;
+    if (!paged) {
+        src = a.kv_indices + kbase;
+    } else if (j0 < Lb) {
+        src = a.req_to_token + kbase;
+        lim = min(ke, Lb);
+    } else {
+        src = a.out_cache_loc + ((int64_t)b * a.T - Lb);
+    }
 #pragma unroll
     for (int q = 0; q < 8; ++q) {  // all eight loads in flight together
         const int j = j0 + 32 * q + lane;
-        v[q] = j < ke ? __ldg(a.kv_indices + kbase + j) : -1;
+        v[q] = j < lim ? __ldg(src + j) : -1;
+    }
+    if (paged && j0 < Lb && j0 + kNT > Lb) {  // through shared memory: each lane its own entries
+        const int32_t* dsrc = a.out_cache_loc + ((int64_t)b * a.T - Lb);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) rows[32 * q + lane] = v[q];
+#pragma unroll 1
+        for (int q = 0; q < 8; ++q) {
+            const int j = j0 + 32 * q + lane;
+            if (j >= Lb && j < ke) rows[32 * q + lane] = __ldg(dsrc + j);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = rows[32 * q + lane];
     }
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
@@ -220,11 +247,17 @@ __device__ __forceinline__ bool quad_item(const PartialArgs& a, int nrb, int n_i
 // (Not inlined: its registers stay out of the roles' budgets; it takes the
 // few arguments it reads by value so that the kernel parameters stay in
 // parameter space.)
-__device__ __noinline__ void build_plan(const int32_t* prefix_lens, const int32_t* kv_indptr, int batch,
-                                        int T, int nsplit, int nrb, int C, int lane, Header& h) {
+__device__ __noinline__ void build_plan(const int32_t* prefix_lens, const int32_t* kv_indptr,
+                                        const int32_t* kv_indices, const int32_t* req_pool_indices,
+                                        int64_t r2t_rows, int64_t r2t_stride, int batch, int T,
+                                        int nsplit, int nrb, int C, int lane, Header& h) {
     PartialArgs a;
     a.prefix_lens = prefix_lens;
     a.kv_indptr = kv_indptr;
+    a.kv_indices = kv_indices;
+    a.req_pool_indices = req_pool_indices;
+    a.r2t_rows = r2t_rows;
+    a.r2t_stride = r2t_stride;
     a.batch = batch;
     a.T = T;
     a.nsplit = nsplit;
@@ -295,7 +328,7 @@ __device__ __forceinline__ bool walk_next(ItemWalk& w, const PartialArgs& a, con
 // staging needs of each: request, key range, tile count).
 struct TileCursor {
     ItemWalk w;
-    int b, kb, ke, ntiles, i, bad;
+    int b, kb, ke, Lb, ntiles, i, bad;
 };
 __device__ __forceinline__ void cursor_init(TileCursor& c, const Header& h, int cid, int C) {
     c.w = walk_init(h, cid, C);
@@ -315,6 +348,7 @@ __device__ __forceinline__ bool cursor_next(TileCursor& c, const PartialArgs& a,
             c.b = it.b;
             c.kb = it.kb;
             c.ke = it.ke;
+            c.Lb = it.Lb;
             c.ntiles = it.ntiles;
             c.i = 0;
             return true;
@@ -422,7 +456,9 @@ partial_quad_kernel(const PartialArgs a) {
         fence_mbar_init();
     }
     pdl_wait();  // the set-up above touches no global memory
-    if (warp == 1) build_plan(a.prefix_lens, a.kv_indptr, a.batch, T, a.nsplit, nrb, C, lane, sm.h);
+    if (warp == 1)
+        build_plan(a.prefix_lens, a.kv_indptr, a.kv_indices, a.req_pool_indices, a.r2t_rows, a.r2t_stride,
+                   a.batch, T, a.nsplit, nrb, C, lane, sm.h);
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();  // every CTA's barriers exist before any remote arrive
@@ -503,7 +539,7 @@ partial_quad_kernel(const PartialArgs a) {
                 const int rs = j % kRowsRing, mi = j % kMetaRing;
                 if (j >= kMetaRing && !warp_wait(S.meta_free[mi], ((j / kMetaRing) - 1) & 1, abort_p))
                     return -1;
-                bad |= stage_rows(a, a.kv_indptr[cur.b], cur.kb + cur.i * kNT, cur.ke, lane,
+                bad |= stage_rows(a, cur.b, key_base(a, cur.b), cur.Lb, cur.kb + cur.i * kNT, cur.ke, lane,
                                   S.rows[rs], S.valid[mi]);
                 __syncwarp();
                 if (lane == 0) {
@@ -672,6 +708,8 @@ partial_quad_kernel(const PartialArgs a) {
                 // S tile was waited for), so neither TMEM's Q columns nor the
                 // RoPE tile are still being read.
                 {
+                    // the item's key slots into L2 for the row staging of its tiles
+                    if (warp == 8) key_prefetch(a, b, key_base(a, b), it.Lb, it.kb, it.ke, lane);
                     const __nv_bfloat16* q0 = a.q + ((int64_t)b * rows_req + row0) * kDqk;
                     for (int f = stid; f < kMh * 8; f += 256) {
                         const int rr = f >> 3, c = f & 7;
@@ -912,7 +950,7 @@ partial_quad_kernel(const PartialArgs a) {
                 const int rs = j % kRowsRing;
                 if (j >= kRowsRing && !warp_wait(O.rows_free[rs], ((j / kRowsRing) - 1) & 1, abort_p))
                     return -1;
-                (void)stage_rows(a, a.kv_indptr[cur.b], cur.kb + cur.i * kNT, cur.ke, lane,
+                (void)stage_rows(a, cur.b, key_base(a, cur.b), cur.Lb, cur.kb + cur.i * kNT, cur.ke, lane,
                                  O.rows[rs], nullptr);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ba(O.rows_full[rs]));

@@ -67,9 +67,9 @@ __global__ void __launch_bounds__(kThreads) partial_simt_kernel(const PartialArg
     const int row0 = rb * kRows;
     int bad = 0;
 
-    const int64_t kbase = a.kv_indptr[b];
     int Lb, K;
     bad |= request_keys(a, b, Lb, K);
+    const int64_t kbase = key_base(a, b);
     int kb, ke;
     split_range(K, a.nsplit, s, kb, ke);
 
@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kThreads) partial_simt_kernel(const PartialArg
             const int j = k0 + tid;
             int32_t sl = -1;
             if (j < ke) {
-                sl = a.kv_indices[kbase + j];
+                sl = key_slot(a, b, kbase, Lb, j);
                 if (sl < 0 || (int64_t)sl >= a.pool_slots) {
                     bad |= MLA_STATUS_BAD_SLOT;
                     sl = -1;

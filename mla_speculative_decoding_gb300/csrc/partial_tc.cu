@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1) partial_tc_kernel(const PartialAr
     int kb, ke;
     split_range(K, a.nsplit, s, kb, ke);
     const int ntiles = (ke - kb + kNK - 1) / kNK;
-    const int64_t kbase = a.kv_indptr[b];
+    const int64_t kbase = key_base(a, b);
 
     if (ntiles <= 0) {  // empty split: lse = -inf, o = 0 (fixed grid, early exit)
         if (warp >= 2) {
@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1) partial_tc_kernel(const PartialAr
             const int j = kb + i * kNK + lane;
             int32_t sl = -1;
             if (j < ke) {
-                sl = a.kv_indices[kbase + j];
+                sl = key_slot(a, b, kbase, Lb, j);
                 if (sl < 0 || (int64_t)sl >= a.pool_slots) {
                     bad |= MLA_STATUS_BAD_SLOT;
                     sl = -1;

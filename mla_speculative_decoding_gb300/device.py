@@ -106,6 +106,14 @@ class DeviceInputs:
         self.build(stream)
         self.attention(True, stream)
 
+    def step_paged(self, stream=None):
+        """The same pass with the index build fused into the partial kernels'
+        gathers (they read the page table): partial, combine."""
+        B.mla_verify_attention_paged(self.q, self.kv_pool, self.req_to_token, self.req_pool_indices,
+                                     self.prefix_lens, self.out_cache_loc, self.tree_parent, self.T,
+                                     self.nsplit, self.workspace, self.out, self.lse,
+                                     self.softmax_scale, stream)
+
 
 def _pack(d: DeviceInputs, names, dev) -> torch.Tensor:
     """Moves the named tensors of `d` into one byte buffer (each at a 256-byte
