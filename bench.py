@@ -277,18 +277,41 @@ def run_ours(args):
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
     flush = L2Flush(l2, dev)
 
+    # One step = the whole verify path through one C-ABI call: the paged
+    # entry point, whose partial kernels fetch each key's pool slot from the
+    # page table as they stage rows (the index build fused in) and build the
+    # tree masks in-kernel, then the combine. (With --simt: the builder and
+    # the CUDA-core partial kernel, through the combined key list.)
+    def step_call():
+        if args.flags:
+            d.build()
+            d.partial(flags=args.flags)
+            d.combine()
+        else:
+            d.step_paged()
+
     def one_step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        d.build()
+        step_call()
         if ev is not None:
             ev[1].record(stream)
-        d.partial(flags=args.flags)
-        if ev is not None:
-            ev[2].record(stream)
+
+    # The same path with events between its launches, for the per-kernel
+    # breakdown (kept out of the timed step: an event between two kernels
+    # keeps the second from starting early).
+    def split_step(ev):
+        ev[0].record(stream)
+        if args.flags:
+            d.build()
+            ev[1].record(stream)
+            d.partial(flags=args.flags)
+        else:
+            ev[1].record(stream)
+            d.partial_paged()
+        ev[2].record(stream)
         d.combine()
-        if ev is not None:
-            ev[3].record(stream)
+        ev[3].record(stream)
 
     for _ in range(args.warmup):
         flush()
@@ -305,7 +328,7 @@ def run_ours(args):
         gpu_id = None
     clocks = ClockSampler(gpu_id)
     time.sleep(0.3)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
@@ -316,10 +339,15 @@ def run_ours(args):
     barrier(world)
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
-    step_us = [evs[k][0].elapsed_time(evs[k][3]) * 1e3 for k in range(args.steps)]
-    part_us = [evs[k][1].elapsed_time(evs[k][2]) * 1e3 for k in range(args.steps)]
-    build_us = [evs[k][0].elapsed_time(evs[k][1]) * 1e3 for k in range(args.steps)]
-    comb_us = [evs[k][2].elapsed_time(evs[k][3]) * 1e3 for k in range(args.steps)]
+    step_us = [evs[k][0].elapsed_time(evs[k][1]) * 1e3 for k in range(args.steps)]
+    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush()
+        split_step(sevs[k])
+    torch.cuda.synchronize()
+    part_us = [sevs[k][1].elapsed_time(sevs[k][2]) * 1e3 for k in range(args.steps)]
+    build_us = [sevs[k][0].elapsed_time(sevs[k][1]) * 1e3 for k in range(args.steps)]
+    comb_us = [sevs[k][2].elapsed_time(sevs[k][3]) * 1e3 for k in range(args.steps)]
     mean_step = statistics.mean(step_us)
     mean_step_max = max_over_ranks(mean_step, world, dev if world > 1 else None)
     value = mean_step_max / world  # whole-job: calls of all ranks over the slowest rank's time
@@ -331,11 +359,11 @@ def run_ours(args):
         s = torch.cuda.Stream(device=dev)
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
-            d.step()
+            step_call()
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
         with torch.cuda.graph(g):
-            d.step()
+            step_call()
         ge = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
         for _ in range(3):
@@ -367,7 +395,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         d.step_in.copy_(h_in, non_blocking=True)
-        d.step()
+        step_call()
         h_out.copy_(d.step_out, non_blocking=True)
         torch.cuda.synchronize()
         if k >= args.warmup:
@@ -400,9 +428,9 @@ def run_ours(args):
         "kv_gbps": round(fig["kv_bytes"] / (value * 1e-6) / 1e9, 1),
         "roofline_frac": round(roof_us / value, 4),
         "roofline_us": round(roof_us, 3),
-        "breakdown_us": {"build": round(statistics.mean(build_us), 3),
-                         "partial": round(part_mean, 3),
-                         "combine": round(statistics.mean(comb_us), 3)},
+        "breakdown_us": ({"build": round(statistics.mean(build_us), 3)} if args.flags else
+                         {"build": "fused into the partial kernel"}) |
+                        {"partial": round(part_mean, 3), "combine": round(statistics.mean(comb_us), 3)},
         "graph_us": None if graph_us is None else round(graph_us, 3),
         "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": runit,
                      "frac": round(achieved / peak, 4), "traffic": ncu_traffic(idx),
@@ -410,7 +438,7 @@ def run_ours(args):
                      "algorithmic": {"bytes": fig["bytes"], "flops": fig["flops"]}},
         "e2e": {"value": round(e2e, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (3 if args.flags else 2) * args.steps,  # partial + combine (+ build)
         "clocks": clk,
         "wall_s_timed_region": round(wall, 4),
     }
@@ -459,13 +487,13 @@ def measure_config(j, mv, dev, flush, peaks, args, steps=10, placement="scattere
     stream = torch.cuda.current_stream()
     for _ in range(3):
         flush()
-        d.step()
+        d.step_paged()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
     for k in range(steps):
         flush()
         ev[k][0].record(stream)
-        d.step()
+        d.step_paged()
         ev[k][1].record(stream)
     torch.cuda.synchronize()
     us = statistics.mean(a.elapsed_time(b) * 1e3 for a, b in ev)
@@ -516,7 +544,7 @@ def measure_next_rows(mv, dev, flush, peaks, which=NEXT_ROWS):
         inp = make_sparse_decode()
         fig = workload_figures(inp)
         d = mv.to_device(inp, device=dev)
-        us = _time_us(d.step, flush)
+        us = _time_us(d.step_paged, flush)
         roof, bound, _, _ = roofline_us(fig, peaks)
         res["sparse_decode"] = {"workload": "batch 16, H=64, top-k 512 + self, nsplit 8",
                                 "us": round(us, 2), "roofline_us": round(roof, 3),

@@ -220,6 +220,17 @@ int mla_verify_attention_paged(const void *q, const void *kv_pool, const int32_t
                                int num_heads, int64_t pool_slots, float softmax_scale,
                                size_t workspace_bytes, cudaStream_t stream);
 
+/* The partial half of mla_verify_attention_paged (the split partials into
+ * the workspace, as mla_verify_partial writes them with flags 0);
+ * mla_verify_combine finishes the call. */
+int mla_verify_partial_paged(const void *q, const void *kv_pool, const int32_t *req_to_token,
+                             int64_t req_to_token_stride, int64_t req_to_token_rows,
+                             const int32_t *req_pool_indices, const int32_t *prefix_lens,
+                             const int32_t *out_cache_loc, const int32_t *tree_parent, int T,
+                             int nsplit, void *workspace, int batch, int num_heads,
+                             int64_t pool_slots, float softmax_scale, size_t workspace_bytes,
+                             cudaStream_t stream);
+
 /*
  * The two halves of mla_verify_attention, for callers that schedule them
  * separately (e.g. to merge partials gathered from elsewhere).

@@ -33,6 +33,7 @@ from .binding import (  # noqa: F401
     mla_verify_attention,
     mla_verify_attention_anc,
     mla_verify_attention_paged,
+    mla_verify_partial_paged,
     mla_verify_attention_noalloc,
     mla_verify_combine,
     mla_verify_init,

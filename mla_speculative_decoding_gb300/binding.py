@@ -61,6 +61,9 @@ _SIGS = {
     "mla_verify_attention_paged": (_c_int, [_vp, _vp, _vp, _c_i64, _c_i64, _vp, _vp, _vp, _vp,
                                             _c_int, _c_int, _vp, _vp, _vp, _c_int, _c_int, _c_i64,
                                             _c_f32, _c_size, _vp]),
+    "mla_verify_partial_paged": (_c_int, [_vp, _vp, _vp, _c_i64, _c_i64, _vp, _vp, _vp, _vp,
+                                          _c_int, _c_int, _vp, _c_int, _c_int, _c_i64, _c_f32,
+                                          _c_size, _vp]),
     "mla_verify_partial": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _vp,
                                     _c_int, _c_int, _c_i64, _c_f32, _c_size, ctypes.c_uint, _vp]),
     "mla_verify_combine": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _c_size,
@@ -246,6 +249,19 @@ def mla_verify_attention_paged(q, kv_pool, req_to_token, req_pool_indices, prefi
         _p(workspace), _p(out), _p(lse), batch, H, kv_pool.shape[0], float(softmax_scale),
         workspace.numel(), _stream(stream))
     _check("mla_verify_attention_paged", rc)
+
+
+def mla_verify_partial_paged(q, kv_pool, req_to_token, req_pool_indices, prefix_lens,
+                             out_cache_loc, tree_parent, T, nsplit, workspace, softmax_scale,
+                             stream=None) -> None:
+    """The partial half of mla_verify_attention_paged."""
+    batch, H = _attn_shapes(q, kv_pool, T, None, None)
+    rc = load().mla_verify_partial_paged(
+        _p(q), _p(kv_pool), _p(req_to_token), req_to_token.shape[1], req_to_token.shape[0],
+        _p(req_pool_indices), _p(prefix_lens), _p(out_cache_loc), _p(tree_parent), T, nsplit,
+        _p(workspace), batch, H, kv_pool.shape[0], float(softmax_scale), workspace.numel(),
+        _stream(stream))
+    _check("mla_verify_partial_paged", rc)
 
 
 def mla_verify_partial(q, kv_pool, kv_indices, kv_indptr, prefix_lens, tree_parent, anc_mask, T,

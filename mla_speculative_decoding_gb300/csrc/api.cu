@@ -271,14 +271,14 @@ MLAV_API int mla_verify_attention_anc(const void* q, const void* kv_pool,
                           softmax_scale, workspace_bytes, stream);
 }
 
-MLAV_API int mla_verify_attention_paged(const void* q, const void* kv_pool,
-                                        const int32_t* req_to_token, int64_t req_to_token_stride,
-                                        int64_t req_to_token_rows, const int32_t* req_pool_indices,
-                                        const int32_t* prefix_lens, const int32_t* out_cache_loc,
-                                        const int32_t* tree_parent, int T, int nsplit,
-                                        void* workspace, void* out, float* lse, int batch,
-                                        int num_heads, int64_t pool_slots, float softmax_scale,
-                                        size_t workspace_bytes, cudaStream_t stream) {
+namespace mlav {
+namespace {
+int paged_partial(const void* q, const void* kv_pool, const int32_t* req_to_token,
+                  int64_t req_to_token_stride, int64_t req_to_token_rows,
+                  const int32_t* req_pool_indices, const int32_t* prefix_lens,
+                  const int32_t* out_cache_loc, const int32_t* tree_parent, int T, int nsplit,
+                  void* workspace, int batch, int num_heads, int64_t pool_slots,
+                  float softmax_scale, size_t workspace_bytes, cudaStream_t stream) {
     if (!req_to_token || !req_pool_indices || !out_cache_loc || !tree_parent)
         return MLA_ERR_INVALID_ARG;
     if (req_to_token_stride < 1 || req_to_token_stride > (int64_t)INT32_MAX - MLA_MAX_TREE ||
@@ -288,8 +288,6 @@ MLAV_API int mla_verify_attention_paged(const void* q, const void* kv_pool,
     int rc = check_partial_args(q, kv_pool, req_to_token, req_pool_indices, prefix_lens, tree_parent,
                                 nullptr, T, nsplit, workspace, batch, num_heads, pool_slots,
                                 softmax_scale, workspace_bytes);
-    if (rc != MLA_OK) return rc;
-    rc = check_combine_args(workspace, batch, T, num_heads, nsplit, out, lse, workspace_bytes);
     if (rc != MLA_OK) return rc;
     int sms = 0;
     rc = ensure_ready(stream, &sms);
@@ -302,7 +300,38 @@ MLAV_API int mla_verify_attention_paged(const void* q, const void* kv_pool,
     a.r2t_rows = req_to_token_rows;
     a.req_pool_indices = req_pool_indices;
     a.out_cache_loc = out_cache_loc;
-    rc = run_partial(a, 0u, sms, stream);
+    return run_partial(a, 0u, sms, stream);
+}
+}  // namespace
+}  // namespace mlav
+
+MLAV_API int mla_verify_partial_paged(const void* q, const void* kv_pool, const int32_t* req_to_token,
+                                      int64_t req_to_token_stride, int64_t req_to_token_rows,
+                                      const int32_t* req_pool_indices, const int32_t* prefix_lens,
+                                      const int32_t* out_cache_loc, const int32_t* tree_parent,
+                                      int T, int nsplit, void* workspace, int batch, int num_heads,
+                                      int64_t pool_slots, float softmax_scale,
+                                      size_t workspace_bytes, cudaStream_t stream) {
+    return paged_partial(q, kv_pool, req_to_token, req_to_token_stride, req_to_token_rows,
+                         req_pool_indices, prefix_lens, out_cache_loc, tree_parent, T, nsplit,
+                         workspace, batch, num_heads, pool_slots, softmax_scale, workspace_bytes,
+                         stream);
+}
+
+MLAV_API int mla_verify_attention_paged(const void* q, const void* kv_pool,
+                                        const int32_t* req_to_token, int64_t req_to_token_stride,
+                                        int64_t req_to_token_rows, const int32_t* req_pool_indices,
+                                        const int32_t* prefix_lens, const int32_t* out_cache_loc,
+                                        const int32_t* tree_parent, int T, int nsplit,
+                                        void* workspace, void* out, float* lse, int batch,
+                                        int num_heads, int64_t pool_slots, float softmax_scale,
+                                        size_t workspace_bytes, cudaStream_t stream) {
+    int rc = check_combine_args(workspace, batch, T, num_heads, nsplit, out, lse, workspace_bytes);
+    if (rc != MLA_OK) return rc;
+    rc = paged_partial(q, kv_pool, req_to_token, req_to_token_stride, req_to_token_rows,
+                       req_pool_indices, prefix_lens, out_cache_loc, tree_parent, T, nsplit,
+                       workspace, batch, num_heads, pool_slots, softmax_scale, workspace_bytes,
+                       stream);
     if (rc != MLA_OK) return rc;
     return run_combine(workspace, batch, T, num_heads, nsplit, out, lse, stream);
 }

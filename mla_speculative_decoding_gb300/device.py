@@ -114,6 +114,12 @@ class DeviceInputs:
                                      self.nsplit, self.workspace, self.out, self.lse,
                                      self.softmax_scale, stream)
 
+    def partial_paged(self, stream=None):
+        """The partial half of step_paged (combine() finishes it)."""
+        B.mla_verify_partial_paged(self.q, self.kv_pool, self.req_to_token, self.req_pool_indices,
+                                   self.prefix_lens, self.out_cache_loc, self.tree_parent, self.T,
+                                   self.nsplit, self.workspace, self.softmax_scale, stream)
+
 
 def _pack(d: DeviceInputs, names, dev) -> torch.Tensor:
     """Moves the named tensors of `d` into one byte buffer (each at a 256-byte
