@@ -115,3 +115,28 @@ def test_paged_rejects_bad_arguments():
         mv.mla_verify_attention_paged(d.q, d.kv_pool, d.req_to_token, d.req_pool_indices,
                                       d.prefix_lens, d.out_cache_loc, d.tree_parent, d.T, 0,
                                       d.workspace, d.out, d.lse, d.softmax_scale)
+
+
+def test_paged_step_in_a_cuda_graph():
+    """The paged call is capture-safe: a captured step replays to the eager
+    result bit for bit (the benchmark times it this way too)."""
+    inp = config_cached(2)
+    d = mv.to_device(inp)
+    d.step_paged()
+    torch.cuda.synchronize()
+    o_ref, l_ref = d.out.clone(), d.lse.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        d.step_paged()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        d.step_paged()
+    d.out.zero_()
+    d.lse.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert status(d) == 0
+    assert _bit_equal(o_ref, d.out) and _bit_equal(l_ref, d.lse)
