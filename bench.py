@@ -96,11 +96,17 @@ def roofline_us(fig, peaks):
     return max(t_mem, t_flop), ("tensor" if t_flop > t_mem else "hbm"), t_mem, t_flop
 
 
-def kernel_source_hash():
+# The partial kernel each committed ncu record was taken on, by its source file.
+KERNEL_SOURCES = {"partial_quad_kernel": "partial_quad.cu", "partial_pair_kernel": "partial_pair.cu"}
+
+
+def kernel_source_hash(kernel="partial_quad_kernel"):
+    """Hash of the kernel's source file and the headers it shares."""
+    files = (KERNEL_SOURCES[kernel], "partial_tc.cuh", "tc_ptx.cuh", "common.cuh", "partition.h")
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_speculative_decoding_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name in ("partial_quad.cu", "partial_tc.cuh", "tc_ptx.cuh", "common.cuh", "partition.h"):
+        if name in files:
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(f.read())
     return h.hexdigest()[:16]
@@ -115,7 +121,9 @@ def ncu_traffic(config_idx):
     with open(path) as f:
         t = json.load(f)
     e = t.get(str(config_idx))
-    if not e or e.get("kernel_hash") != kernel_source_hash():
+    if not e or e.get("kernel") not in KERNEL_SOURCES:
+        return None
+    if e.get("kernel_hash") != kernel_source_hash(e["kernel"]):
         return None
     return e.get("dram_bytes_per_launch")
 
