@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -100,15 +101,23 @@ def roofline_us(fig, peaks):
 KERNEL_SOURCES = {"partial_quad_kernel": "partial_quad.cu", "partial_pair_kernel": "partial_pair.cu"}
 
 
+def _code_only(text):
+    """Source text without comments and trailing blanks (a comment edit does
+    not change the kernel the counters were taken on)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash(kernel="partial_quad_kernel"):
-    """Hash of the kernel's source file and the headers it shares."""
+    """Hash of the code of the kernel's source file and the headers it shares."""
     files = (KERNEL_SOURCES[kernel], "partial_tc.cuh", "tc_ptx.cuh", "common.cuh", "partition.h")
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_speculative_decoding_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name in files:
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -40,13 +40,20 @@
 // into another CTA's shared memory (the final row maxima and sums) uses
 // cluster scope.
 //
-// Persistent clusters: the launch holds one cluster per resident slot, and
-// cluster c takes the work items of rounds k = 0, 1, ... at position
-// (c + k) mod C of each round of C items (C = the launch's clusters), so that
-// over the rounds every cluster meets every request and row block. Every
-// ring, slot and barrier phase counts over the cluster's whole tile
-// sequence, so one item's drain (last softmax, P hand-over, last P V and the
-// partial write) overlaps the next item's Q staging and first key stages.
+// Persistent clusters: the launch holds one cluster per resident slot. By
+// default (the balanced plan) the key tiles of all (request, row block)
+// pairs form one sequence and each cluster takes one contiguous range of it,
+// each range's part of a pair being one partition (the pair's unused
+// partitions get lse = -inf); where that plan does not fit (more than 128
+// requests, or a pair cut into more than nsplit parts), cluster c takes the
+// work items of rounds k = 0, 1, ... at position (c + k) mod C of each round
+// of C items. Every ring, slot and barrier phase counts over the cluster's
+// whole tile sequence, so one item's drain (last softmax, P hand-over, last
+// P V and the partial write) overlaps the next item's start.
+//
+// Each tile's pool slots come from the combined key list or, in the paged
+// form, from the request's page-table row and its draft slots; control
+// warps stage them a few tiles ahead of the copies.
 //
 // Every wait is bounded; on a timeout a CTA drains its MMAs, reaches the
 // final cluster barrier, frees TMEM and flags MLA_STATUS_TIMEOUT.
@@ -80,7 +87,7 @@ constexpr int kKStages = 8;
 static_assert(kSProd / kSGroup <= kKStages, "producer groups must not exceed the K stages");
 constexpr uint32_t kKBlock = kNh * 128;        // 128 keys x 64 dims (bf16) = 16 KB
 constexpr int kMetaRing = 4;
-constexpr int kRowsRing = 4;       // pool-row staging, two tiles ahead of the copies
+constexpr int kRowsRing = 4;       // pool-row staging, up to three tiles ahead of the copies
 constexpr int kVKeys = 32;
 constexpr int kVStages = 4;
 constexpr uint32_t kVSub = kVKeys * 128;       // 32 keys x 64 dims = 4 KB
