@@ -45,6 +45,11 @@
  *     it only launches kernels on `stream`. Every call below except
  *     mla_verify_init is safe inside CUDA stream capture (call
  *     mla_verify_init for the device first).
+ *   - The kernels are launched with programmatic dependent launch: each may
+ *     start its set-up while the kernel before it on `stream` is still
+ *     running, but reads and writes global memory only after that kernel
+ *     (and so all earlier work on `stream`) has completed. Stream order is
+ *     kept for the caller; nothing is needed on its side.
  *   - Host-checkable arguments (sizes, null/alignment, finite scale) are
  *     checked before any launch and give a negative mla_status_t.
  *   - Device data is never read on the host. Bad device data never traps:
