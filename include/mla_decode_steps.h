@@ -9,7 +9,8 @@
  * one-time set-up of mla_verify_init must have run before capture). Host-
  * checkable arguments return a negative MLA_ERR_* code before any launch;
  * bad device data never traps: it sets bits in the caller's device status
- * word (int32, OR of MLA_STATUS_* bits, which the caller resets).
+ * word (int32, OR of MLA_STATUS_* bits, which the caller resets). Kernels
+ * use programmatic dependent launch as in mla_verify.h (stream order kept).
  *
  * Sources: [VK] "The Custom sm_120 Verify Kernel: From 0.7 tok/s to 3-6x
  * Decode Speedup on Blackwell Consumer GPUs"; [CR] "The Capstone Report";
