@@ -1,9 +1,8 @@
 """MLA tree-verify attention for speculative decoding on GB300 (sm_103a).
 
 The product is the C-ABI library libmlaverify.so (include/mla_verify.h):
-an index/tree-mask builder kernel, a split-KV partial attention kernel
-(tcgen05/TMEM tensor cores, with a CUDA-core path for other shapes) and a
-log-sum-exp combine kernel; beside them (include/mla_decode_steps.h) greedy
+an index/tree-mask builder kernel, the split-KV partial attention kernels
+(tcgen05/TMEM tensor cores) and a log-sum-exp combine kernel; beside them (include/mla_decode_steps.h) greedy
 tree acceptance, KV relocation and the fp8 paged indexer logits. This
 package is its thin Python binding.
 """
@@ -11,8 +10,6 @@ package is its thin Python binding.
 from .binding import (  # noqa: F401
     D_QK,
     D_V,
-    MLA_PARTIAL_SIMT,
-    MLA_PARTIAL_TC_QUARTER,
     MLA_PARTIAL_PAIR,
     MLA_PARTIAL_QUAD,
     MLA_STATUS_BAD_INDPTR,
@@ -22,8 +19,10 @@ from .binding import (  # noqa: F401
     MLA_STATUS_CAPACITY,
     MLA_STATUS_EMPTY_ROW,
     MLA_STATUS_TIMEOUT,
+    BoundCall,
     MlaError,
     alloc_workspace,
+    bind_verify_attention_paged,
     library_path,
     load,
     mla_build_verify_meta,

@@ -89,7 +89,8 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
 
 
 def build_selftest(force: bool = False) -> str:
-    """Test-only library with the tcgen05 layout self-test (shares tc_ptx.cuh)."""
+    """Test-only library with the tcgen05 layout self-tests (shares tc_ptx.cuh);
+    built on demand by the tests that load it, not by build()."""
     deps = [SELFTEST_SRC, os.path.join(CSRC, "tc_ptx.cuh"), os.path.join(CSRC, "tmap.cu"),
             os.path.join(CSRC, "tmap.cuh"), os.path.abspath(__file__)]
     if (not force and os.path.exists(SELFTEST_LIB)

@@ -1,16 +1,12 @@
-// Tensor-core (tcgen05 / TMEM) split-KV partial attention: interface.
+// Tensor-core (tcgen05 / TMEM) split-KV partial attention kernels: interface.
 #pragma once
 
 #include "common.cuh"
 
 namespace mlav {
 
-// True when the tensor-core kernel handles this shape.
-bool partial_tc_supported(const PartialArgs& a);
-cudaError_t launch_partial_tc(const PartialArgs& a, int sm_count, cudaStream_t stream);
-cudaError_t setup_partial_tc();
-
-// Split-role pair kernel (two SMs per 128-row block): the default tensor-core path.
+// Split-role pair kernel (two SMs per 128-row block): the default for
+// requests of at most 128 rows.
 cudaError_t launch_partial_pair(const PartialArgs& a, cudaStream_t stream);
 cudaError_t setup_partial_pair();
 

@@ -34,7 +34,7 @@
 // warpgroups (setmaxnreg). Every wait is bounded; on a timeout a CTA drains
 // its MMAs, frees TMEM, reaches the final cluster barrier and flags
 // MLA_STATUS_TIMEOUT.
-#include "partial_tc.cuh"
+#include "partial_kernels.cuh"
 #include "tc_ptx.cuh"
 
 namespace mlav {

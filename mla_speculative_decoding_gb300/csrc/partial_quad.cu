@@ -57,7 +57,7 @@
 //
 // Every wait is bounded; on a timeout a CTA drains its MMAs, reaches the
 // final cluster barrier, frees TMEM and flags MLA_STATUS_TIMEOUT.
-#include "partial_tc.cuh"
+#include "partial_kernels.cuh"
 #include "tc_ptx.cuh"
 
 namespace mlav {

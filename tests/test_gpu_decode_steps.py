@@ -159,7 +159,7 @@ def test_sparse_decode_workload():
     compare(out[rows], lse[rows], ref_out, ref_lse, "sparse decode")
 
 
-@pytest.mark.parametrize("flags", [0, mv.MLA_PARTIAL_SIMT])
+@pytest.mark.parametrize("flags", [0, mv.MLA_PARTIAL_QUAD])
 def test_sparse_decode_small_batch_full(flags):
     inp = make_sparse_decode(batch=2, pool_slots=20000, seed=9)
     d = run_gpu(inp, flags=flags)

@@ -10,8 +10,7 @@ from tests.gpu_util import compare, host_out, oracle_ref, run_gpu, status
 from workloads import make_inputs
 
 pytestmark = pytest.mark.gpu
-PATHS = [0, mv.MLA_PARTIAL_PAIR, mv.MLA_PARTIAL_QUAD, mv.MLA_PARTIAL_SIMT,
-         mv.MLA_PARTIAL_TC_QUARTER]
+PATHS = [0, mv.MLA_PARTIAL_PAIR, mv.MLA_PARTIAL_QUAD]
 
 
 def _bits(d):
