@@ -110,9 +110,11 @@ const char *mla_verify_status_string(int status);
 int mla_verify_version(void);
 
 /* One-time per-device set-up: checks the device is sm_103, sets kernel
- * attributes (dynamic shared memory), caches the SM count. Call it once per
- * device, with that device current, OUTSIDE stream capture. The attention
- * calls run it lazily on first use when not capturing.
+ * attributes (dynamic shared memory), caches the resident cluster counts,
+ * and looks up the allocation-free entry point's scratch area (see
+ * mla_verify_attention_noalloc; the device reserves its 32 MiB here). Call
+ * it once per device, with that device current, OUTSIDE stream capture. The
+ * other calls run it lazily on first use when not capturing.
  * Returns MLA_OK, MLA_ERR_UNSUPPORTED or MLA_ERR_CUDA. */
 int mla_verify_init(int device);
 
@@ -249,20 +251,17 @@ int mla_verify_partial_paged(const void *q, const void *kv_pool, const int32_t *
  *                                   unspecified (not read by the combine)
  * at workspace + 256 (lse_part, padded to 256 bytes) and right after it
  * (o_part). Exactly one of tree_parent / anc_mask must be non-NULL.
- * flags: 0 = default kernel (tensor cores: for requests with more than 128
- * rows T*H, four SMs per 256-row block with 2-SM MMAs; otherwise two SMs per
- * 128-row block); MLA_PARTIAL_PAIR forces the two-SM kernel,
- * MLA_PARTIAL_QUAD the four-SM one (rows past T*H are padding);
- * MLA_PARTIAL_SIMT the CUDA-core kernel; MLA_PARTIAL_TC_QUARTER the
- * single-SM tensor-core kernel that splits the V dims over four CTAs. All
- * give results within the documented tolerance of each other.
+ * flags: 0 = default kernel (for requests with more than 128 rows T*H, four
+ * SMs per 256-row block with 2-SM MMAs; otherwise two SMs per 128-row
+ * block); MLA_PARTIAL_PAIR forces the two-SM kernel, MLA_PARTIAL_QUAD the
+ * four-SM one (rows past T*H are padding). Both give results within the
+ * documented tolerance of each other. Any other bit, or both bits, is
+ * MLA_ERR_INVALID_ARG.
  *
  * mla_verify_combine merges them ([VK] Part VII "reduce"):
  *   lse[n] = ln sum_s exp(lse_part[n,s]);  out[n] = sum_s exp(lse_part[n,s] - lse[n]) o_part[n,s]
  * rounded to bf16 (nearest even); splits with lse_part = -inf get weight 0.
  */
-#define MLA_PARTIAL_SIMT 0x1u
-#define MLA_PARTIAL_TC_QUARTER 0x2u
 #define MLA_PARTIAL_PAIR 0x4u
 #define MLA_PARTIAL_QUAD 0x8u
 int mla_verify_partial(const void *q, const void *kv_pool, const int32_t *kv_indices,
@@ -283,22 +282,24 @@ int mla_verify_combine(const void *workspace, int batch, int T, int num_heads, i
  * application's allocator is locked), and so cannot provide the workspace
  * that mla_verify_attention needs.
  *
- * Same inputs, outputs and results as mla_verify_attention, but the
- * per-split partials live in one fixed scratch area in device global memory
- * that the library reserves on every GPU that loads it, for the life of the
- * process: mla_verify_noalloc_scratch_bytes() bytes (32 MiB).
+ * Same inputs, outputs and results as mla_verify_attention (the same
+ * kernels, bit for bit), but the per-split partials live in one fixed
+ * scratch area in device global memory, mla_verify_noalloc_scratch_bytes()
+ * bytes (32 MiB), that a device holds from its set-up to process exit.
  *   - Shapes whose mla_verify_workspace_bytes(batch, T, num_heads, nsplit)
  *     exceeds that size are rejected with MLA_ERR_WORKSPACE_TOO_SMALL before
- *     anything is launched.
+ *     anything is launched: at most 16,351 partials (batch * T * num_heads *
+ *     nsplit), e.g. 128 query rows with 127 splits.
  *   - Nothing is allocated: no cudaMalloc/cudaFree, no allocating library
- *     call. The call enqueues a 4-byte memset (clearing the area's status
- *     word), the two kernels, and, if `status` is not NULL, a 4-byte
- *     device-to-device copy of this call's status bits into *status
- *     (overwriting it; NULL discards them).
- *   - The first call on each device looks up the area's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     outside stream capture (inside capture it returns
- *     MLA_ERR_NOT_INITIALIZED).
+ *     call. All host-side checks run first; then the call enqueues a 4-byte
+ *     memset (clearing the area's status word), the two kernels, and, if
+ *     `status` is not NULL, a 4-byte device-to-device copy of this call's
+ *     status bits into *status (overwriting it; NULL discards them).
+ *   - The area's device address is looked up (cudaGetSymbolAddress) by the
+ *     library's per-device set-up, mla_verify_init, which is also when the
+ *     device reserves the area. If mla_verify_init has not run on the
+ *     current device, the first call runs it; make that first call outside
+ *     stream capture (inside capture it returns MLA_ERR_NOT_INITIALIZED).
  *   - All calls share the one area and it keeps the previous call's
  *     contents: calls whose GPU work overlaps on the same device (other
  *     streams, other host threads) race on it and must be serialised by the

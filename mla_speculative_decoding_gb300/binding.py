@@ -32,8 +32,6 @@ MLA_STATUS_BAD_PREFIX = 0x10
 MLA_STATUS_EMPTY_ROW = 0x20
 MLA_STATUS_TIMEOUT = 0x40
 
-MLA_PARTIAL_SIMT = 0x1
-MLA_PARTIAL_TC_QUARTER = 0x2
 MLA_PARTIAL_PAIR = 0x4
 MLA_PARTIAL_QUAD = 0x8
 D_QK = 576
@@ -249,6 +247,42 @@ def mla_verify_attention_paged(q, kv_pool, req_to_token, req_pool_indices, prefi
         _p(workspace), _p(out), _p(lse), batch, H, kv_pool.shape[0], float(softmax_scale),
         workspace.numel(), _stream(stream))
     _check("mla_verify_attention_paged", rc)
+
+
+class BoundCall:
+    """One C-ABI call with its arguments marshalled once (device pointers,
+    sizes, scale and stream held as ctypes values); calling it issues the
+    same call again. The tensors it was bound to must stay alive and keep
+    their addresses (fixed buffers, as in a captured graph)."""
+
+    def __init__(self, name, args, keep):
+        self._name = name
+        self._fn = getattr(load(), name)
+        self._args = args
+        self._keep = keep  # the tensors whose pointers the arguments hold
+
+    def __call__(self) -> None:
+        rc = self._fn(*self._args)
+        if rc != MLA_OK:
+            raise MlaError(self._name, rc)
+
+
+def bind_verify_attention_paged(q, kv_pool, req_to_token, req_pool_indices, prefix_lens,
+                                out_cache_loc, tree_parent, T, nsplit, workspace, out, lse,
+                                softmax_scale, stream=None) -> BoundCall:
+    """mla_verify_attention_paged with its arguments checked and marshalled
+    once, for a caller that repeats the same call on fixed buffers."""
+    batch, H = _attn_shapes(q, kv_pool, T, out, lse)
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    args = (vp(_p(q)), vp(_p(kv_pool)), vp(_p(req_to_token)), i64(req_to_token.shape[1]),
+            i64(req_to_token.shape[0]), vp(_p(req_pool_indices)), vp(_p(prefix_lens)),
+            vp(_p(out_cache_loc)), vp(_p(tree_parent)), i32(T), i32(nsplit), vp(_p(workspace)),
+            vp(_p(out)), vp(_p(lse)), i32(batch), i32(H), i64(kv_pool.shape[0]),
+            ctypes.c_float(float(softmax_scale)), ctypes.c_size_t(workspace.numel()),
+            vp(_stream(stream)))
+    keep = (q, kv_pool, req_to_token, req_pool_indices, prefix_lens, out_cache_loc, tree_parent,
+            workspace, out, lse)
+    return BoundCall("mla_verify_attention_paged", args, keep)
 
 
 def mla_verify_partial_paged(q, kv_pool, req_to_token, req_pool_indices, prefix_lens,

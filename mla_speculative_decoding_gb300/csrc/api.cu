@@ -15,7 +15,7 @@
 
 #include "common.cuh"
 #include "mla_decode_steps.h"
-#include "partial_tc.cuh"
+#include "partial_kernels.cuh"
 
 namespace mlav {
 namespace {
@@ -43,9 +43,8 @@ int init_device(int device) {
         rc = MLA_ERR_CUDA;
     } else if (major != 10 || minor != 3) {
         rc = MLA_ERR_UNSUPPORTED;  // the library carries sm_103a code only
-    } else if (setup_partial_simt() != cudaSuccess || setup_partial_tc() != cudaSuccess ||
-               setup_partial_pair() != cudaSuccess || setup_partial_quad() != cudaSuccess ||
-               setup_fp8_indexer() != cudaSuccess) {
+    } else if (setup_partial_pair() != cudaSuccess || setup_partial_quad() != cudaSuccess ||
+               setup_fp8_indexer() != cudaSuccess || setup_noalloc(device) != cudaSuccess) {
         rc = MLA_ERR_CUDA;
     }
     if (rc == MLA_OK) {
@@ -143,13 +142,9 @@ PartialArgs make_partial_args(const void* q, const void* kv_pool, const int32_t*
     return a;
 }
 
-int run_partial(const PartialArgs& a, unsigned flags, int sm_count, cudaStream_t stream) {
+int run_partial(const PartialArgs& a, unsigned flags, cudaStream_t stream) {
     cudaError_t e;
-    if (flags & MLA_PARTIAL_SIMT)
-        e = launch_partial_simt(a, stream);
-    else if ((flags & MLA_PARTIAL_TC_QUARTER) && partial_tc_supported(a))
-        e = launch_partial_tc(a, sm_count, stream);
-    else if ((flags & MLA_PARTIAL_PAIR) || (!(flags & MLA_PARTIAL_QUAD) && a.T * a.H <= 128))
+    if ((flags & MLA_PARTIAL_PAIR) || (!(flags & MLA_PARTIAL_QUAD) && a.T * a.H <= 128))
         e = launch_partial_pair(a, stream);
     else
         e = launch_partial_quad(a, stream);
@@ -179,18 +174,33 @@ int attention_impl(const void* q, const void* kv_pool, const int32_t* kv_indices
     if (rc != MLA_OK) return rc;
     rc = check_combine_args(workspace, batch, T, num_heads, nsplit, out, lse, workspace_bytes);
     if (rc != MLA_OK) return rc;
-    int sms = 0;
-    rc = ensure_ready(stream, &sms);
+    rc = ensure_ready(stream, nullptr);
     if (rc != MLA_OK) return rc;
     const PartialArgs a =
         make_partial_args(q, kv_pool, kv_indices, kv_indptr, prefix_lens, tree_parent, anc_mask,
                           T, nsplit, workspace, batch, num_heads, pool_slots, softmax_scale);
-    rc = run_partial(a, 0u, sms, stream);
+    rc = run_partial(a, 0u, stream);
     if (rc != MLA_OK) return rc;
     return run_combine(workspace, batch, T, num_heads, nsplit, out, lse, stream);
 }
 
 }  // namespace
+
+int check_attention_args(const void* q, const void* kv_pool, const int32_t* kv_indices,
+                         const int32_t* kv_indptr, const int32_t* prefix_lens,
+                         const int32_t* tree_parent, int T, int nsplit, const void* workspace,
+                         const void* out, const float* lse, int batch, int num_heads,
+                         int64_t pool_slots, float softmax_scale, size_t workspace_bytes) {
+    if (!tree_parent) return MLA_ERR_INVALID_ARG;
+    const int rc = check_partial_args(q, kv_pool, kv_indices, kv_indptr, prefix_lens, tree_parent,
+                                      nullptr, T, nsplit, workspace, batch, num_heads, pool_slots,
+                                      softmax_scale, workspace_bytes);
+    if (rc != MLA_OK) return rc;
+    return check_combine_args(workspace, batch, T, num_heads, nsplit, out, lse, workspace_bytes);
+}
+
+int ensure_device_ready(cudaStream_t stream) { return ensure_ready(stream, nullptr); }
+
 }  // namespace mlav
 
 using namespace mlav;
@@ -289,8 +299,7 @@ int paged_partial(const void* q, const void* kv_pool, const int32_t* req_to_toke
                                 nullptr, T, nsplit, workspace, batch, num_heads, pool_slots,
                                 softmax_scale, workspace_bytes);
     if (rc != MLA_OK) return rc;
-    int sms = 0;
-    rc = ensure_ready(stream, &sms);
+    rc = ensure_ready(stream, nullptr);
     if (rc != MLA_OK) return rc;
     PartialArgs a = make_partial_args(q, kv_pool, nullptr, nullptr, prefix_lens, tree_parent, nullptr,
                                       T, nsplit, workspace, batch, num_heads, pool_slots,
@@ -300,7 +309,7 @@ int paged_partial(const void* q, const void* kv_pool, const int32_t* req_to_toke
     a.r2t_rows = req_to_token_rows;
     a.req_pool_indices = req_pool_indices;
     a.out_cache_loc = out_cache_loc;
-    return run_partial(a, 0u, sms, stream);
+    return run_partial(a, 0u, stream);
 }
 }  // namespace
 }  // namespace mlav
@@ -346,15 +355,15 @@ MLAV_API int mla_verify_partial(const void* q, const void* kv_pool, const int32_
                                 anc_mask, T, nsplit, workspace, batch, num_heads, pool_slots,
                                 softmax_scale, workspace_bytes);
     if (rc != MLA_OK) return rc;
-    if (flags & ~(MLA_PARTIAL_SIMT | MLA_PARTIAL_TC_QUARTER | MLA_PARTIAL_PAIR | MLA_PARTIAL_QUAD))
+    if ((flags & ~(MLA_PARTIAL_PAIR | MLA_PARTIAL_QUAD)) ||
+        (flags & (MLA_PARTIAL_PAIR | MLA_PARTIAL_QUAD)) == (MLA_PARTIAL_PAIR | MLA_PARTIAL_QUAD))
         return MLA_ERR_INVALID_ARG;
-    int sms = 0;
-    rc = ensure_ready(stream, &sms);
+    rc = ensure_ready(stream, nullptr);
     if (rc != MLA_OK) return rc;
     const PartialArgs a =
         make_partial_args(q, kv_pool, kv_indices, kv_indptr, prefix_lens, tree_parent, anc_mask,
                           T, nsplit, workspace, batch, num_heads, pool_slots, softmax_scale);
-    return run_partial(a, flags, sms, stream);
+    return run_partial(a, flags, stream);
 }
 
 MLAV_API int mla_verify_combine(const void* workspace, int batch, int T, int num_heads,

@@ -223,8 +223,17 @@ __device__ __forceinline__ void key_prefetch(const PartialArgs& a, int b, int64_
     }
 }
 
-cudaError_t launch_partial_simt(const PartialArgs& a, cudaStream_t stream);
-cudaError_t setup_partial_simt();
+// Host-side checks of mla_verify_attention's arguments (api.cu); the
+// library's per-device set-up on the current device, run lazily outside
+// stream capture (MLA_ERR_NOT_INITIALIZED inside it); the allocation-free
+// entry point's per-device scratch look-up (noalloc.cu), run by that set-up.
+int check_attention_args(const void* q, const void* kv_pool, const int32_t* kv_indices,
+                         const int32_t* kv_indptr, const int32_t* prefix_lens,
+                         const int32_t* tree_parent, int T, int nsplit, const void* workspace,
+                         const void* out, const float* lse, int batch, int num_heads,
+                         int64_t pool_slots, float softmax_scale, size_t workspace_bytes);
+int ensure_device_ready(cudaStream_t stream);
+cudaError_t setup_noalloc(int device);
 
 cudaError_t launch_combine(const float* lse_part, const float* o_part, int rows, int nsplit,
                            __nv_bfloat16* out, float* lse, int32_t* status, cudaStream_t stream);

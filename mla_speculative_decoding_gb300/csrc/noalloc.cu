@@ -8,17 +8,21 @@
 // mla_verify_attention needs for its per-split partial results.
 //
 // For them this file keeps one fixed scratch area in device global memory,
-// declared at file scope. Every GPU that loads the library reserves it (for
-// the lifetime of the process), so its size is capped at a modest 32 MiB:
-// enough for rows * nsplit up to about 16k partials (e.g. 128 query rows x 128
-// splits, or 256 rows x 64 splits).
+// declared at file scope, capped at a modest 32 MiB because every GPU that
+// loads this part of the library holds it until the process exits. The
+// workspace of a shape is 256 + round_up(4 p, 256) + 2048 p bytes for
+// p = batch * T * num_heads * nsplit partials, so the area takes at most
+// p = 16,351 partials: 128 query rows x 127 splits fit, 128 x 128 do not.
 //
 // Host code cannot use the array's name as a device address (on the host it
-// names a shadow object), so the first call on each device looks up the
-// real address with cudaGetSymbolAddress, with that device current, and
-// caches it. That first call must therefore happen outside stream capture.
-// All calls share the one area: calls whose GPU work overlaps (different
-// streams, or different host threads, on the same device) race on it.
+// names a shadow object), so the library's per-device set-up
+// (mla_verify_init, with that device current) looks up the real address
+// with cudaGetSymbolAddress and caches it; the look-up also loads this
+// file's module, which is when the device reserves the area. The first
+// noalloc call on a device runs that set-up if it has not run yet, so that
+// first call must happen outside stream capture. All calls share the one
+// area: calls whose GPU work overlaps (different streams, or different host
+// threads, on the same device) race on it.
 #include <mutex>
 
 #include "common.cuh"
@@ -33,26 +37,31 @@ constexpr int kMaxDev = 64;
 void* g_scratch_addr[kMaxDev];
 std::mutex g_scratch_mutex;
 
-// Device address of the scratch area on the current device (set-up on first
-// use; refused during stream capture). Returns an mla_status_t.
-int scratch_address(cudaStream_t stream, void** out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return MLA_ERR_CUDA;
+// Cached device address of the scratch area on `dev`, or nullptr before the
+// set-up has run there.
+void* scratch_of(int dev) {
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_addr[dev] == nullptr) {
-        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return MLA_ERR_CUDA;
-        if (cs != cudaStreamCaptureStatusNone) return MLA_ERR_NOT_INITIALIZED;
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_mla_noalloc_scratch) != cudaSuccess || p == nullptr)
-            return MLA_ERR_CUDA;
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
-    return MLA_OK;
+    return g_scratch_addr[dev];
 }
 
 }  // namespace
+
+namespace mlav {
+
+// Per-device set-up, called by mla_verify_init with `device` current.
+cudaError_t setup_noalloc(int device) {
+    if (device < 0 || device >= kMaxDev) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_addr[device] != nullptr) return cudaSuccess;
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_mla_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    if (p == nullptr) return cudaErrorInvalidSymbol;
+    g_scratch_addr[device] = p;
+    return cudaSuccess;
+}
+
+}  // namespace mlav
 
 MLAV_API size_t mla_verify_noalloc_scratch_bytes(void) { return MLA_NOALLOC_SCRATCH_BYTES; }
 
@@ -67,9 +76,19 @@ MLAV_API int mla_verify_attention_noalloc(const void* q, const void* kv_pool,
     if (need > MLA_NOALLOC_SCRATCH_BYTES) return MLA_ERR_WORKSPACE_TOO_SMALL;
     if (status != nullptr && (reinterpret_cast<uintptr_t>(status) & 3u) != 0)
         return MLA_ERR_INVALID_ARG;
-    void* ws = nullptr;
-    int rc = scratch_address(stream, &ws);
+    // Every host-side check runs before anything is queued. A stand-in
+    // pointer with the area's alignment takes the workspace's place in them.
+    const void* ws_probe = reinterpret_cast<const void*>(uintptr_t{256});
+    int rc = mlav::check_attention_args(q, kv_pool, kv_indices, kv_indptr, prefix_lens, tree_parent,
+                                        T, nsplit, ws_probe, out, lse, batch, num_heads, pool_slots,
+                                        softmax_scale, need);
     if (rc != MLA_OK) return rc;
+    rc = mlav::ensure_device_ready(stream);  // the set-up (and the scratch look-up) if not yet run
+    if (rc != MLA_OK) return rc;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return MLA_ERR_CUDA;
+    void* ws = scratch_of(dev);
+    if (ws == nullptr) return MLA_ERR_CUDA;
     // The status word lives in the shared area and keeps the previous call's
     // bits: clear it so this call reports only its own.
     int32_t* ws_status = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(ws) +

@@ -3,19 +3,19 @@
 It serves callers that cannot allocate device memory where they run the
 verify step (for example inside a runtime that owns all device memory), so
 it keeps its partial results in the library's fixed device scratch area
-instead of a caller workspace. This file checks, through the C ABI, that it
-returns the same results as the workspace entry point on two calls in a
-row (the second call reuses the scratch left by the first), that it
-reports its own status bits only, and that shapes beyond the scratch size
-are refused. It is collected last on purpose.
+instead of a caller workspace. It launches the same kernels as the
+workspace entry point, so this file checks, through the C ABI, that its
+results are bit-identical to that entry point's on two calls in a row (the
+second call reuses the scratch left by the first), at a shape just under
+the scratch size, that it reports its own status bits only, and that
+shapes just past the scratch size are refused before anything runs. It is
+collected last on purpose.
 """
 
-import numpy as np
 import pytest
 import torch
 
 import mla_speculative_decoding_gb300 as mv
-from tests.gpu_util import compare, host_out
 from workloads import make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -41,18 +41,27 @@ def _noalloc(d, status=None):
     return out, lse
 
 
-def test_noalloc_matches_workspace_entry_point_twice():
-    cases = [_case(31, [5000, 777], 16, 8, 32), _case(32, [12000], 8, 16, 64)]
+def _same_bits(a, b):
+    return torch.equal(a.view(torch.int16 if a.dtype == torch.bfloat16 else torch.int32),
+                       b.view(torch.int16 if b.dtype == torch.bfloat16 else torch.int32))
+
+
+def _partials(inp):
+    return inp.batch * inp.T * inp.num_heads * inp.nsplit
+
+
+def test_noalloc_bit_identical_to_workspace_entry_point_twice():
+    limit = mv.mla_verify_noalloc_scratch_bytes()
+    cases = [_case(31, [5000, 777], 16, 8, 32), _case(32, [12000], 8, 16, 64),
+             # 150 rows x 109 splits = 16,350 partials: just under the 32 MiB area
+             _case(35, [3000], 10, 15, 109)]
+    assert _partials(cases[-1][0]) == 16350
     status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
     for inp, d in cases:
-        assert (mv.mla_verify_workspace_bytes(inp.batch, inp.T, inp.num_heads, inp.nsplit)
-                <= mv.mla_verify_noalloc_scratch_bytes())
-        ref_out, ref_lse = host_out(d)
+        assert mv.mla_verify_workspace_bytes(inp.batch, inp.T, inp.num_heads, inp.nsplit) <= limit
         for _ in range(2):  # two calls in a row: the scratch keeps the last call's contents
             out, lse = _noalloc(d, status)
-            o = out.float().cpu().numpy().astype(np.float64).reshape(-1, 512)
-            l = lse.cpu().numpy().astype(np.float64).reshape(-1)
-            compare(o, l, ref_out, ref_lse, "noalloc vs workspace entry point")
+            assert _same_bits(out, d.out) and _same_bits(lse, d.lse)
             assert int(status.item()) == 0
 
 
@@ -67,17 +76,30 @@ def test_noalloc_status_reports_this_call_only():
     assert int(status.item()) == 0  # the previous call's bits are not carried over
 
 
-def test_noalloc_refuses_shapes_beyond_the_scratch():
-    limit = mv.mla_verify_noalloc_scratch_bytes()
-    assert limit == 32 << 20
-    T, H, ns = 64, 128, 128  # 8192 rows x 128 splits: far beyond 32 MiB
-    assert mv.mla_verify_workspace_bytes(1, T, H, ns) > limit
+def _refused_shape(T, H, ns):
     q = torch.zeros(T, H, 576, dtype=torch.bfloat16, device="cuda")
     kv = torch.zeros(16, 576, dtype=torch.bfloat16, device="cuda")
     i32 = torch.zeros(T + 2, dtype=torch.int32, device="cuda")
     par = torch.full((1, T), -1, dtype=torch.int32, device="cuda")
-    out = torch.empty(T, H, 512, dtype=torch.bfloat16, device="cuda")
-    lse = torch.empty(T, H, dtype=torch.float32, device="cuda")
+    out = torch.full((T, H, 512), 7.0, dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((T, H), 7.0, dtype=torch.float32, device="cuda")
+    status = torch.full((1,), 5, dtype=torch.int32, device="cuda")
     with pytest.raises(mv.MlaError) as e:
-        mv.mla_verify_attention_noalloc(q, kv, i32, i32, i32, par, T, ns, out, lse, 0.07)
-    assert e.value.code == -3
+        mv.mla_verify_attention_noalloc(q, kv, i32, i32, i32, par, T, ns, out, lse, 0.07,
+                                        status=status)
+    torch.cuda.synchronize()
+    # refused before anything was queued: outputs and status untouched
+    assert bool((out == 7.0).all()) and bool((lse == 7.0).all()) and int(status.item()) == 5
+    return e.value.code
+
+
+def test_noalloc_refuses_shapes_beyond_the_scratch():
+    limit = mv.mla_verify_noalloc_scratch_bytes()
+    assert limit == 32 << 20
+    # 224 rows x 73 splits = 16,352 partials: one past what the area holds
+    T, H, ns = 14, 16, 73
+    assert mv.mla_verify_workspace_bytes(1, T, H, ns) > limit
+    assert mv.mla_verify_workspace_bytes(1, 10, 15, 109) <= limit
+    assert _refused_shape(T, H, ns) == -3
+    # far beyond: 8192 rows x 128 splits
+    assert _refused_shape(64, 128, 128) == -3
