@@ -1,17 +1,22 @@
 """Benchmark of the MLA tree-verify path on GB300.
 
 One step = one pass of the whole verify path on one batch of seeded
-synthetic input: the index/tree-mask builder, the split-KV partial kernel
-and the log-sum-exp combine, launched through the C ABI on one stream.
+synthetic input, through one C-ABI call (mla_verify_attention_paged): the
+split-KV partial kernel, which reads each key's pool slot from the page
+table and builds the tree masks as it stages rows (the index build fused
+in), and the log-sum-exp combine, on one stream.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config C]
-                    [--impl ours|reference] [--no-extras]
+                    [--impl ours|reference] [--no-extras] [--next-rows ...]
 
-The headline workload is the long-context verify (batch 1, 8 heads,
-prefix 184,728 keys, 64-node random tree, nsplit 64): the pages' longest
-measured context. Inputs are resident in HBM when the timed region starts;
-each timed step is preceded (outside its events) by a write of a buffer
-larger than L2, so every step reads the KV rows from HBM.
+The headline workload is the batched mixed verify (batch 8, 64 heads,
+prefix lengths uniform in [1024, 131072], 16-node random trees, nsplit 64,
+a 1.2M-slot pool): the largest of the five workloads on one GPU. The line
+also carries, for every other workload, the same timings, and for the mid
+and long workloads the roofline block, the end-to-end time and a CPU-oracle
+sample. Inputs are resident in HBM when the timed region starts; each timed
+step is preceded (outside its events) by a write of a buffer larger than
+L2, so every step reads the KV rows from HBM.
 
 --impl reference times the CPU fp64 oracle (the only reference that exists
 for this method) on the machine's host cores, on a bounded sample of the same
@@ -24,7 +29,6 @@ import argparse
 import hashlib
 import re
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -111,7 +115,7 @@ def _code_only(text):
 
 def kernel_source_hash(kernel="partial_quad_kernel"):
     """Hash of the code of the kernel's source file and the headers it shares."""
-    files = (KERNEL_SOURCES[kernel], "partial_tc.cuh", "tc_ptx.cuh", "common.cuh", "partition.h")
+    files = (KERNEL_SOURCES[kernel], "partial_kernels.cuh", "tc_ptx.cuh", "common.cuh", "partition.h")
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_speculative_decoding_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
@@ -121,16 +125,16 @@ def kernel_source_hash(kernel="partial_quad_kernel"):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(config_idx):
-    """DRAM bytes per launch of the partial kernel from a committed ncu summary,
-    if it was taken on the current kernel source; else None."""
+def ncu_traffic(config_idx, kernel):
+    """DRAM bytes per launch of the workload's partial kernel from a committed
+    ncu summary, if it was taken on that kernel's current source; else None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         t = json.load(f)
     e = t.get(str(config_idx))
-    if not e or e.get("kernel") not in KERNEL_SOURCES:
+    if not e or e.get("kernel") != kernel or kernel not in KERNEL_SOURCES:
         return None
     if e.get("kernel_hash") != kernel_source_hash(e["kernel"]):
         return None
@@ -268,6 +272,172 @@ class L2Flush:
         self.buf[:2 * self.l2].sum()
 
 
+def time_steps(fn, flush, steps, warmup, stream):
+    """Device time (µs) of each of `steps` calls of fn, L2 flushed before
+    every call (outside the events); `warmup` untimed calls first."""
+    import torch
+    for _ in range(warmup):
+        flush()
+        fn()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        flush()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) * 1e3 for a, b in ev]
+
+
+def split_times(d, flush, steps, stream):
+    """The paged call's two launches timed apart (events between them keep
+    the second from starting early, so this is kept out of the timed step)."""
+    import torch
+    for _ in range(2):
+        flush()
+        d.partial_paged()
+        d.combine()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for e in ev:
+        flush()
+        e[0].record(stream)
+        d.partial_paged()
+        e[1].record(stream)
+        d.combine()
+        e[2].record(stream)
+    torch.cuda.synchronize()
+    part = statistics.mean(e[0].elapsed_time(e[1]) * 1e3 for e in ev)
+    comb = statistics.mean(e[1].elapsed_time(e[2]) * 1e3 for e in ev)
+    return part, comb
+
+
+def graph_time(fn, flush, steps, dev, stream):
+    """Median device time of a CUDA-graph replay of fn (the pages' deployment
+    mode); fn must launch on the current stream (it is captured on a side
+    stream)."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        fn()
+    return statistics.median(time_steps(g.replay, flush, steps, 3, stream))
+
+
+def e2e_time(d, flush, steps, warmup, stream):
+    """End to end through the public API with host buffers: per step the H2D
+    copy of that step's inputs from pinned memory (queries, tree, prefix
+    lengths, table rows, draft slots; the KV pool and req_to_token are
+    resident device state), the verify call, the D2H copy of out and lse,
+    and a synchronize, timed on the host clock. A second pass with events
+    between the pieces splits the time."""
+    import torch
+    call = d.bound_step_paged()
+    h_in = d.step_in.cpu().pin_memory()
+    h_out = d.step_out.cpu().pin_memory()
+
+    def one():
+        d.step_in.copy_(h_in, non_blocking=True)
+        call()
+        h_out.copy_(d.step_out, non_blocking=True)
+
+    walls = []
+    for k in range(warmup + steps):
+        flush()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        one()
+        torch.cuda.synchronize()
+        if k >= warmup:
+            walls.append((time.perf_counter() - t0) * 1e6)
+    # breakdown pass (events between the pieces)
+    parts = {"h2d": [], "verify": [], "d2h": [], "issue": []}
+    for _ in range(steps):
+        flush()
+        torch.cuda.synchronize()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        t0 = time.perf_counter()
+        e[0].record(stream)
+        d.step_in.copy_(h_in, non_blocking=True)
+        e[1].record(stream)
+        call()
+        e[2].record(stream)
+        h_out.copy_(d.step_out, non_blocking=True)
+        e[3].record(stream)
+        parts["issue"].append((time.perf_counter() - t0) * 1e6)
+        torch.cuda.synchronize()
+        parts["h2d"].append(e[0].elapsed_time(e[1]) * 1e3)
+        parts["verify"].append(e[1].elapsed_time(e[2]) * 1e3)
+        parts["d2h"].append(e[2].elapsed_time(e[3]) * 1e3)
+    wall = statistics.mean(walls)
+    br = {k: round(statistics.mean(v), 2) for k, v in parts.items()}
+    br["host_and_sync"] = round(wall - br["h2d"] - br["verify"] - br["d2h"], 2)
+    br["note"] = ("h2d / verify / d2h: device time between events (each after a flush); "
+                  "issue: host time to enqueue the three calls; host_and_sync: the rest of "
+                  "the wall time (launch latency before the first copy, gaps, synchronize)")
+    return wall, int(h_in.numel()), int(h_out.numel()), br
+
+
+def roofline_block(fig, peaks, peak_src, part_us, traffic, kernel):
+    """Roofline of the dominant (partial) kernel: algorithmic flops or bytes
+    of one launch over its measured device time."""
+    roof_us, bound, _, _ = roofline_us(fig, peaks)
+    if bound == "tensor":
+        achieved, peak, unit = fig["flops"] / (part_us * 1e-6) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = fig["bytes"] / (part_us * 1e-6) / 1e9, peaks["hbm_gbs"], "GB/s"
+    return {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel,
+            "peak_source": f"{peak_src} (burst)",
+            "frac_of_sustained": (round(achieved / peaks["bf16_tflops_sustained"], 4)
+                                  if bound == "tensor" and "bf16_tflops_sustained" in peaks
+                                  else None),
+            "algorithmic": {"bytes": fig["bytes"], "flops": fig["flops"]}}
+
+
+def default_kernel(inp):
+    return "partial_pair_kernel" if inp.T * inp.num_heads <= 128 else "partial_quad_kernel"
+
+
+def measure_workload(idx, inp, mv, dev, flush, peaks, peak_src, steps, warmup, full):
+    """One workload: the paged verify call (the benchmark's step) timed with
+    events after an L2 flush, its graph replay, the list-form call (builder +
+    mla_verify_attention, the boundary's own signature), the per-kernel
+    split; with `full`, also the roofline block, the end-to-end time and a
+    CPU-oracle sample."""
+    import torch
+    stream = torch.cuda.current_stream()
+    fig = workload_figures(inp)
+    d = mv.to_device(inp, device=dev)
+    call = d.bound_step_paged()
+    us = statistics.mean(time_steps(call, flush, steps, warmup, stream))
+    part, comb = split_times(d, flush, min(steps, 10), stream)
+    gus = graph_time(d.step_paged, flush, min(steps, 10), dev, stream)
+    lus = statistics.mean(time_steps(lambda: (d.build(), d.attention(use_anc=False)), flush,
+                                     min(steps, 10), 3, stream))
+    roof, bound, _, _ = roofline_us(fig, peaks)
+    res = {"us": round(us, 3), "graph_us": round(gus, 3), "list_form_us": round(lus, 3),
+           "breakdown_us": {"build": "fused into the partial kernel", "partial": round(part, 3),
+                            "combine": round(comb, 3)},
+           "roofline_us": round(roof, 3), "frac": round(roof / us, 4), "bound": bound,
+           "kv_gbps": round(fig["kv_bytes"] / (us * 1e-6) / 1e9, 1)}
+    if full:
+        kernel = default_kernel(inp)
+        res["roofline"] = roofline_block(fig, peaks, peak_src, part, ncu_traffic(idx, kernel), kernel)
+        wall, bi, bo, br = e2e_time(d, flush, steps, 3, stream)
+        res["e2e"] = {"value": round(wall, 3), "unit": UNIT, "h2d_bytes_per_step": bi,
+                      "d2h_bytes_per_step": bo, "breakdown_us": br}
+    res["status_ok"] = int(d.status.item()) == 0
+    del d, call
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import torch
 
@@ -297,42 +467,12 @@ def run_ours(args):
     # One step = the whole verify path through one C-ABI call: the paged
     # entry point, whose partial kernels fetch each key's pool slot from the
     # page table as they stage rows (the index build fused in) and build the
-    # tree masks in-kernel, then the combine. (With --simt: the builder and
-    # the CUDA-core partial kernel, through the combined key list.)
-    def step_call():
-        if args.flags:
-            d.build()
-            d.partial(flags=args.flags)
-            d.combine()
-        else:
-            d.step_paged()
-
-    def one_step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        step_call()
-        if ev is not None:
-            ev[1].record(stream)
-
-    # The same path with events between its launches, for the per-kernel
-    # breakdown (kept out of the timed step: an event between two kernels
-    # keeps the second from starting early).
-    def split_step(ev):
-        ev[0].record(stream)
-        if args.flags:
-            d.build()
-            ev[1].record(stream)
-            d.partial(flags=args.flags)
-        else:
-            ev[1].record(stream)
-            d.partial_paged()
-        ev[2].record(stream)
-        d.combine()
-        ev[3].record(stream)
+    # tree masks in-kernel, then the combine: two launches.
+    step_call = d.bound_step_paged()
 
     for _ in range(args.warmup):
         flush()
-        one_step()
+        step_call()
     torch.cuda.synchronize()
     assert int(d.status.item()) == 0, "device status word set during warm-up"
 
@@ -351,86 +491,35 @@ def run_ours(args):
     wall0 = time.perf_counter()
     for k in range(args.steps):
         flush()
-        one_step(evs[k])
+        evs[k][0].record(stream)
+        step_call()
+        evs[k][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
     step_us = [evs[k][0].elapsed_time(evs[k][1]) * 1e3 for k in range(args.steps)]
-    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    for k in range(args.steps):
-        flush()
-        split_step(sevs[k])
-    torch.cuda.synchronize()
-    part_us = [sevs[k][1].elapsed_time(sevs[k][2]) * 1e3 for k in range(args.steps)]
-    build_us = [sevs[k][0].elapsed_time(sevs[k][1]) * 1e3 for k in range(args.steps)]
-    comb_us = [sevs[k][2].elapsed_time(sevs[k][3]) * 1e3 for k in range(args.steps)]
     mean_step = statistics.mean(step_us)
     mean_step_max = max_over_ranks(mean_step, world, dev if world > 1 else None)
     value = mean_step_max / world  # whole-job: calls of all ranks over the slowest rank's time
-
-    # CUDA-graph replay of the same step (deployment mode on the pages).
-    graph_us = None
-    try:
-        g = torch.cuda.CUDAGraph()
-        s = torch.cuda.Stream(device=dev)
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            step_call()
-        torch.cuda.current_stream().wait_stream(s)
-        torch.cuda.synchronize()
-        with torch.cuda.graph(g):
-            step_call()
-        ge = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-        for _ in range(3):
-            flush()
-            g.replay()
-        for k in range(args.steps):
-            flush()
-            ge[k][0].record(stream)
-            g.replay()
-            ge[k][1].record(stream)
-        torch.cuda.synchronize()
-        graph_us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in ge)
-    except Exception as e:  # reported, not hidden
-        log(f"[bench] graph replay failed: {e!r}")
-
-    # End to end through the public API with host buffers: per step, H2D of the
-    # step's inputs (queries, tree, prefix lengths, table rows, draft slots) from
-    # pinned memory, the verify path, D2H of out and lse. The KV pool and the
-    # req_to_token table are resident device state.
-    # The step's inputs live in one device buffer (d.step_in) and its outputs
-    # in another (d.step_out), so each direction is one copy.
-    h_in = d.step_in.cpu().pin_memory()
-    h_out = d.step_out.cpu().pin_memory()
-    h2d = h_in.numel()
-    d2h = h_out.numel()
-    e2e_us = []
-    for k in range(args.warmup + args.steps):
-        flush()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        d.step_in.copy_(h_in, non_blocking=True)
-        step_call()
-        h_out.copy_(d.step_out, non_blocking=True)
-        torch.cuda.synchronize()
-        if k >= args.warmup:
-            e2e_us.append((time.perf_counter() - t0) * 1e6)
-    e2e = max_over_ranks(statistics.mean(e2e_us), world, dev if world > 1 else None) / world
     assert int(d.status.item()) == 0
 
-    roof_us, bound, t_mem, t_flop = roofline_us(fig, peaks)
-    part_mean = statistics.mean(part_us)
-    if bound == "tensor":
-        achieved = fig["flops"] / (part_mean * 1e-6) / 1e12
-        peak = peaks["bf16_tflops"]
-        runit = "TFLOP/s"
-    else:
-        achieved = fig["bytes"] / (part_mean * 1e-6) / 1e9
-        peak = peaks["hbm_gbs"]
-        runit = "GB/s"
+    part_us, comb_us = split_times(d, flush, args.steps, stream)
+    graph_us = None
+    try:
+        graph_us = graph_time(d.step_paged, flush, args.steps, dev, stream)
+    except Exception as e:  # reported, not hidden
+        log(f"[bench] graph replay failed: {e!r}")
+    list_us = statistics.mean(time_steps(lambda: (d.build(), d.attention(use_anc=False)), flush,
+                                         args.steps, 3, stream))
+    e2e_wall, h2d, d2h, e2e_br = e2e_time(d, flush, args.steps, args.warmup, stream)
+    e2e = max_over_ranks(e2e_wall, world, dev if world > 1 else None) / world
+    assert int(d.status.item()) == 0
+    del step_call, d
+    torch.cuda.empty_cache()
 
+    roof_us, bound, t_mem, t_flop = roofline_us(fig, peaks)
+    kernel = default_kernel(inp)
     result = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_step_max / 1e3, 6),
@@ -439,23 +528,20 @@ def run_ours(args):
         "config": {"workload": workload_name(idx), "batch": inp.batch,
                    "heads": inp.num_heads, "prefix_lens": [int(x) for x in inp.prefix_lens][:8],
                    "T": inp.T, "nsplit": inp.nsplit, "pool_slots": inp.pool_slots,
+                   "call": "mla_verify_attention_paged (partial + combine, two launches)",
                    "l2": L2Flush.DESCRIPTION,
-                   "parallelism": "replicas" if world > 1 else "single-gpu",
-                   "kernel": "simt" if args.flags else "default"},
+                   "parallelism": "replicas" if world > 1 else "single-gpu"},
         "kv_gbps": round(fig["kv_bytes"] / (value * 1e-6) / 1e9, 1),
         "roofline_frac": round(roof_us / value, 4),
         "roofline_us": round(roof_us, 3),
-        "breakdown_us": ({"build": round(statistics.mean(build_us), 3)} if args.flags else
-                         {"build": "fused into the partial kernel"}) |
-                        {"partial": round(part_mean, 3), "combine": round(statistics.mean(comb_us), 3)},
+        "breakdown_us": {"build": "fused into the partial kernel", "partial": round(part_us, 3),
+                         "combine": round(comb_us, 3)},
         "graph_us": None if graph_us is None else round(graph_us, 3),
-        "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": runit,
-                     "frac": round(achieved / peak, 4), "traffic": ncu_traffic(idx),
-                     "kernel": "partial", "peak_source": f"{peak_src} (burst)",
-                     "algorithmic": {"bytes": fig["bytes"], "flops": fig["flops"]}},
-        "e2e": {"value": round(e2e, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": (3 if args.flags else 2) * args.steps,  # partial + combine (+ build)
+        "list_form_us": round(list_us, 3),
+        "roofline": roofline_block(fig, peaks, peak_src, part_us, ncu_traffic(idx, kernel), kernel),
+        "e2e": {"value": round(e2e, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "breakdown_us": e2e_br},
+        "gpu_launches": 2 * args.steps,  # partial + combine per step
         "clocks": clk,
         "wall_s_timed_region": round(wall, 4),
     }
@@ -466,19 +552,22 @@ def run_ours(args):
             if j == idx:
                 continue
             try:
-                per[j] = measure_config(j, mv, dev, flush, peaks, args)
+                per[str(j)] = measure_workload(j, make_config(j), mv, dev, flush, peaks, peak_src,
+                                               10, 3, full=j >= 3)
             except Exception as e:
-                per[j] = {"error": repr(e)}
-        per[idx] = {"us": round(value, 3), "roofline_us": round(roof_us, 3),
-                    "frac": round(roof_us / value, 4), "bound": bound}
-        result["per_config"] = {str(k): per[k] for k in sorted(per)}
+                per[str(j)] = {"error": repr(e)}
+        per[str(idx)] = {"us": result["value"], "graph_us": result["graph_us"],
+                         "list_form_us": result["list_form_us"], "roofline_us": round(roof_us, 3),
+                         "frac": result["roofline_frac"], "bound": bound,
+                         "kv_gbps": result["kv_gbps"], "headline": True}
         # the mid workload once more with its keys in contiguous slots (the
         # defragmented placement), to compare gather cost
         try:
-            result["per_config"]["3c"] = measure_config(3, mv, dev, flush, peaks, args,
-                                                        placement="contiguous")
+            per["3c"] = measure_workload(3, make_config(3, placement="contiguous"), mv, dev, flush,
+                                         peaks, peak_src, 10, 3, full=False)
         except Exception as e:
-            result["per_config"]["3c"] = {"error": repr(e)}
+            per["3c"] = {"error": repr(e)}
+        result["per_config"] = {k: per[k] for k in sorted(per)}
         try:
             result["next_rows"] = measure_next_rows(mv, dev, flush, peaks)
         except Exception as e:
@@ -489,38 +578,19 @@ def run_ours(args):
         result["cpu_baseline"] = {"value": round(us, 1), "unit": UNIT, "cores": threads,
                                   "kind": "oracle", "sample": sample,
                                   "sample_seconds": round(dt, 2)}
+        if args.extras:
+            for j in (3, 4):
+                if j == idx or str(j) not in result.get("per_config", {}):
+                    continue
+                us, sample, threads, dt = time_oracle(make_config(j), target_s=3.0)
+                result["per_config"][str(j)]["cpu_baseline"] = {
+                    "value": round(us, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
+                    "sample": sample, "sample_seconds": round(dt, 2)}
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
-
-
-def measure_config(j, mv, dev, flush, peaks, args, steps=10, placement="scattered"):
-    import torch
-    inp = make_config(j, placement=placement)
-    fig = workload_figures(inp)
-    d = mv.to_device(inp, device=dev)
-    stream = torch.cuda.current_stream()
-    for _ in range(3):
-        flush()
-        d.step_paged()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps)]
-    for k in range(steps):
-        flush()
-        ev[k][0].record(stream)
-        d.step_paged()
-        ev[k][1].record(stream)
-    torch.cuda.synchronize()
-    us = statistics.mean(a.elapsed_time(b) * 1e3 for a, b in ev)
-    roof, bound, _, _ = roofline_us(fig, peaks)
-    ok = int(d.status.item()) == 0
-    del d
-    torch.cuda.empty_cache()
-    return {"us": round(us, 3), "roofline_us": round(roof, 3), "frac": round(roof / us, 4),
-            "bound": bound, "kv_gbps": round(fig["kv_bytes"] / (us * 1e-6) / 1e9, 1),
-            "status_ok": ok}
 
 
 def _time_us(fn, flush, steps=10, warm=3):
@@ -679,221 +749,26 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
-# ----------------------------------------------------------------- building-block probes
-PROBES = ("mma", "gather", "blocks", "dsmem", "mbar")
-
-
-def run_probes(which=PROBES):
-    """Microbenchmarks of the building blocks the kernels rely on (test-only
-    library libmlaselftest.so): 2-SM MMA issue rate, scattered-row gather
-    throughput, contiguous 8 KB block streams by copy method, mbarrier
-    operation costs and producer/consumer hand-over. Prints one table; not
-    part of the bench contract."""
-    import ctypes
-    import torch
-    from mla_speculative_decoding_gb300 import build as mbuild
-
-    lib = ctypes.CDLL(mbuild.build_selftest())
-    torch.cuda.set_device(0)
-    cyc = torch.zeros(1, dtype=torch.int64, device="cuda")
-    err = torch.zeros(1, dtype=torch.int32, device="cuda")
-
-    if "mma" in which:
-        _probe_mma(lib, cyc, err)
-    if "gather" in which:
-        _probe_gather(lib, err)
-    if "blocks" in which:
-        _probe_blocks(lib, err)
-    if "dsmem" in which:
-        _probe_dsmem(lib, err)
-    if "mbar" in which:
-        _probe_mbar(lib, cyc, err)
-
-
-def _probe_mma(lib, cyc, err):
-    import ctypes
-    import torch
-    # 2-SM MMA (M = 256, K = 16), single accumulator chain, tight issue loop.
-    f = lib.mlav_pair_probe
-    f.restype = ctypes.c_int
-    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 + [ctypes.c_void_p] * 3
-    g = torch.Generator().manual_seed(1)
-    A = torch.randn(256, 64, generator=g).to(torch.bfloat16).cuda()
-    addr = torch.zeros(2, dtype=torch.int32, device="cuda")
-    print("pair MMA (cta_group::2, M=256, K=16), cycles per MMA; peak = 128 (N=256) / 64 (N=128)")
-    for mode, N, label in ((1, 256, "A TMEM, B K-major"), (0, 256, "A smem, B K-major"),
-                           (2, 256, "A smem, B MN-major"), (1, 128, "A TMEM, B K-major")):
-        Bm = (torch.randn(N, 64, generator=g) if mode in (0, 1) else torch.randn(64, N, generator=g))
-        Bm = Bm.to(torch.bfloat16).cuda()
-        D = torch.zeros(256, N, dtype=torch.float32, device="cuda")
-        row = []
-        for var in (0, 2):
-            rc = f(A.data_ptr(), Bm.data_ptr(), D.data_ptr(), N, mode, 256, var, addr.data_ptr(),
-                   cyc.data_ptr(), err.data_ptr())
-            assert rc == 0 and int(err.item()) == 0
-            row.append(int(cyc.item()) / (4 * 256))
-        print(f"  N={N:3d} {label:20s}: plain {row[0]:6.1f}   with per-4-MMA barrier test, fences, commit {row[1]:6.1f}")
-
-
-
-def _probe_gather(lib, err):
-    import ctypes
-    import torch
-    # Scattered 128-byte row segments into shared memory, all SMs.
-    f = lib.mlav_gather_rate
-    f.restype = ctypes.c_int
-    f.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p] + [ctypes.c_int] * 5 + \
-        [ctypes.c_void_p] * 2
-    pool = 1_200_000
-    kv = torch.randn(pool, 576, device="cuda", dtype=torch.bfloat16)
-    nsm = torch.cuda.get_device_properties(0).multi_processor_count
-    cyc_sm = torch.zeros(nsm, dtype=torch.int64, device="cuda")
-    print("gather: bytes per clock per SM, 256 keys x 9 segments per tile, all SMs")
-    for label, hi in (("rows in HBM (1.2M-slot pool)", pool), ("rows L2-resident (20k slots)", 20000)):
-        rng = np.random.default_rng(0)
-        slots = torch.from_numpy(rng.integers(0, hi, size=nsm * 8 * 256).astype(np.int32)).cuda()
-        parts = []
-        for method, nw, tr in ((0, 2, 0), (0, 4, 0), (0, 8, 0), (0, 12, 0), (2, 1, 0), (4, 4, 32)):
-            for _ in range(2):
-                rc = f(kv.data_ptr(), pool, slots.data_ptr(), nsm, 8, method, nw, tr, cyc_sm.data_ptr(),
-                       err.data_ptr())
-            assert rc == 0 and int(err.item()) == 0
-            c = cyc_sm.float().mean().item()
-            name = {0: f"cp.async x{nw} warps", 2: "TMA gather4", 4: "cp.async x4 + gather4 1/8"}[method]
-            parts.append(f"{name} {8 * 9 * 256 * 128 / c:5.1f}")
-        print(f"  {label}: " + "; ".join(parts))
-
-    del kv
-    torch.cuda.empty_cache()
-
-
-def _probe_blocks(lib, err):
-    import ctypes
-    import torch
-    # Contiguous 8 KB blocks (the fp8 indexer cache) into a swizzled ring, all SMs.
-    f = lib.mlav_block_rate
-    f.restype = ctypes.c_int
-    f.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p] + [ctypes.c_int] * 4 + \
-        [ctypes.c_longlong] + [ctypes.c_void_p] * 2
-    nblk = 120_000                      # ~1 GB pool
-    rows = nblk * 8448 // 1152          # the same bytes as latent-cache rows
-    kv = torch.zeros(nblk * 8448, dtype=torch.uint8, device="cuda")
-    nsm = torch.cuda.get_device_properties(0).multi_processor_count
-    cyc_sm = torch.zeros(nsm, dtype=torch.int64, device="cuda")
-    ntile = 512
-    rng = np.random.default_rng(1)
-    blocks = torch.from_numpy(rng.integers(0, nblk, size=nsm * ntile * 2).astype(np.int32)).cuda()
-    row_slots = torch.from_numpy(rng.integers(0, rows, size=nsm * 128 * 126).astype(np.int32)).cuda()
-    print("8 KB blocks: bytes per clock per SM (and GB/s over all SMs), 2 blocks per 16 KB stage, "
-          "8-stage ring, all SMs")
-    for method, nw, label in ((0, 1, "TMA 3-D boxes"), (2, 1, "1-D bulk copies"),
-                              (1, 4, "cp.async x4 warps"), (1, 8, "cp.async x8 warps"),
-                              (3, 4, "TMA + cp.async x4 (half each)"),
-                              (3, 8, "TMA + cp.async x8 (half each)"),
-                              (4, 4, "ld.global x4 warps"), (4, 8, "ld.global x8 warps"),
-                              (5, 1, "TMA boxes + 256 B bulk scales"),
-                              (6, 1, "TMA boxes + 256 B TMA scale boxes"),
-                              (7, 8, "whole 1152 B rows, cp.async x8"),
-                              (7, 12, "whole 1152 B rows, cp.async x12"),
-                              (8, 8, "128 B of each row, cp.async x8"),
-                              (8, 12, "128 B of each row, cp.async x12"),
-                              (9, 1, "whole 1152 B rows, 1-D bulk copies")):
-        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-        nt = ntile if method < 7 else 128
-        idx = blocks if method < 7 else row_slots
-        for rep in range(2):
-            ev[0].record()
-            rc = f(kv.data_ptr(), nblk, idx.data_ptr(), nsm, nt, method, nw, rows,
-                   cyc_sm.data_ptr(), err.data_ptr())
-            ev[1].record()
-        assert rc == 0 and int(err.item()) == 0
-        torch.cuda.synchronize()
-        c = cyc_sm.float().mean().item()
-        stage = 16128 if method >= 7 else 16384
-        gbs = nsm * nt * stage / (ev[0].elapsed_time(ev[1]) * 1e-3) / 1e9
-        print(f"  {label:34s} {nt * stage / c:6.1f} B/clk   {gbs:7.0f} GB/s")
-    del kv
-    torch.cuda.empty_cache()
-
-
-def _probe_dsmem(lib, err):
-    import ctypes
-    import torch
-    # Bulk copies from one CTA's shared memory into its cluster peer's, through
-    # a 4-slot ring released by remote arrives (2-CTA clusters).
-    f = lib.mlav_bulk_rate
-    f.restype = ctypes.c_int
-    f.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p] * 2
-    nsm = torch.cuda.get_device_properties(0).multi_processor_count
-    cyc = torch.zeros(nsm, dtype=torch.int64, device="cuda")
-    print("DSMEM bulk copy CTA -> peer: bytes per clock per sending SM")
-    for ncl in (1, nsm // 2):
-        parts = []
-        for chunk in (4096, 16384, 32768):
-            n = (64 << 20) // chunk // max(1, ncl) + 64
-            rc = f(ncl, chunk, n, cyc.data_ptr(), err.data_ptr())
-            assert rc == 0 and int(err.item()) == 0
-            c = cyc[:ncl].float().mean().item()
-            parts.append(f"{chunk // 1024} KB chunks {n * chunk / c:5.1f}")
-        print(f"  {ncl:3d} cluster(s): " + "; ".join(parts))
-
-
-def _probe_mbar(lib, cyc, err):
-    import ctypes
-    import torch
-    # mbarrier operations (one thread) and a producer/consumer ring.
-    f = lib.mlav_mbar_cost
-    f.restype = ctypes.c_int
-    f.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
-    names = ["try_wait, phase complete", "test_wait, phase complete", "arrive",
-             "try_wait.acquire.cluster, complete", "arrive + try_wait"]
-    print("mbarrier, cycles per operation (one thread)")
-    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
-    for op in range(5):
-        rc = f(op, 4096, cyc.data_ptr(), sink.data_ptr())
-        assert rc == 0
-        print(f"  {names[op]:36s} {int(cyc.item()) / 4096:6.1f}")
-    f = lib.mlav_ring_probe
-    f.restype = ctypes.c_int
-    f.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p] * 2
-    print("empty ring (producer warp -> consumer thread, parking try_wait), cycles per stage")
-    for depth in (1, 8):
-        for pm in (0, 1):
-            for cm in (0, 1):
-                rc = f(depth, 4096, pm, cm, cyc.data_ptr(), err.data_ptr())
-                assert rc == 0 and int(err.item()) == 0
-                print(f"  depth {depth} producer {'cp.async arrive' if pm else 'arrive':15s} "
-                      f"consumer {'tcgen05.commit' if cm else 'arrive':14s} {int(cyc.item()) / 4096:6.1f}")
-
-
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=4, choices=sorted(CONFIGS))
+    ap.add_argument("--config", type=int, default=5, choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--simt", action="store_true", help="force the CUDA-core partial kernel")
     ap.add_argument("--no-extras", dest="extras", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-step-s", type=float, default=4.0)
-    ap.add_argument("--probes", nargs="*", choices=PROBES, default=None,
-                    help="run these building-block microbenchmarks (all if none named) "
-                         "instead of the bench")
     ap.add_argument("--next-rows", nargs="*", choices=NEXT_ROWS, default=None,
                     help="time only these steps beside the verify attention (all if none named) "
                          "and print their JSON instead of the bench line")
     args = ap.parse_args()
-    if args.probes is not None:
-        run_probes(args.probes or PROBES)
-        return
     if args.next_rows is not None:
         run_next_rows(args.next_rows or NEXT_ROWS)
         return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    args.flags = 1 if args.simt else 0
     if args.impl == "reference":
         run_reference(args)
     else:

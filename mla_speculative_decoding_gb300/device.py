@@ -114,6 +114,14 @@ class DeviceInputs:
                                      self.nsplit, self.workspace, self.out, self.lse,
                                      self.softmax_scale, stream)
 
+    def bound_step_paged(self, stream=None) -> B.BoundCall:
+        """step_paged with its arguments marshalled once (for a loop that
+        repeats the call on these fixed buffers)."""
+        return B.bind_verify_attention_paged(
+            self.q, self.kv_pool, self.req_to_token, self.req_pool_indices, self.prefix_lens,
+            self.out_cache_loc, self.tree_parent, self.T, self.nsplit, self.workspace, self.out,
+            self.lse, self.softmax_scale, stream)
+
     def partial_paged(self, stream=None):
         """The partial half of step_paged (combine() finishes it)."""
         B.mla_verify_partial_paged(self.q, self.kv_pool, self.req_to_token, self.req_pool_indices,

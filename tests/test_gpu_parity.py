@@ -3,8 +3,7 @@
 Every test calls the C ABI (through the thin binding) on seeded inputs and
 compares with the oracle run on the same inputs. Both kernel paths are
 covered: the default (the four-SM 2-SM-MMA kernel for requests of more
-than 128 rows, the two-SM kernel otherwise), the two-SM kernel forced, the
-single-SM tensor-core kernel and the CUDA-core one.
+than 128 rows, the two-SM kernel otherwise), and each of the two forced.
 """
 
 import numpy as np
@@ -16,8 +15,7 @@ from tests.gpu_util import config_cached, compare, host_out, oracle_ref, run_gpu
 from workloads import make_config, make_inputs
 
 pytestmark = pytest.mark.gpu
-PATHS = [0, mv.MLA_PARTIAL_PAIR, mv.MLA_PARTIAL_QUAD, mv.MLA_PARTIAL_SIMT,
-         mv.MLA_PARTIAL_TC_QUARTER]
+PATHS = [0, mv.MLA_PARTIAL_PAIR, mv.MLA_PARTIAL_QUAD]
 
 
 @pytest.mark.parametrize("flags", PATHS)
@@ -44,6 +42,21 @@ def test_configs_sampled_rows(idx, flags):
     ref_out, ref_lse = oracle_ref(inp, rows=rows)
     compare(out[rows], lse[rows], ref_out, ref_lse, f"config {idx} flags {flags}")
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+
+
+@pytest.mark.parametrize("idx", [4, 5])
+def test_configs_every_row_in_the_benchmark_call(idx):
+    """The long and batched workloads at full size through the call the
+    benchmark times (mla_verify_attention_paged): every output row and every
+    lse against the oracle."""
+    inp = config_cached(idx)
+    d = mv.to_device(inp)
+    d.step_paged()
+    torch.cuda.synchronize()
+    assert status(d) == 0
+    out, lse = host_out(d)
+    ref_out, ref_lse = oracle_ref(inp)
+    compare(out, lse, ref_out, ref_lse, f"config {idx}, every row, paged call")
 
 
 def test_config3_contiguous_placement():
