@@ -157,7 +157,9 @@ int run_combine(const void* workspace, int batch, int T, int num_heads, int nspl
     const unsigned char* ws = static_cast<const unsigned char*>(workspace);
     const cudaError_t e = launch_combine(
         reinterpret_cast<const float*>(ws + w.lse_off), reinterpret_cast<const float*>(ws + w.o_off),
-        batch * T * num_heads, nsplit, static_cast<__nv_bfloat16*>(out), lse,
+        batch * T * num_heads, nsplit,
+        T * num_heads <= 128 ? nsplit : quad_expected_parts(batch, T, num_heads, nsplit),
+        static_cast<__nv_bfloat16*>(out), lse,
         const_cast<int32_t*>(reinterpret_cast<const int32_t*>(ws)), stream);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

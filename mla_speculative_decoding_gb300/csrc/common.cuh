@@ -235,8 +235,11 @@ int check_attention_args(const void* q, const void* kv_pool, const int32_t* kv_i
 int ensure_device_ready(cudaStream_t stream);
 cudaError_t setup_noalloc(int device);
 
+// `live_hint`: the number of splits with keys a row is expected to have
+// (it only sets how the combine spreads a row's splits over threads).
 cudaError_t launch_combine(const float* lse_part, const float* o_part, int rows, int nsplit,
-                           __nv_bfloat16* out, float* lse, int32_t* status, cudaStream_t stream);
+                           int live_hint, __nv_bfloat16* out, float* lse, int32_t* status,
+                           cudaStream_t stream);
 
 cudaError_t launch_build_meta(const int32_t* req_to_token, int64_t stride, int64_t rows,
                               const int32_t* req_pool_indices, const int32_t* prefix_lens,

@@ -14,5 +14,8 @@ cudaError_t setup_partial_pair();
 // requests with more than 128 rows.
 cudaError_t launch_partial_quad(const PartialArgs& a, cudaStream_t stream);
 cudaError_t setup_partial_quad();
+// Partitions per query row the four-SM kernel's balanced plan is expected to
+// fill on the current device for this shape (a hint for the combine).
+int quad_expected_parts(int batch, int T, int H, int nsplit);
 
 }  // namespace mlav

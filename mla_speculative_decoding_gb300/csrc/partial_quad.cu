@@ -1189,6 +1189,16 @@ cudaError_t setup_partial_quad() {
     return cudaSuccess;
 }
 
+int quad_expected_parts(int batch, int T, int H, int nsplit) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nsplit;
+    const int C = g_quad_clusters[dev];
+    const long long pairs = (long long)batch * ((T * H + kRowsBlk - 1) / kRowsBlk);
+    if (C <= 0 || batch > kPlanMaxReq) return nsplit;  // rotated rounds: any partition may hold keys
+    const long long est = (C + pairs - 1) / pairs + 2;  // one range per cluster, plus its cut ends
+    return est < nsplit ? (int)est : nsplit;
+}
+
 cudaError_t launch_partial_quad(const PartialArgs& a, cudaStream_t stream) {
     const int rows_req = a.T * a.H;
     const int nrb = (rows_req + kRowsBlk - 1) / kRowsBlk;
