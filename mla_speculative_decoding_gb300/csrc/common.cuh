@@ -136,6 +136,19 @@ __device__ inline int build_anc_warp(const int32_t* par, int T, uint64_t* anc, i
     return __reduce_or_sync(0xffffffffu, bad);
 }
 
+// Visibility bits of 32 consecutive keys of a request, the first of which has
+// tree index u0 (key L_b + u0): keys with a negative tree index are prefix
+// keys, always visible; tree key u is visible iff bit u of `anc`, the row's
+// ancestor-or-self mask with no bit at or above T, is set.
+__device__ __forceinline__ uint32_t tree_keep_word(uint64_t anc, int u0) {
+    if (u0 >= 64) return 0u;
+    if (u0 >= 0) return (uint32_t)(anc >> u0);
+    if (u0 <= -32) return 0xffffffffu;
+    return (uint32_t)(anc << (-u0)) | ((1u << (-u0)) - 1u);
+}
+// The bits below T of a 64-bit mask.
+__device__ __forceinline__ uint64_t tree_bits(int T) { return T >= 64 ? ~0ull : ((1ull << T) - 1ull); }
+
 struct PartialArgs;
 
 // Internal launchers (defined in the kernel translation units).

@@ -387,7 +387,7 @@ partial_pair_kernel(const PartialArgs a) {
                 asm volatile("bar.sync 1, 256;" ::: "memory");
                 mbar_arrive(ba(S.q_ready));
             }
-            const uint64_t anc_t = S.anc[t];
+            const uint64_t anc_t = S.anc[t] & tree_bits(T);
             const uint32_t p_peer = mapa_shared(smem_u32(sm.u.o.p), peer);
             const uint32_t alpha_peer = mapa_shared(smem_u32(&sm.u.o.alpha[r]), peer);
             const uint32_t pfull_peer = mapa_shared(ba(sm.h.p_full), peer);
@@ -422,10 +422,7 @@ partial_pair_kernel(const PartialArgs a) {
                 const int k0 = kb + i * kNT + 128 * half;
                 if (k0 + 128 > Lb) {  // this half reaches the tree keys
 #pragma unroll
-                    for (int c = 0; c < 128; ++c) {
-                        const int u = k0 + c - Lb;
-                        if (u >= 0 && !(u < T && ((anc_t >> u) & 1ull))) vw[c >> 5] &= ~(1u << (c & 31));
-                    }
+                    for (int q = 0; q < 4; ++q) vw[q] &= tree_keep_word(anc_t, k0 + 32 * q - Lb);
                 }
                 // Max over the raw scores (the scale is positive, so scaling
                 // the max is exact); masked keys become -inf only where this

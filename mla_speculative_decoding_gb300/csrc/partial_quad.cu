@@ -765,7 +765,7 @@ partial_quad_kernel(const PartialArgs a) {
                         break;
                     }
                 }
-                const uint64_t anc_t = S.anc[t];
+                const uint64_t anc_t = S.anc[t] & tree_bits(T);
                 float m_ref = -INFINITY, l_part = 0.f;
                 for (int i = 0; i < it.ntiles; ++i, ++jt) {
                     if (!warp_wait(S.s_full, jt & 1, abort_p)) {
@@ -800,10 +800,7 @@ partial_quad_kernel(const PartialArgs a) {
                     const int k0 = it.kb + i * kNT + 128 * half;
                     if (k0 + 128 > it.Lb) {  // this half reaches the tree keys
 #pragma unroll
-                        for (int c = 0; c < 128; ++c) {
-                            const int u = k0 + c - it.Lb;
-                            if (u >= 0 && !(u < T && ((anc_t >> u) & 1ull))) vw[c >> 5] &= ~(1u << (c & 31));
-                        }
+                        for (int q = 0; q < 4; ++q) vw[q] &= tree_keep_word(anc_t, k0 + 32 * q - it.Lb);
                     }
                     // Max over the raw scores (the scale is positive, so scaling
                     // the max is exact); masked keys become -inf only where this
