@@ -146,6 +146,44 @@ __device__ __forceinline__ uint32_t tree_keep_word(uint64_t anc, int u0) {
     if (u0 <= -32) return 0xffffffffu;
     return (uint32_t)(anc << (-u0)) | ((1u << (-u0)) - 1u);
 }
+// Pairs of fp32 values in one 64-bit register (packed two-lane arithmetic,
+// one instruction for two keys) and a three-input maximum.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Maximum of 128 scores in eight independent chains of three-input maxima.
+__device__ __forceinline__ float max128(const float (&sc)[128]) {
+    float m8[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m8[j] = fmaxf(sc[j], sc[8 + j]);
+#pragma unroll
+    for (int c = 16; c < 128; c += 16)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) m8[j] = fmax3(m8[j], sc[c + j], sc[c + 8 + j]);
+    return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+}
+
 // The bits below T of a 64-bit mask.
 __device__ __forceinline__ uint64_t tree_bits(int T) { return T >= 64 ? ~0ull : ((1ull << T) - 1ull); }
 

@@ -811,15 +811,7 @@ partial_quad_kernel(const PartialArgs a) {
                         for (int c = 0; c < 128; ++c)
                             if (!((vw[c >> 5] >> (c & 31)) & 1u)) sc[c] = -INFINITY;
                     }
-                    {  // eight independent chains, then a tree
-                        float m8[8];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) m8[j] = sc[j];
-#pragma unroll
-                        for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], sc[c]);
-                        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-                    }
+                    mx = max128(sc);
                     mx *= sl;
                     S.mx[jt & 1][half][r] = mx;
                     __syncwarp();
@@ -845,12 +837,13 @@ partial_quad_kernel(const PartialArgs a) {
                         ok = false;
                         break;
                     }
-                    // p = 2^(s * scale_log2 - m_ref) in one FMA per key; masked
-                    // keys (-inf) give 2^-inf = 0; a row with no visible key yet
-                    // (m_ref = -inf) writes zeros.
-                    float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // eight chains
+                    // p = 2^(s * scale_log2 - m_ref), one packed FMA per two
+                    // keys; masked keys (-inf) give 2^-inf = 0, and a row with
+                    // no visible key yet (m_ref = -inf: every key of the tile
+                    // masked) writes zeros. Sums in four chains of key pairs.
                     const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
-                    const bool any = m_ref != -INFINITY;
+                    const uint64_t sl2 = f2_pack(sl, sl), nm2 = f2_pack(nm, nm);
+                    uint64_t ps4[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                     for (int blk = 0; blk < 2; ++blk) {
                         const uint32_t pb = p_local + (2 * half + blk) * kPBlock;
@@ -860,9 +853,11 @@ partial_quad_kernel(const PartialArgs a) {
 #pragma unroll
                             for (int u = 0; u < 4; ++u) {
                                 const int kk = blk * 64 + c * 8 + 2 * u;
-                                const float p0 = any ? ex2_approx(fmaf(sc[kk], sl, nm)) : 0.f;
-                                const float p1 = any ? ex2_approx(fmaf(sc[kk + 1], sl, nm)) : 0.f;
-                                ps8[(c & 3) * 2 + (u & 1)] += p0 + p1;
+                                float y0, y1;
+                                f2_unpack(f2_fma(f2_pack(sc[kk], sc[kk + 1]), sl2, nm2), y0, y1);
+                                const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+                                uint64_t& acc = ps4[(c & 1) * 2 + (u & 1)];
+                                acc = f2_add(acc, f2_pack(p0, p1));
                                 w[u] = pack_bf16x2(p0, p1);
                             }
                             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pb + sw128_offset(r, c)),
@@ -870,7 +865,12 @@ partial_quad_kernel(const PartialArgs a) {
                                          : "memory");
                         }
                     }
-                    l_part += ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
+                    {
+                        float q[8];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) f2_unpack(ps4[j], q[2 * j], q[2 * j + 1]);
+                        l_part += ((q[0] + q[1]) + (q[2] + q[3])) + ((q[4] + q[5]) + (q[6] + q[7]));
+                    }
                     if (half == 0) alpha_local[r] = alpha;
                     fence_proxy_async_smem();
                     __syncwarp();
