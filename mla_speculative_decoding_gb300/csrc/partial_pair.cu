@@ -433,7 +433,15 @@ partial_pair_kernel(const PartialArgs a) {
                     for (int c = 0; c < 128; ++c)
                         if (!((vw[c >> 5] >> (c & 31)) & 1u)) sc[c] = -INFINITY;
                 }
-                mx = max128(sc);
+                {  // eight independent chains, then a tree
+                    float m8[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) m8[j] = sc[j];
+#pragma unroll
+                    for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], sc[c]);
+                    mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                }
                 mx *= a.scale_log2;
                 S.mx[i & 1][half][r] = mx;
                 mbar_arrive(ba(S.mx_bar[i & 1]));
@@ -457,14 +465,13 @@ partial_pair_kernel(const PartialArgs a) {
                     break;
                 }
                 // P (bf16) -> the O-CTA's A-operand tile, 8 keys (16 bytes) at a time.
-                // p = 2^(s * scale_log2 - m_ref), one packed FMA per two keys;
-                // masked keys (-inf) give 2^-inf = 0, and a row with no
-                // visible key yet (m_ref = -inf: every key of the tile masked)
-                // writes zeros. Sums in four chains of key pairs.
+                // p = 2^(s * scale_log2 - m_ref) in one FMA per key; masked
+                // keys (-inf) give 2^-inf = 0; a row with no visible key yet
+                // (m_ref = -inf) writes zeros.
+                float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // eight chains
                 const float sl = a.scale_log2;
                 const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
-                const uint64_t sl2 = f2_pack(sl, sl), nm2 = f2_pack(nm, nm);
-                uint64_t ps4[4] = {0ull, 0ull, 0ull, 0ull};
+                const bool any = m_ref != -INFINITY;
 #pragma unroll
                 for (int blk = 0; blk < 2; ++blk) {
                     const uint32_t pb = p_peer + (2 * half + blk) * kPBlock;
@@ -474,22 +481,15 @@ partial_pair_kernel(const PartialArgs a) {
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
                             const int k = blk * 64 + c * 8 + 2 * u;
-                            float y0, y1;
-                            f2_unpack(f2_fma(f2_pack(sc[k], sc[k + 1]), sl2, nm2), y0, y1);
-                            const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
-                            uint64_t& acc = ps4[(c & 1) * 2 + (u & 1)];
-                            acc = f2_add(acc, f2_pack(p0, p1));
+                            const float p0 = any ? ex2_approx(fmaf(sc[k], sl, nm)) : 0.f;
+                            const float p1 = any ? ex2_approx(fmaf(sc[k + 1], sl, nm)) : 0.f;
+                            ps8[(c & 3) * 2 + (u & 1)] += p0 + p1;
                             w[u] = pack_bf16x2(p0, p1);
                         }
                         st_cluster_v4(pb + sw128_offset(r, c), w[0], w[1], w[2], w[3]);
                     }
                 }
-                {
-                    float q[8];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) f2_unpack(ps4[j], q[2 * j], q[2 * j + 1]);
-                    l_part += ((q[0] + q[1]) + (q[2] + q[3])) + ((q[4] + q[5]) + (q[6] + q[7]));
-                }
+                l_part += ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
                 if (half == 0) st_cluster_f32(alpha_peer, alpha);
                 fence_proxy_async_all();
                 mbar_arrive_cluster(pfull_peer);
