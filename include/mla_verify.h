@@ -170,8 +170,9 @@ int mla_build_verify_meta(const int32_t *req_to_token, int64_t req_to_token_stri
  *   T            tree tokens per request, 1..64
  *   nsplit       KV partitions per request, 1..128: request b's L_b + T keys
  *                are cut into at most nsplit contiguous ranges (the pages cut
- *                ceil((L_b+T)/nsplit)-key chunks; the kernels cut at 256-key
- *                tiles and balance the ranges over the SMs); each range gives
+ *                ceil((L_b+T)/nsplit)-key chunks; the kernels balance the
+ *                ranges over the SMs, mostly at 256-key tiles, and may use
+ *                fewer ranges, depending on the launch); each range gives
  *                one partial result per query row and empty ranges give
  *                lse = -inf ([VK] Part VII: NSPLIT multiplies the number of
  *                partials)

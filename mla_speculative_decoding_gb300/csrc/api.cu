@@ -135,6 +135,7 @@ PartialArgs make_partial_args(const void* q, const void* kv_pool, const int32_t*
     a.pool_slots = pool_slots;
     a.scale_log2 = softmax_scale * kLog2e;
     a.wave_full = 0x7fffffff;  // no wave shaping unless a launcher sets it
+    a.parts = 0;
     a.req_to_token = nullptr;  // the combined-list form
     a.r2t_stride = a.r2t_rows = 0;
     a.req_pool_indices = nullptr;
@@ -158,7 +159,8 @@ int run_combine(const void* workspace, int batch, int T, int num_heads, int nspl
     const cudaError_t e = launch_combine(
         reinterpret_cast<const float*>(ws + w.lse_off), reinterpret_cast<const float*>(ws + w.o_off),
         batch * T * num_heads, nsplit,
-        T * num_heads <= 128 ? nsplit : quad_expected_parts(batch, T, num_heads, nsplit),
+        T * num_heads <= 128 ? pair_expected_parts(batch, T, num_heads, nsplit)
+                             : quad_expected_parts(batch, T, num_heads, nsplit),
         static_cast<__nv_bfloat16*>(out), lse,
         const_cast<int32_t*>(reinterpret_cast<const int32_t*>(ws)), stream);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;

@@ -205,6 +205,8 @@ struct PartialArgs {
     int64_t pool_slots;
     float scale_log2;  // softmax_scale * log2(e)
     int wave_full;     // first item of the last, partial wave (split_range_waves)
+    int parts;         // > 0: the two-SM kernel's split over this many partitions,
+                       // all in one wave (split_range_one_wave); 0: wave-shaped
     // Paged form (kv_indices == nullptr): request b's keys are its table row
     // req_to_token[req_pool_indices[b]][0, L_b) followed by its T draft slots
     // out_cache_loc[b*T, b*T + T), read where the combined list would be.

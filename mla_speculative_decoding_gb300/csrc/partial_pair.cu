@@ -110,6 +110,13 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 __device__ __forceinline__ uint32_t ba(const uint64_t& b) { return smem_u32(&b); }
 
+// Keys of tile i of the partition [kb, ke) (a prefix of the tile; >= 1 for
+// i < the partition's tile count).
+__device__ __forceinline__ int tile_keys(int kb, int ke, int i) { return min(kNT, ke - kb - i * kNT); }
+// V stages (32 keys each) holding keys of that tile: the V producers and the
+// P V issuer both walk exactly these.
+__device__ __forceinline__ int tile_vstages(int kb, int ke, int i) { return (tile_keys(kb, ke, i) + 31) >> 5; }
+
 __device__ __forceinline__ bool warp_wait(const uint64_t& bar, uint32_t parity,
                                           volatile int* abort) {
     const bool ok = mbar_wait(ba(bar), parity, abort);
@@ -139,20 +146,26 @@ partial_pair_kernel(const PartialArgs a) {
     int bad = request_keys(a, b, Lb, K);
     int kb, ke;
     const int nrb_req = (a.T * a.H + kM - 1) / kM;
-    split_range_waves(K, a.nsplit, s, kNT, b * nrb_req + rb, a.batch * nrb_req, a.wave_full, kb, ke);
+    if (a.parts > 0)  // one wave; partitions past a.parts not launched
+        split_range_one_wave(K, a.parts, s, kNT, kb, ke);
+    else
+        split_range_waves(K, a.nsplit, s, kNT, b * nrb_req + rb, a.batch * nrb_req, a.wave_full, kb, ke);
     const int ntiles = (ke - kb + kNT - 1) / kNT;
     const int64_t kbase = key_base(a, b);
 
-    if (ntiles <= 0) {  // empty split (fixed grid, early exit): lse = -inf, o = 0
-        if (rank == 1 && warp >= 8 && warp < 12) {
-            const int grow = rb * kM + 32 * (warp & 3) + lane;
-            if (grow < rows_req) {
-                const int64_t pid = ((int64_t)b * rows_req + grow) * a.nsplit + s;
-                float4* o = reinterpret_cast<float4*>(a.o_part + pid * kDv);
-                for (int c = 0; c < kDv / 4; ++c) o[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-                a.lse_part[pid] = -INFINITY;
-            }
+    // lse = -inf for this item's empty partitions: its own if it has no
+    // keys, and the unlaunched partitions s + parts, s + 2 parts, ... (the
+    // combine reads no o of a split whose lse is -inf)
+    if (rank == 1 && warp >= 8 && warp < 12) {
+        const int grow = rb * kM + 32 * (warp & 3) + lane;
+        if (grow < rows_req) {
+            float* lp = a.lse_part + ((int64_t)b * rows_req + grow) * a.nsplit;
+            if (ntiles <= 0) lp[s] = -INFINITY;
+            if (a.parts > 0)
+                for (int s2 = s + a.parts; s2 < a.nsplit; s2 += a.parts) lp[s2] = -INFINITY;
         }
+    }
+    if (ntiles <= 0) {  // empty split (fixed grid, early exit)
         if (rank == 0 && tid == 0) status_or(a.status, bad);
         return;
     }
@@ -260,6 +273,7 @@ partial_pair_kernel(const PartialArgs a) {
                     ok = false;
                     break;
                 }
+                const int nit = (tile_keys(kb, ke, i) + 3) >> 2;  // 4 keys per warp step
                 for (int kbk = 0; kbk < kDqk / 64; ++kbk) {
                     const int g = i * (kDqk / 64) + kbk;
                     const int st = g % kKStages;
@@ -267,8 +281,11 @@ partial_pair_kernel(const PartialArgs a) {
                         ok = false;
                         break;
                     }
+                    // Only the rows up to the tile's last key (rounded up to a
+                    // warp step) are copied; the rest of the stage keeps stale
+                    // data, whose scores are masked.
                     const uint32_t dst0 = smem_u32(S.kring[st]);
-                    for (int it = pw; it < 64; it += kSProd) {
+                    for (int it = pw; it < nit; it += kSProd) {
                         const int key = it * 4 + (lane >> 3), c = lane & 7;
                         const int32_t slot = S.rows[rb2][key];
                         const __nv_bfloat16* src =
@@ -299,6 +316,10 @@ partial_pair_kernel(const PartialArgs a) {
                         break;
                     }
                     tc_fence_after();
+                    // a partly filled tile: N = its keys rounded up to 16 (the
+                    // score columns past them keep stale values, all masked)
+                    const int nv = tile_keys(kb, ke, i);
+                    const uint32_t idt = nv >= kNT ? idesc : make_idesc_bf16(kM, (nv + 15) & ~15, false, false);
                     for (int kbk = 0; kbk < kDqk / 64; ++kbk) {
                         const int g = i * (kDqk / 64) + kbk;
                         const int st = g % kKStages;
@@ -311,15 +332,15 @@ partial_pair_kernel(const PartialArgs a) {
                         const uint64_t bd = kdesc0 + (uint64_t)st * (kKBlock >> 4);
                         if (kbk < 8) {
                             const uint32_t aa = tbase + kColQ + kbk * 32;
-                            mma_ts(dS, aa, bd, idesc, kbk > 0 ? 1u : 0u);
-                            mma_ts(dS, aa + 8, bd + 2, idesc, 1u);
-                            mma_ts(dS, aa + 16, bd + 4, idesc, 1u);
-                            mma_ts(dS, aa + 24, bd + 6, idesc, 1u);
+                            mma_ts(dS, aa, bd, idt, kbk > 0 ? 1u : 0u);
+                            mma_ts(dS, aa + 8, bd + 2, idt, 1u);
+                            mma_ts(dS, aa + 16, bd + 4, idt, 1u);
+                            mma_ts(dS, aa + 24, bd + 6, idt, 1u);
                         } else {
-                            mma_ss(dS, qrdesc, bd, idesc, 1u);
-                            mma_ss(dS, qrdesc + 2, bd + 2, idesc, 1u);
-                            mma_ss(dS, qrdesc + 4, bd + 4, idesc, 1u);
-                            mma_ss(dS, qrdesc + 6, bd + 6, idesc, 1u);
+                            mma_ss(dS, qrdesc, bd, idt, 1u);
+                            mma_ss(dS, qrdesc + 2, bd + 2, idt, 1u);
+                            mma_ss(dS, qrdesc + 4, bd + 4, idt, 1u);
+                            mma_ss(dS, qrdesc + 6, bd + 6, idt, 1u);
                         }
                         mma_commit(ba(S.k_empty[st]));
                     }
@@ -398,15 +419,20 @@ partial_pair_kernel(const PartialArgs a) {
                     ok = false;
                     break;
                 }
+                // Keys of this half of the tile: a half without any has no
+                // scores to read and no P that the P V steps read.
+                const int hk = tile_keys(kb, ke, i) - 128 * half;
                 tc_fence_after();
                 float sc[128];
+                if (hk > 0) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t w[32];
-                    tmem_ld32(tbase + lb + kColS + half * 128 + c * 32, w);
-                    tmem_wait_ld();
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t w[32];
+                        tmem_ld32(tbase + lb + kColS + half * 128 + c * 32, w);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) sc[c * 32 + u] = __uint_as_float(w[u]);
+                        for (int u = 0; u < 32; ++u) sc[c * 32 + u] = __uint_as_float(w[u]);
+                    }
                 }
                 tc_fence_before();
                 mbar_arrive(ba(S.s_free));
@@ -428,12 +454,12 @@ partial_pair_kernel(const PartialArgs a) {
                 // the max is exact); masked keys become -inf only where this
                 // row's half-tile has any.
                 float mx = -INFINITY;
-                if ((vw[0] & vw[1] & vw[2] & vw[3]) != 0xffffffffu) {
+                if (hk > 0 && (vw[0] & vw[1] & vw[2] & vw[3]) != 0xffffffffu) {
 #pragma unroll
                     for (int c = 0; c < 128; ++c)
                         if (!((vw[c >> 5] >> (c & 31)) & 1u)) sc[c] = -INFINITY;
                 }
-                {  // eight independent chains, then a tree
+                if (hk > 0) {  // eight independent chains, then a tree
                     float m8[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) m8[j] = sc[j];
@@ -474,6 +500,7 @@ partial_pair_kernel(const PartialArgs a) {
                 const bool any = m_ref != -INFINITY;
 #pragma unroll
                 for (int blk = 0; blk < 2; ++blk) {
+                    if (hk <= 64 * blk) break;  // keys from here on are past the tile's last 16-key step
                     const uint32_t pb = p_peer + (2 * half + blk) * kPBlock;
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
@@ -513,6 +540,7 @@ partial_pair_kernel(const PartialArgs a) {
             // split the 16-byte copies (32 lanes = one half of a 1024-byte V row).
             const int pw = warp < kWarpMMA ? warp : (warp < 8 ? warp - 1 : warp - 5);  // 0..10
             bool ok = true;
+            int g = 0;  // V stages so far (a tile takes only the stages holding its keys)
             for (int i = 0; ok && i < ntiles; ++i) {
                 const int rb2 = i & 1;
                 if (pw == 0) {
@@ -537,15 +565,19 @@ partial_pair_kernel(const PartialArgs a) {
                     ok = false;
                     break;
                 }
-                for (int q = 0; q < 8; ++q) {
-                    const int g = i * 8 + q;
+                // keys the P V steps read: the tile's keys rounded up to 16
+                // (zeros where there is no pool row, so that p = 0 adds 0)
+                const int nv16 = (tile_keys(kb, ke, i) + 15) & ~15;
+                const int nq = tile_vstages(kb, ke, i);
+                for (int q = 0; q < nq; ++q, ++g) {
                     const int st = g % kVStages;
                     if (g >= kVStages && !warp_wait(O.v_empty[st], ((g / kVStages) - 1) & 1, abort_p)) {
                         ok = false;
                         break;
                     }
                     const uint32_t dst0 = smem_u32(O.vring[st]);
-                    for (int it = pw; it < 64; it += kOProd) {
+                    const int nit = 2 * min(kVKeys, nv16 - kVKeys * q);  // two lanes' chunks per key
+                    for (int it = pw; it < nit; it += kOProd) {
                         const int kl = it >> 1;                 // key within the stage
                         const int c = (it & 1) * 32 + lane;     // 16-byte chunk of the V row
                         const int32_t slot = O.rows[rb2][32 * q + kl];
@@ -572,6 +604,7 @@ partial_pair_kernel(const PartialArgs a) {
                 const uint32_t vlo = (uint32_t)vdesc0, vhi = (uint32_t)(vdesc0 >> 32);
                 auto dsc = [](uint32_t lo, uint32_t hi) { return ((uint64_t)hi << 32) | lo; };
                 bool ok = true;
+                int g = 0;  // V stages so far, as counted by the V producers
                 for (int i = 0; ok && i < ntiles; ++i) {
                     if (!mbar_wait_cluster(ba(sm.h.p_full), i & 1, abort_p) ||
                         !mbar_wait(ba(O.o_gate), i & 1, abort_p)) {
@@ -580,8 +613,9 @@ partial_pair_kernel(const PartialArgs a) {
                     }
                     fence_proxy_async_smem();
                     tc_fence_after();
-                    for (int q = 0; q < 8; ++q) {
-                        const int g = i * 8 + q;
+                    const int nv = tile_keys(kb, ke, i);
+                    const int nq = tile_vstages(kb, ke, i);
+                    for (int q = 0; q < nq; ++q, ++g) {
                         const int st = g % kVStages;
                         if (!mbar_wait(ba(O.v_full[st]), (g / kVStages) & 1, abort_p)) {
                             ok = false;
@@ -593,10 +627,14 @@ partial_pair_kernel(const PartialArgs a) {
                         // keys q*32 .. q*32+31 of the tile: P block q / 2, 16-key steps
                         const uint32_t pd = plo + (uint32_t)((q >> 1) * kPBlock + (q & 1) * 64) / 16;
                         const uint32_t acc0 = (i > 0 || q > 0) ? 1u : 0u;
-                        mma_ss(tbase, dsc(pd, phi), dsc(vd, vhi), idesc, acc0);
-                        mma_ss(tbase + 256, dsc(pd, phi), dsc(vd + (4 * kVBlock) / 16, vhi), idesc, acc0);
-                        mma_ss(tbase, dsc(pd + 2, phi), dsc(vd + 2048 / 16, vhi), idesc, 1u);
-                        mma_ss(tbase + 256, dsc(pd + 2, phi), dsc(vd + (4 * kVBlock + 2048) / 16, vhi), idesc, 1u);
+                        if (kVKeys * q < nv) {  // 16-key steps holding keys of the tile
+                            mma_ss(tbase, dsc(pd, phi), dsc(vd, vhi), idesc, acc0);
+                            mma_ss(tbase + 256, dsc(pd, phi), dsc(vd + (4 * kVBlock) / 16, vhi), idesc, acc0);
+                        }
+                        if (kVKeys * q + 16 < nv) {
+                            mma_ss(tbase, dsc(pd + 2, phi), dsc(vd + 2048 / 16, vhi), idesc, 1u);
+                            mma_ss(tbase + 256, dsc(pd + 2, phi), dsc(vd + (4 * kVBlock + 2048) / 16, vhi), idesc, 1u);
+                        }
                         mma_commit(ba(O.v_empty[st]));
                     }
                     if (!ok) break;
@@ -726,15 +764,29 @@ cudaError_t setup_partial_pair() {
     return cudaSuccess;
 }
 
+static int pair_resident() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    return g_pair_clusters[dev];
+}
+
+int pair_expected_parts(int batch, int T, int H, int nsplit) {
+    const int p = one_wave_parts((long long)batch * ((T * H + kM - 1) / kM), pair_resident(), nsplit);
+    return p > 0 ? p : nsplit;
+}
+
 cudaError_t launch_partial_pair(const PartialArgs& a, cudaStream_t stream) {
     const int rows_req = a.T * a.H;
     const int nrb = (rows_req + kM - 1) / kM;
-    dim3 grid(2 * nrb, a.batch, a.nsplit);
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+    const int resident = pair_resident();
     PartialArgs w = a;
-    w.wave_full = wave_full_items((long long)a.batch * a.nsplit * nrb,
-                                  dev >= 0 && dev < 64 ? g_pair_clusters[dev] : 0);
+    // When every (request, row block) pair can take at least one cluster of
+    // one wave, the keys are split evenly over as many partitions as the
+    // wave holds (up to nsplit), and only those are launched; otherwise all
+    // nsplit partitions are, with the wave-shaped split.
+    w.parts = one_wave_parts((long long)a.batch * nrb, resident, a.nsplit);
+    w.wave_full = wave_full_items((long long)a.batch * a.nsplit * nrb, resident);
+    const dim3 grid(2 * nrb, a.batch, w.parts > 0 ? w.parts : a.nsplit);
     return launch_pdl(partial_pair_kernel, grid, dim3(kThreads), kSmemBytes, stream, w);
 }
 

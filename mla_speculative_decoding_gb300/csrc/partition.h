@@ -67,6 +67,51 @@ MLAV_HD inline void split_range_waves(int K, int nsplit, int s, int tile, int it
     end = mlav_min(K, (t0 + nt) * tile);
 }
 
+// Even split of K keys over `parts` partitions for launches in which all of
+// them run at once: partition s < parts takes keys [floor(s K / parts),
+// floor((s + 1) K / parts)), so sizes differ by at most one key and a
+// request's largest partition holds ceil(K / parts) keys (the same number of
+// 256-key tiles as the largest tile-aligned partition, but no more keys);
+// partitions at or past `parts` are empty.
+MLAV_HD inline void split_range_keys(int K, int parts, int s, int& beg, int& end) {
+    if (parts <= 0 || s >= parts) {
+        beg = end = K;
+        return;
+    }
+    beg = (int)((long long)K * s / parts);
+    end = (int)((long long)K * (s + 1) / parts);
+}
+
+// Split of K keys over `parts` partitions that all run at once (one wave):
+// with no more tiles than partitions, the even key split (every partition at
+// most one tile, as few keys as possible); otherwise whole tiles, shared as
+// evenly as possible with the extra tiles on the last partitions, so that
+// the request's last, partly filled tile is one of them and as few
+// partitions as possible hold a tile more than the rest.
+MLAV_HD inline void split_range_one_wave(int K, int parts, int s, int tile, int& beg, int& end) {
+    const int tiles = (K + tile - 1) / tile;
+    if (tiles <= parts || s >= parts) {
+        split_range_keys(K, parts, s, beg, end);
+        return;
+    }
+    const int base = tiles / parts, lo = parts - tiles % parts;  // partitions [lo, parts) take base + 1
+    const int t0 = s * base + (s > lo ? s - lo : 0);
+    const int nt = base + (s >= lo ? 1 : 0);
+    beg = mlav_min(K, t0 * tile);
+    end = mlav_min(K, (t0 + nt) * tile);
+}
+
+// Partitions per (request, row block) pair for a launch of `pairs` pairs on
+// `resident` clusters of one CTA pair each when each partition is one
+// cluster: as many as one wave of resident clusters holds, at most nsplit;
+// 0 (no even key split: the wave-shaped split instead) when the pairs do not
+// fit one wave or the resident count is unknown.
+inline int one_wave_parts(long long pairs, int resident, int nsplit) {
+    if (resident <= 0 || pairs <= 0 || pairs > resident) return 0;
+    const long long p = resident / pairs;
+    return (int)(p < nsplit ? p : nsplit);
+}
+
 // Index of the first item of the last, partial wave when `items` work items
 // run on `resident` clusters at a time (items when every wave is full or
 // when there is no more than one wave, or the resident count is unknown).

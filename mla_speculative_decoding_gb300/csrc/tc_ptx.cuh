@@ -138,6 +138,10 @@ __device__ __forceinline__ void cp_async_16_zfill_nc(uint32_t dst, const void* s
     const uint32_t n = valid ? 16u : 0u;
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n));
 }
+// Plain 16-byte copy without a compiler memory barrier (see above).
+__device__ __forceinline__ void cp_async_16_nc(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src));
+}
 // The mbarrier receives one arrival when all of this thread's earlier
 // cp.async copies have landed (the arrival counts toward the expected count).
 __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {

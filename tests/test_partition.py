@@ -5,7 +5,9 @@ boundaries; the tensor-core kernels' wave-shaped split keeps every partition
 non-empty once there are 2 * nsplit tiles, gives the items of the last,
 partial wave of resident clusters one tile each, and shares the rest evenly;
 and the first index of the partial wave is the largest multiple of the
-resident count (or the item count when there is at most one wave)."""
+resident count (or the item count when there is at most one wave). The
+two-SM kernel's one-wave split cuts the keys, not tiles, evenly over as
+many partitions as one wave of resident clusters holds."""
 
 import os
 import subprocess
@@ -45,22 +47,58 @@ int main() {
         split_range_tiles(K, ns, s, tile, beg, end);
         printf("T %d %d %d %d %d\n", K, ns, s, beg, end);
     }
+    for (int K : Ks) for (int ns : nsplits) for (int s = 0; s < ns + 2; ++s) {
+        int beg, end;
+        split_range_keys(K, ns, s, beg, end);
+        printf("K %d %d %d %d %d\n", K, ns, s, beg, end);
+    }
+    for (int K : Ks) for (int ns : nsplits) for (int s = 0; s < ns + 2; ++s) {
+        int beg, end;
+        split_range_one_wave(K, ns, s, tile, beg, end);
+        printf("Q %d %d %d %d %d\n", K, ns, s, beg, end);
+    }
+    const long long pairs[] = {0, 1, 2, 16, 19, 76, 77, 1000};
+    const int res2[] = {-1, 0, 36, 76};
+    for (long long p : pairs) for (int r : res2) for (int ns : nsplits)
+        printf("O %lld %d %d %d\n", p, r, ns, one_wave_parts(p, r, ns));
     return 0;
 }
 '''
 
 
 @pytest.fixture(scope="module")
-def table(tmp_path_factory):
+def harness_out(tmp_path_factory):
     d = tmp_path_factory.mktemp("partition")
     src, exe = d / "harness.cpp", d / "harness"
     src.write_text(HARNESS)
     subprocess.run(["g++", "-O1", "-std=c++17", "-I", CSRC, str(src), "-o", str(exe)], check=True,
                    capture_output=True)
-    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
-    waves, parts, even = [], {}, {}
-    for line in out.splitlines():
+    return subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+
+
+@pytest.fixture(scope="module")
+def key_table(harness_out):
+    keys, owp, onew = {}, [], {}
+    for line in harness_out.splitlines():
         f = line.split()
+        if f[0] == "K":
+            K, ns, s, beg, end = (int(x) for x in f[1:])
+            keys.setdefault((K, ns), []).append((s, beg, end))
+        elif f[0] == "Q":
+            K, ns, s, beg, end = (int(x) for x in f[1:])
+            onew.setdefault((K, ns), []).append((s, beg, end))
+        elif f[0] == "O":
+            owp.append(tuple(int(x) for x in f[1:]))
+    return keys, owp, onew
+
+
+@pytest.fixture(scope="module")
+def table(harness_out):
+    waves, parts, even = [], {}, {}
+    for line in harness_out.splitlines():
+        f = line.split()
+        if f[0] in ("K", "O", "Q"):
+            continue
         if f[0] == "W":
             waves.append(tuple(int(x) for x in f[1:]))
         elif f[0] == "P":
@@ -268,3 +306,75 @@ def test_long_workload_plan():
         parts[b0 // 722] += 1
         assert b0 // 722 == (e0 - 1) // 722, "no cluster spans both row blocks"
     assert set(sizes) <= {40, 41} and parts == {0: 18, 1: 18}
+
+
+def test_even_key_split(key_table):
+    """split_range_keys: partitions 0..parts-1 tile [0, K) in order with sizes
+    that differ by at most one key, the largest one ceil(K / parts) keys in
+    no more 256-key tiles than the largest tile-aligned partition; those at
+    or past `parts` are empty at K. The mid workload (65,552 keys over 64
+    partitions) gets 16 partitions of 1025 keys and 48 of 1024."""
+    keys, _, _ = key_table
+    for (K, ns), ranges in keys.items():
+        ranges.sort()
+        pos = 0
+        for s, beg, end in ranges:
+            if s >= ns:
+                assert beg == end == K
+                continue
+            assert beg == pos and end >= beg
+            pos = end
+        assert pos == K
+        sizes = [e - b for s, b, e in ranges if s < ns]
+        assert max(sizes) - min(sizes) <= 1 and max(sizes) == -(-K // ns)
+        tiles = -(-K // 256)
+        assert -(-max(sizes) // 256) == -(-tiles // ns)
+    mid = [e - b for s, b, e in sorted(keys[(65552, 64)]) if s < 64]
+    assert sorted(mid) == [1024] * 48 + [1025] * 16
+
+
+def test_one_wave_parts(key_table):
+    """Partitions per pair for the one-wave split: floor(resident / pairs)
+    capped at nsplit, and 0 (the wave-shaped split) when the pairs exceed one
+    wave or the resident count is unknown."""
+    _, owp, _ = key_table
+    for pairs, res, ns, got in owp:
+        if res <= 0 or pairs <= 0 or pairs > res:
+            assert got == 0
+        else:
+            assert got == min(ns, res // pairs) and got >= 1
+    got = {(p, r, n): g for p, r, n, g in owp}
+    assert got[(1, 76, 64)] == 64      # the mid workload: all 64 partitions in one wave
+    assert got[(16, 76, 8)] == 4       # sparse decode: 16 requests x 4 partitions
+    assert got[(77, 76, 64)] == 0      # more pairs than clusters: wave-shaped
+
+
+def test_one_wave_split(key_table):
+    """split_range_one_wave: with no more tiles than partitions, the even key
+    split; otherwise tile-aligned ranges in order whose tile counts differ by
+    at most one, the larger ones last (so the last, partly filled tile sits
+    in one of them); partitions at or past `parts` are empty. The mid
+    workload (65,552 keys = 256 full tiles and one of 16 keys, 64
+    partitions): partitions 0-62 take 4 full tiles, partition 63 four and
+    the 16-key one."""
+    keys, _, onew = key_table
+    for (K, ns), ranges in onew.items():
+        ranges.sort()
+        tiles = -(-K // 256)
+        if tiles <= ns:
+            assert ranges == sorted(keys[(K, ns)])
+            continue
+        pos, sizes = 0, []
+        for s, beg, end in ranges:
+            if s >= ns:
+                assert beg == end == K
+                continue
+            assert beg == pos and end > beg
+            assert beg % 256 == 0 and (end % 256 == 0 or end == K)
+            sizes.append(-(-(end - beg) // 256))
+            pos = end
+        assert pos == K
+        assert max(sizes) - min(sizes) <= 1 and sizes == sorted(sizes)
+    mid = sorted(onew[(65552, 64)])
+    assert all(e - b == 1024 for s, b, e in mid[:63])
+    assert (mid[63][1], mid[63][2]) == (64512, 65552)
