@@ -714,12 +714,15 @@ partial_pair_kernel(const PartialArgs a) {
                             __uint_as_float(o[4 * u]) * inv, __uint_as_float(o[4 * u + 1]) * inv,
                             __uint_as_float(o[4 * u + 2]) * inv, __uint_as_float(o[4 * u + 3]) * inv);
                     __syncwarp();
+                    // all eight tile reads before the first store (the stores
+                    // may not be ordered ahead of later reads of the tile)
+                    float4 v[8];
 #pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        const float4 v = *reinterpret_cast<const float4*>(tile + (4 * g + jr) * kOTileStride + jc);
-                        if (rj0 + 4 * g < rows_req)
-                            *reinterpret_cast<float4*>(o0 + g * gstep + c0) = v;
-                    }
+                    for (int g = 0; g < 8; ++g)
+                        v[g] = *reinterpret_cast<const float4*>(tile + (4 * g + jr) * kOTileStride + jc);
+#pragma unroll
+                    for (int g = 0; g < 8; ++g)
+                        if (rj0 + 4 * g < rows_req) *reinterpret_cast<float4*>(o0 + g * gstep + c0) = v[g];
                     __syncwarp();
                 }
                 if (row_ok)
