@@ -14,7 +14,7 @@
 //     36 per tile). TMEM: Q's 512 latent dims [0, 256) as the A operand, S
 //     [256, 512). Q's 64 RoPE dims are an A operand in shared memory. K is
 //     streamed in 64-dim blocks of 256 keys (32 KB, 6-stage ring), gathered
-//     from the scattered rows by seven warps of 16-byte cp.async copies
+//     from the scattered rows by six warps of 16-byte cp.async copies
 //     (eight lanes per 128-byte row segment; measured faster than TMA gather4
 //     for this pattern). Eight softmax warps (two per
 //     TMEM lane quarter, one per 128-key half) copy S out of TMEM at once
@@ -24,11 +24,15 @@
 //     2^8), and store P as bf16 straight into the O-CTA's shared memory
 //     (distributed shared memory), with the per-row rescale factor.
 //   O-CTA (rank 1): O += P V with TMEM O = [0, 512) (two N = 256 accumulator
-//     chains, one per half of the V dims). V rows are gathered by eleven
+//     chains, one per half of the V dims). V rows are gathered by ten
 //     warps of cp.async copies in 32-key stages (32 KB, 4-stage ring). Four
 //     correction warps apply the rare
 //     rescales to O between tiles and, at the end, normalise O and write the
 //     partial (o, lse).
+//
+// In both CTAs warp 0 only stages the tiles' pool rows (from the key list or
+// the page table), up to four tiles ahead of the copy warps, so that the
+// slot look-ups are off the copies' path.
 //
 // 16 warps: the producer and MMA warpgroups give registers to the softmax
 // warpgroups (setmaxnreg). Every wait is bounded; on a timeout a CTA drains
@@ -46,8 +50,9 @@ constexpr int kM = 128;
 constexpr int kNT = 256;          // keys per tile
 constexpr int kThreads = 512;     // 16 warps = 4 warpgroups
 constexpr int kWarpMMA = 4;
-constexpr int kSProd = 7;         // S-side producer warps: 0-3, 5-7
-constexpr int kOProd = 11;        // O-side producer warps: 0-3, 5-7, 12-15
+constexpr int kSProd = 6;         // S-side copy warps: 1-3, 5-7 (warp 0 stages the rows)
+constexpr int kOProd = 10;        // O-side copy warps: 1-3, 5-7, 12-15 (warp 0 stages the rows)
+constexpr int kRowsRing = 4;      // tiles of pool rows staged ahead of the copies
 // Register budget: launched at 128 per thread (512 x 128 = 65,536). S-CTA:
 // warpgroups 0-1 drop to 64, the two softmax warpgroups rise to 192
 // (256 x 64 + 256 x 192 = 65,536). O-CTA: warpgroups 0, 1, 3 drop to 64.
@@ -69,25 +74,25 @@ struct SmemS {
     unsigned char q_rope[kM * 128];            // [128 rows x 64 dims], 128B-swizzled
     unsigned char kring[kKStages][kKBlock];    // [256 keys x 64 dims] per stage
     uint32_t valid[kMetaRing][kNT / 32];
-    int32_t rows[2][kNT];                      // pool rows of the tiles being gathered
+    int32_t rows[kRowsRing][kNT];              // pool rows of the tiles being gathered
     float mx[2][2][kM];
     uint64_t anc[MLA_MAX_TREE];
     int32_t par[MLA_MAX_TREE];
     uint64_t k_full[kKStages], k_empty[kKStages];
     uint64_t meta_full[kMetaRing], meta_free[kMetaRing];
     uint64_t s_full, s_free, q_ready, mx_bar[2];
-    uint64_t rows_full[2], rows_free[2];
+    uint64_t rows_full[kRowsRing], rows_free[kRowsRing];
 };
 struct SmemO {
     unsigned char p[4 * kPBlock];              // [128 rows x 256 keys], 4 swizzled 64-key blocks
     unsigned char vring[kVStages][kVStage];    // [32 keys x 512 dims] per stage
-    int32_t rows[2][kNT];
+    int32_t rows[kRowsRing][kNT];
     float alpha[kM];
     float fin_m[kM];
     float fin_l[2][kM];
     uint64_t v_full[kVStages], v_empty[kVStages];
     uint64_t o_gate, o_prog;
-    uint64_t rows_full[2], rows_free[2];
+    uint64_t rows_full[kRowsRing], rows_free[kRowsRing];
 };
 // The header sits at the same offset in both CTAs: the S-CTA arrives on the
 // O-CTA's p_full / fin and the O-CTA on the S-CTA's p_free.
@@ -195,7 +200,7 @@ partial_pair_kernel(const PartialArgs a) {
             mbar_init(ba(S.q_ready), 256);
             mbar_init(ba(S.mx_bar[0]), 256);
             mbar_init(ba(S.mx_bar[1]), 256);
-            for (int i = 0; i < 2; ++i) {
+            for (int i = 0; i < kRowsRing; ++i) {
                 mbar_init(ba(S.rows_full[i]), 1);
                 mbar_init(ba(S.rows_free[i]), kSProd);
             }
@@ -207,7 +212,7 @@ partial_pair_kernel(const PartialArgs a) {
             }
             mbar_init(ba(O.o_gate), 128);
             mbar_init(ba(O.o_prog), 1);
-            for (int i = 0; i < 2; ++i) {
+            for (int i = 0; i < kRowsRing; ++i) {
                 mbar_init(ba(O.rows_full[i]), 1);
                 mbar_init(ba(O.rows_free[i]), kOProd);
             }
@@ -228,48 +233,45 @@ partial_pair_kernel(const PartialArgs a) {
     if (rank == 0 && wg < 2) {
         regs_dec<kRegsLow>();
         SmemS& S = sm.u.s;
-        if (warp != kWarpMMA) {
-            // ------------------------------------------------ S producers: K blocks
-            // Warp 0 stages each tile's pool rows (and the key-validity bits
-            // for the softmax); warps 0-3 and 5-7 split the 16-byte copies,
-            // eight lanes per 128-byte row segment.
-            const int pw = warp < kWarpMMA ? warp : warp - 1;  // 0..6
-            bool ok = true;
-            if (pw == 0) key_prefetch(a, b, kbase, Lb, kb + kNT, ke, lane);  // later tiles' slots
-            for (int i = 0; ok && i < ntiles; ++i) {
-                const int rb2 = i & 1;
-                if (pw == 0) {
-                    if (i >= 2 && !warp_wait(S.rows_free[rb2], ((i >> 1) - 1) & 1, abort_p)) {
-                        ok = false;
-                        break;
-                    }
-                    const int mi = i % kMetaRing;
-                    if (i >= kMetaRing && !warp_wait(S.meta_free[mi], ((i / kMetaRing) - 1) & 1, abort_p)) {
-                        ok = false;
-                        break;
-                    }
+        if (warp == 0) {
+            // ------------------------------------------------ S row stager
+            // Each tile's pool rows (and the key-validity bits for the
+            // softmax), up to kRowsRing tiles ahead of the copies.
+            key_prefetch(a, b, kbase, Lb, kb + kNT, ke, lane);  // later tiles' slots
+            for (int i = 0; i < ntiles; ++i) {
+                const int rb2 = i % kRowsRing, mi = i % kMetaRing;
+                if (i >= kRowsRing && !warp_wait(S.rows_free[rb2], ((i / kRowsRing) - 1) & 1, abort_p)) break;
+                if (i >= kMetaRing && !warp_wait(S.meta_free[mi], ((i / kMetaRing) - 1) & 1, abort_p)) break;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const int j = kb + i * kNT + 32 * q + lane;
-                        int32_t v = -1;
-                        if (j < ke) {
-                            v = key_slot(a, b, kbase, Lb, j);
-                            if (v < 0 || (int64_t)v >= a.pool_slots) {
-                                bad |= MLA_STATUS_BAD_SLOT;
-                                v = -1;
-                            }
+                for (int q = 0; q < 8; ++q) {
+                    const int j = kb + i * kNT + 32 * q + lane;
+                    int32_t v = -1;
+                    if (j < ke) {
+                        v = key_slot(a, b, kbase, Lb, j);
+                        if (v < 0 || (int64_t)v >= a.pool_slots) {
+                            bad |= MLA_STATUS_BAD_SLOT;
+                            v = -1;
                         }
-                        S.rows[rb2][32 * q + lane] = v;
-                        const uint32_t w = __ballot_sync(0xffffffffu, v >= 0);
-                        if (lane == q) S.valid[mi][q] = w;
                     }
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(ba(S.meta_full[mi]));
-                        mbar_arrive(ba(S.rows_full[rb2]));
-                    }
+                    S.rows[rb2][32 * q + lane] = v;
+                    const uint32_t w = __ballot_sync(0xffffffffu, v >= 0);
+                    if (lane == q) S.valid[mi][q] = w;
                 }
-                if (!warp_wait(S.rows_full[rb2], (i >> 1) & 1, abort_p)) {
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(ba(S.meta_full[mi]));
+                    mbar_arrive(ba(S.rows_full[rb2]));
+                }
+            }
+        } else if (warp != kWarpMMA) {
+            // ------------------------------------------------ S copy warps: K blocks
+            // Warps 1-3 and 5-7 split the 16-byte copies, eight lanes per
+            // 128-byte row segment.
+            const int pw = (warp < kWarpMMA ? warp : warp - 1) - 1;  // 0..5
+            bool ok = true;
+            for (int i = 0; ok && i < ntiles; ++i) {
+                const int rb2 = i % kRowsRing;
+                if (!warp_wait(S.rows_full[rb2], (i / kRowsRing) & 1, abort_p)) {
                     ok = false;
                     break;
                 }
@@ -534,34 +536,35 @@ partial_pair_kernel(const PartialArgs a) {
     } else if (wg != 2) {
         regs_dec<kRegsLow>();
         SmemO& O = sm.u.o;
-        if (warp != kWarpMMA) {
-            // ------------------------------------------------ O producers: V rows
-            // Warp 0 stages each tile's pool rows; warps 0-3, 5-7 and 12-15
-            // split the 16-byte copies (32 lanes = one half of a 1024-byte V row).
-            const int pw = warp < kWarpMMA ? warp : (warp < 8 ? warp - 1 : warp - 5);  // 0..10
+        if (warp == 0) {
+            // ------------------------------------------------ O row stager
+            // Each tile's pool rows, up to kRowsRing tiles ahead of the copies.
+            for (int i = 0; i < ntiles; ++i) {
+                const int rb2 = i % kRowsRing;
+                if (i >= kRowsRing && !warp_wait(O.rows_free[rb2], ((i / kRowsRing) - 1) & 1, abort_p)) break;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int j = kb + i * kNT + 32 * q + lane;
+                    int32_t v = -1;
+                    if (j < ke) {
+                        v = key_slot(a, b, kbase, Lb, j);
+                        if (v < 0 || (int64_t)v >= a.pool_slots) v = -1;
+                    }
+                    O.rows[rb2][32 * q + lane] = v;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ba(O.rows_full[rb2]));
+            }
+        } else if (warp != kWarpMMA) {
+            // ------------------------------------------------ O copy warps: V rows
+            // Warps 1-3, 5-7 and 12-15 split the 16-byte copies (32 lanes =
+            // one half of a 1024-byte V row).
+            const int pw = (warp < kWarpMMA ? warp : (warp < 8 ? warp - 1 : warp - 5)) - 1;  // 0..9
             bool ok = true;
             int g = 0;  // V stages so far (a tile takes only the stages holding its keys)
             for (int i = 0; ok && i < ntiles; ++i) {
-                const int rb2 = i & 1;
-                if (pw == 0) {
-                    if (i >= 2 && !warp_wait(O.rows_free[rb2], ((i >> 1) - 1) & 1, abort_p)) {
-                        ok = false;
-                        break;
-                    }
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const int j = kb + i * kNT + 32 * q + lane;
-                        int32_t v = -1;
-                        if (j < ke) {
-                            v = key_slot(a, b, kbase, Lb, j);
-                            if (v < 0 || (int64_t)v >= a.pool_slots) v = -1;
-                        }
-                        O.rows[rb2][32 * q + lane] = v;
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(ba(O.rows_full[rb2]));
-                }
-                if (!warp_wait(O.rows_full[rb2], (i >> 1) & 1, abort_p)) {
+                const int rb2 = i % kRowsRing;
+                if (!warp_wait(O.rows_full[rb2], (i / kRowsRing) & 1, abort_p)) {
                     ok = false;
                     break;
                 }
