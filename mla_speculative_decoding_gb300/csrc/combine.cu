@@ -7,7 +7,7 @@
 // splits with lse_s = -inf weighing 0.
 //
 // A block takes max(1, 4 / P) query rows with 64 * P threads per row (256
-// threads, 512 for P = 8): one warp per row first reads the row's split lse
+// threads; 512 for P = 8, 1024 for P = 16): one warp per row first reads the row's split lse
 // values (max and sum by warp shuffles) and lists the splits with non-zero
 // weight, in index order, in shared memory; then each of the row's P split
 // groups takes every P-th listed split, each thread 8 output dims (two
@@ -164,7 +164,10 @@ cudaError_t launch_combine(const float* lse_part, const float* o_part, int rows,
     if (live_hint <= 16)
         return launch_pdl(combine_kernel<4>, dim3(rows), dim3(256), 0, stream, lse_part, o_part, rows,
                           nsplit, out, lse, status);
-    return launch_pdl(combine_kernel<8>, dim3(rows), dim3(512), 0, stream, lse_part, o_part, rows,
+    if (live_hint <= 32)
+        return launch_pdl(combine_kernel<8>, dim3(rows), dim3(512), 0, stream, lse_part, o_part, rows,
+                          nsplit, out, lse, status);
+    return launch_pdl(combine_kernel<16>, dim3(rows), dim3(1024), 0, stream, lse_part, o_part, rows,
                       nsplit, out, lse, status);
 }
 
