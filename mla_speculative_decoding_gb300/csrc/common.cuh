@@ -256,11 +256,6 @@ __device__ __forceinline__ int64_t key_base(const PartialArgs& a, int b) {
     const int32_t r = a.req_pool_indices[b];
     return (r >= 0 && r < a.r2t_rows) ? (int64_t)r * a.r2t_stride : 0;
 }
-// Pool slot of key j (0 <= j < K) of request b, given key_base and L_b.
-__device__ __forceinline__ int32_t key_slot(const PartialArgs& a, int b, int64_t base, int Lb, int j) {
-    if (a.kv_indices != nullptr) return __ldg(a.kv_indices + base + j);
-    return j < Lb ? __ldg(a.req_to_token + base + j) : __ldg(a.out_cache_loc + (int64_t)b * a.T + (j - Lb));
-}
 
 // Warms L2 with the slot entries of keys [j0, j1) of request b, one 128-byte
 // line (32 entries) per lane step, so that the row staging of the tiles to
@@ -274,6 +269,63 @@ __device__ __forceinline__ void key_prefetch(const PartialArgs& a, int b, int64_
                                     : a.out_cache_loc + (int64_t)b * a.T + (j - Lb);
         asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
     }
+}
+
+// Pool rows of one tile of kTile keys starting at key j0 (and, for the
+// softmax, their validity bits).
+// Returns MLA_STATUS_BAD_SLOT if a slot was out of range (that key is masked).
+// The source is chosen once per tile (one base for all the lanes' loads, as for
+// the combined list): the table row while the tile is in the prefix, the
+// draft slots after it; the one tile that straddles L_b takes its draft
+// keys in a second pass.
+template <int kTile>
+__device__ __forceinline__ int stage_rows(const PartialArgs& a, int b, int64_t kbase, int Lb, int j0,
+                                          int ke, int lane, int32_t* rows, uint32_t* valid) {
+    int bad = 0;
+    constexpr int kQ = kTile / 32;
+    int32_t v[kQ];
+    const bool paged = a.kv_indices == nullptr;
+    const int32_t* src;
+    int lim = ke;
+    if (!paged) {
+        src = a.kv_indices + kbase;
+    } else if (j0 < Lb) {
+        src = a.req_to_token + kbase;
+        lim = min(ke, Lb);
+    } else {
+        src = a.out_cache_loc + ((int64_t)b * a.T - Lb);
+    }
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {  // all the loads in flight together
+        const int j = j0 + 32 * q + lane;
+        v[q] = j < lim ? __ldg(src + j) : -1;
+    }
+    if (paged && j0 < Lb && j0 + kTile > Lb) {  // through shared memory: each lane its own entries
+        const int32_t* dsrc = a.out_cache_loc + ((int64_t)b * a.T - Lb);
+#pragma unroll
+        for (int q = 0; q < kQ; ++q) rows[32 * q + lane] = v[q];
+#pragma unroll 1
+        for (int q = 0; q < kQ; ++q) {
+            const int j = j0 + 32 * q + lane;
+            if (j >= Lb && j < ke) rows[32 * q + lane] = __ldg(dsrc + j);
+        }
+#pragma unroll
+        for (int q = 0; q < kQ; ++q) v[q] = rows[32 * q + lane];
+    }
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {
+        if (v[q] < -1 || (v[q] >= 0 && (int64_t)v[q] >= a.pool_slots) ||
+            (v[q] == -1 && j0 + 32 * q + lane < ke)) {
+            bad |= MLA_STATUS_BAD_SLOT;
+            v[q] = -1;
+        }
+        rows[32 * q + lane] = v[q];
+        if (valid != nullptr) {
+            const uint32_t w = __ballot_sync(0xffffffffu, v[q] >= 0);
+            if (lane == q) valid[q] = w;
+        }
+    }
+    return bad;
 }
 
 // Host-side checks of mla_verify_attention's arguments (api.cu); the

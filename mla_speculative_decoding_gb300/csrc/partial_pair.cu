@@ -242,21 +242,7 @@ partial_pair_kernel(const PartialArgs a) {
                 const int rb2 = i % kRowsRing, mi = i % kMetaRing;
                 if (i >= kRowsRing && !warp_wait(S.rows_free[rb2], ((i / kRowsRing) - 1) & 1, abort_p)) break;
                 if (i >= kMetaRing && !warp_wait(S.meta_free[mi], ((i / kMetaRing) - 1) & 1, abort_p)) break;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int j = kb + i * kNT + 32 * q + lane;
-                    int32_t v = -1;
-                    if (j < ke) {
-                        v = key_slot(a, b, kbase, Lb, j);
-                        if (v < 0 || (int64_t)v >= a.pool_slots) {
-                            bad |= MLA_STATUS_BAD_SLOT;
-                            v = -1;
-                        }
-                    }
-                    S.rows[rb2][32 * q + lane] = v;
-                    const uint32_t w = __ballot_sync(0xffffffffu, v >= 0);
-                    if (lane == q) S.valid[mi][q] = w;
-                }
+                bad |= stage_rows<kNT>(a, b, kbase, Lb, kb + i * kNT, ke, lane, S.rows[rb2], S.valid[mi]);
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(ba(S.meta_full[mi]));
@@ -542,16 +528,7 @@ partial_pair_kernel(const PartialArgs a) {
             for (int i = 0; i < ntiles; ++i) {
                 const int rb2 = i % kRowsRing;
                 if (i >= kRowsRing && !warp_wait(O.rows_free[rb2], ((i / kRowsRing) - 1) & 1, abort_p)) break;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int j = kb + i * kNT + 32 * q + lane;
-                    int32_t v = -1;
-                    if (j < ke) {
-                        v = key_slot(a, b, kbase, Lb, j);
-                        if (v < 0 || (int64_t)v >= a.pool_slots) v = -1;
-                    }
-                    O.rows[rb2][32 * q + lane] = v;
-                }
+                (void)stage_rows<kNT>(a, b, kbase, Lb, kb + i * kNT, ke, lane, O.rows[rb2], nullptr);  // the S-CTA reports
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ba(O.rows_full[rb2]));
             }

@@ -165,60 +165,6 @@ __device__ __forceinline__ bool warp_wait_cluster(const uint64_t& bar, uint32_t 
     return __all_sync(0xffffffffu, ok);
 }
 
-// Pool rows of one 256-key tile (and, for the softmax, their validity bits).
-// Returns MLA_STATUS_BAD_SLOT if a slot was out of range (that key is masked).
-// The source is chosen once per tile (one base for all eight loads, as for
-// the combined list): the table row while the tile is in the prefix, the
-// draft slots after it; the one tile that straddles L_b takes its draft
-// keys in a second pass.
-__device__ __forceinline__ int stage_rows(const PartialArgs& a, int b, int64_t kbase, int Lb, int j0,
-                                          int ke, int lane, int32_t* rows, uint32_t* valid) {
-    int bad = 0;
-    int32_t v[8];
-    const bool paged = a.kv_indices == nullptr;
-    const int32_t* src;
-    int lim = ke;
-    if (!paged) {
-        src = a.kv_indices + kbase;
-    } else if (j0 < Lb) {
-        src = a.req_to_token + kbase;
-        lim = min(ke, Lb);
-    } else {
-        src = a.out_cache_loc + ((int64_t)b * a.T - Lb);
-    }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {  // all eight loads in flight together
-        const int j = j0 + 32 * q + lane;
-        v[q] = j < lim ? __ldg(src + j) : -1;
-    }
-    if (paged && j0 < Lb && j0 + kNT > Lb) {  // through shared memory: each lane its own entries
-        const int32_t* dsrc = a.out_cache_loc + ((int64_t)b * a.T - Lb);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) rows[32 * q + lane] = v[q];
-#pragma unroll 1
-        for (int q = 0; q < 8; ++q) {
-            const int j = j0 + 32 * q + lane;
-            if (j >= Lb && j < ke) rows[32 * q + lane] = __ldg(dsrc + j);
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = rows[32 * q + lane];
-    }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        if (v[q] < -1 || (v[q] >= 0 && (int64_t)v[q] >= a.pool_slots) ||
-            (v[q] == -1 && j0 + 32 * q + lane < ke)) {
-            bad |= MLA_STATUS_BAD_SLOT;
-            v[q] = -1;
-        }
-        rows[32 * q + lane] = v[q];
-        if (valid != nullptr) {
-            const uint32_t w = __ballot_sync(0xffffffffu, v[q] >= 0);
-            if (lane == q) valid[q] = w;
-        }
-    }
-    return bad;
-}
-
 // One work item of a cluster's sequence: request b, partition s and row
 // block rb, with its key range [kb, ke) in ntiles tiles.
 struct QuadItem {
@@ -549,7 +495,7 @@ partial_quad_kernel(const PartialArgs a) {
                 const int rs = j % kRowsRing, mi = j % kMetaRing;
                 if (j >= kMetaRing && !warp_wait(S.meta_free[mi], ((j / kMetaRing) - 1) & 1, abort_p))
                     return -1;
-                bad |= stage_rows(a, cur.b, key_base(a, cur.b), cur.Lb, cur.kb + cur.i * kNT, cur.ke, lane,
+                bad |= stage_rows<kNT>(a, cur.b, key_base(a, cur.b), cur.Lb, cur.kb + cur.i * kNT, cur.ke, lane,
                                   S.rows[rs], S.valid[mi]);
                 __syncwarp();
                 if (lane == 0) {
@@ -957,7 +903,7 @@ partial_quad_kernel(const PartialArgs a) {
                 const int rs = j % kRowsRing;
                 if (j >= kRowsRing && !warp_wait(O.rows_free[rs], ((j / kRowsRing) - 1) & 1, abort_p))
                     return -1;
-                (void)stage_rows(a, cur.b, key_base(a, cur.b), cur.Lb, cur.kb + cur.i * kNT, cur.ke, lane,
+                (void)stage_rows<kNT>(a, cur.b, key_base(a, cur.b), cur.Lb, cur.kb + cur.i * kNT, cur.ke, lane,
                                  O.rows[rs], nullptr);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ba(O.rows_full[rs]));
