@@ -326,7 +326,8 @@ def graph_time(fn, flush, steps, dev, stream):
     torch.cuda.synchronize()
     with torch.cuda.graph(g):
         fn()
-    return statistics.median(time_steps(g.replay, flush, steps, 3, stream))
+    # the mean: CUDA events tick in ~2 us steps, which a median of a few replays keeps
+    return statistics.mean(time_steps(g.replay, flush, steps, 3, stream))
 
 
 def e2e_time(d, flush, steps, warmup, stream):
