@@ -88,6 +88,10 @@ CASES = [
     # walks several items of different requests, row blocks and lengths
     (6, 32, [1500, 0, 17, 4000, 260, 2500], 16, "random", 8),
     (2, 16, [20000, 100], 32, "random", 48),
+    # more two-SM (request, row block) pairs than one wave of 76 clusters
+    # holds: the wave-shaped split over several waves of partitions
+    (96, 8, [(37 * k) % 1500 for k in range(96)], 4, "random", 8),
+    (80, 4, [1200 + 13 * k for k in range(80)], 8, "random", 2),
 ]
 
 
