@@ -34,6 +34,15 @@
 // the page table), up to four tiles ahead of the copy warps, so that the
 // slot look-ups are off the copies' path.
 //
+// A partly filled tile (a partition's last) costs in proportion to its keys:
+// only their rows are gathered, the score MMAs use N = the keys rounded up
+// to 16, the V stages and P V steps stop at the last 16-key step, and a
+// softmax half or 64-key block without keys is skipped. The launcher picks
+// the partitions: when every (request, row block) pair of the launch can
+// have a cluster of one wave, min(nsplit, resident clusters / pairs) per
+// pair, all launched at once (split_range_one_wave); otherwise all nsplit,
+// with the wave-shaped split over several waves.
+//
 // 16 warps: the producer and MMA warpgroups give registers to the softmax
 // warpgroups (setmaxnreg). Every wait is bounded; on a timeout a CTA drains
 // its MMAs, frees TMEM, reaches the final cluster barrier and flags
