@@ -31,8 +31,10 @@
 //     per SM apply the rare rescales to O and write the partial (o, lse).
 //
 // Operand readiness across a pair: each CTA's copies land on its own
-// mbarrier; the odd CTA's MMA warp forwards each completed stage to the
-// even CTA's barrier with a remote arrive. MMA completion is committed to
+// mbarrier; one thread per CTA (the odd CTA's MMA warp, a spare warp of the
+// even CTA) waits for each landed stage, fences it for the tensor cores
+// (proxy fence) and arrives on the even CTA's ready barrier, which the MMA
+// issuer waits for, so no fence sits in the issue loop. MMA completion is committed to
 // the barriers of both CTAs of the pair (multicast). Barriers that only
 // signal completed work (landed copies, finished TMEM reads, completed
 // MMAs) use default (CTA-scope) arrive and wait semantics, which cost far
@@ -72,7 +74,8 @@ constexpr int kNh = 128;          // keys per S-CTA per tile
 constexpr int kThreads = 640;     // 20 warps = 5 warpgroups
 constexpr int kWarpMMA = 4;
 constexpr int kWarpCtl = 7;       // P sender (S CTAs) / P slot release (O pair)
-constexpr int kSProd = 10;        // S-side producer warps: 0-3, 5, 6, 16-19
+constexpr int kSProd = 8;         // S-side producer warps: 0-3, 5, 6, 16, 17
+constexpr int kWarpFwd = 18;      // rank 0: fences each landed K stage for the MMA issuer
 constexpr int kSGroup = 2;        // producer warps per K stage (stages go round-robin to groups)
 constexpr int kOProd = 14;        // O-side producer warps: 0-3, 5, 6, 12-19
 // Launched at 96 registers per thread (640 x 96 = 61,440). S CTAs:
@@ -110,6 +113,7 @@ struct SmemS {
     uint64_t anc[MLA_MAX_TREE];
     int32_t par[MLA_MAX_TREE];
     uint64_t k_full[kKStages], k_empty[kKStages];
+    uint64_t k_ready[kKStages];  // rank 0: both CTAs' stage landed and fenced (two forwarders)
     uint64_t meta_full[kMetaRing], meta_free[kMetaRing];
     uint64_t s_full, s_free, q_landed, q_ready, q_peer, mx_bar[2], pw_bar[2], pstage_free;
     uint64_t rows_full[kRowsRing];
@@ -368,8 +372,9 @@ partial_quad_kernel(const PartialArgs a) {
         if (sside) {
             SmemS& S = sm.u.s;
             for (int i = 0; i < kKStages; ++i) {
-                mbar_init(ba(S.k_full[i]), 32 * kSGroup + (rank == 0 ? 1 : 0));
+                mbar_init(ba(S.k_full[i]), 32 * kSGroup);
                 mbar_init(ba(S.k_empty[i]), 1);
+                mbar_init(ba(S.k_ready[i]), 2);
             }
             for (int i = 0; i < kMetaRing; ++i) {
                 mbar_init(ba(S.meta_full[i]), 1);
@@ -426,13 +431,13 @@ partial_quad_kernel(const PartialArgs a) {
     if (sside && wg != 2 && wg != 3) {
         regs_dec<kRegsLow>();
         SmemS& S = sm.u.s;
-        if (warp != kWarpMMA && warp != kWarpCtl) {
+        if ((warp < 8 && warp != kWarpMMA && warp != kWarpCtl) || warp == 16 || warp == 17) {
             // ------------------------------------------------ S producers: K blocks
-            // The ten producer warps form five groups of two; fill g of the
+            // The eight producer warps form four groups of two; fill g of the
             // cluster's sequence (this CTA's 128 keys x 64 dims of one tile)
-            // is copied by group g mod 5, eight lanes per 128-byte row
+            // is copied by group g mod 4, eight lanes per 128-byte row
             // segment, so that stages complete independently of one another.
-            const int pw = warp < kWarpMMA ? warp : (warp < 8 ? warp - 1 : warp - 10);  // 0..9
+            const int pw = warp < kWarpMMA ? warp : (warp < 8 ? warp - 1 : warp - 10);  // 0..7
             const int grp = pw / kSGroup, gw = pw % kSGroup;
             constexpr int kNGroups = kSProd / kSGroup;
             constexpr int kFills = kDqk / 64;  // per tile
@@ -540,7 +545,7 @@ partial_quad_kernel(const PartialArgs a) {
             }
             if (lane == 0) bulk_wait_all();
             bad |= cur.bad;
-        } else if (rank == 0) {
+        } else if (warp == kWarpMMA && rank == 0) {
             // ------------------------------------------------ S MMA issuer (pair)
             // The issue loop is kept free of per-MMA descriptor construction
             // and branches: a pair MMA takes about 128 cycles, and any work the
@@ -550,7 +555,7 @@ partial_quad_kernel(const PartialArgs a) {
                 const uint32_t dS = tbase + kColS;
                 const uint64_t kdesc0 = make_sdesc(smem_u32(S.kring[0]), 16, 1024, kSwizzle128B);
                 const uint64_t qrdesc = make_sdesc(smem_u32(S.q_rope), 16, 1024, kSwizzle128B);
-                const uint32_t kfull0 = ba(S.k_full[0]), kempty0 = ba(S.k_empty[0]);
+                const uint32_t kready0 = ba(S.k_ready[0]), kempty0 = ba(S.k_empty[0]);
                 int st = 0, jt = 0, ne = 0;  // ring stage, tiles and non-empty items so far
                 uint32_t ph = 0;
                 bool ok = true;
@@ -569,11 +574,12 @@ partial_quad_kernel(const PartialArgs a) {
                         tc_fence_after();
 #pragma unroll 1
                         for (int kbk = 0; kbk < kDqk / 64; ++kbk) {
-                            if (!mbar_wait_spin(kfull0 + 8 * st, ph, abort_p)) {
+                            // both CTAs' copies landed, each fenced for the
+                            // tensor cores by its forwarder
+                            if (!mbar_wait_spin(kready0 + 8 * st, ph, abort_p)) {
                                 ok = false;
                                 break;
                             }
-                            fence_proxy_async_smem();
                             tc_fence_after();
                             const uint64_t bd = kdesc0 + (uint64_t)(st * (kKBlock >> 4));
                             if (kbk < 8) {  // latent dims: A = Q from TMEM
@@ -601,7 +607,30 @@ partial_quad_kernel(const PartialArgs a) {
                 mma_commit_pair_mc(ba(sm.h.drain), 0x1);
                 mbar_wait(ba(sm.h.drain), 0, &sm.h.no_abort);
             }
-        } else {
+        } else if (warp == kWarpFwd && rank == 0) {
+            // ------------------------------------------------ rank 0: fence each landed stage
+            // Copies complete on this CTA's own barriers; this thread orders
+            // each filled stage for the tensor cores (proxy fence) and tells
+            // the MMA issuer, off the issuer's path.
+            if (lane == 0) {
+                int g = 0;
+                bool ok = true;
+                QuadItem it;
+                for (ItemWalk wk = walk_init(sm.h, cid, C); ok && walk_next(wk, a, sm.h, nrb, n_items, C, cid, it);) {
+                    if (it.ntiles <= 0) continue;
+                    const int gend = g + it.ntiles * (kDqk / 64);
+                    for (; ok && g < gend; ++g) {
+                        const int st = g % kKStages;
+                        if (!mbar_wait_spin(ba(S.k_full[st]), (g / kKStages) & 1, abort_p)) {
+                            ok = false;
+                            break;
+                        }
+                        fence_proxy_async_smem();
+                        mbar_arrive(ba(S.k_ready[st]));
+                    }
+                }
+            }
+        } else if (warp == kWarpMMA) {
             // ------------------------------------------------ rank 1: forward readiness to rank 0
             // Copies complete on this CTA's own barriers; rank 0's MMA issuer
             // learns of each filled K stage (and of this CTA's Q) through
@@ -624,7 +653,7 @@ partial_quad_kernel(const PartialArgs a) {
                             break;
                         }
                         fence_proxy_async_smem();
-                        mbar_arrive_remote(mapa_shared(ba(S.k_full[st]), 0));
+                        mbar_arrive_remote(mapa_shared(ba(S.k_ready[st]), 0));
                     }
                     ++ne;
                 }
